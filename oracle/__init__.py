@@ -1,0 +1,161 @@
+"""fp64 CPU oracle for the selective scan (S6) -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never loads it, and it loads nothing of theirs.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain C, double precision, one
+sequential recurrence per channel).  This module only compiles it with gcc on
+first use and marshals numpy arrays to it.  See ``ssm_oracle.c`` for the
+formulas and the passages of the pages they follow.
+
+Pin status: every function here is pinned by ``tests/test_oracle_pins.py``
+against closed forms, brute-force sums and limits that the pages fix.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_LIB = os.path.join(_HERE, "libssm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ssm_oracle.c into libssm_oracle.so next to it (gcc, -O2)."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        # -ffp-contract=off: no fused multiply-adds, so each product and sum
+        # rounds exactly as written in the C source.
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+               "-o", _LIB + ".tmp", _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_scan.argtypes = [P] * 11 + [I] * 6
+            lib.oracle_scan.restype = I
+            lib.oracle_state_update.argtypes = [P] * 10 + [I] * 4
+            lib.oracle_state_update.restype = I
+            _lib = lib
+    return _lib
+
+
+class _use_library:
+    """Temporarily route this module's calls to another build of the oracle
+    source (the mutation tests compile deliberately broken copies)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self.saved = _lib
+        lib = ctypes.CDLL(self.path)
+        lib.oracle_scan.argtypes = self.saved.oracle_scan.argtypes
+        lib.oracle_scan.restype = ctypes.c_int
+        lib.oracle_state_update.argtypes = self.saved.oracle_state_update.argtypes
+        lib.oracle_state_update.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def _f64(x, shape=None):
+    if x is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    if shape is not None and a.shape != tuple(shape):
+        raise ValueError(f"expected shape {tuple(shape)}, got {a.shape}")
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
+
+
+def scan(u, delta, A, B, C, z=None, Dskip=None, dt_bias=None, h0=None, *,
+         return_final_state=False, nthreads=None):
+    """Selective scan over whole sequences, in fp64.
+
+    u, delta, z: [batch, dim, L]; A: [dim, N]; B, C: [batch, G, N, L];
+    Dskip, dt_bias: [dim]; h0: [batch, dim, N].  Returns y [batch, dim, L]
+    (and h_final [batch, dim, N] when ``return_final_state``).
+    """
+    u = _f64(u)
+    if u.ndim != 3:
+        raise ValueError("u must be [batch, dim, L]")
+    batch, dim, L = u.shape
+    delta = _f64(delta, u.shape)
+    z = _f64(z, u.shape)
+    A = _f64(A)
+    if A.ndim != 2 or A.shape[0] != dim:
+        raise ValueError("A must be [dim, N]")
+    N = A.shape[1]
+    B = _f64(B)
+    if B.ndim != 4 or B.shape[0] != batch or B.shape[2:] != (N, L):
+        raise ValueError("B must be [batch, G, N, L]")
+    G = B.shape[1]
+    C = _f64(C, B.shape)
+    Dskip = _f64(Dskip, (dim,))
+    dt_bias = _f64(dt_bias, (dim,))
+    h0 = _f64(h0, (batch, dim, N))
+    y = np.empty((batch, dim, L), dtype=np.float64)
+    hf = np.empty((batch, dim, N), dtype=np.float64) if return_final_state else None
+    rc = _load().oracle_scan(_ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C),
+                             _ptr(Dskip), _ptr(dt_bias), _ptr(h0), _ptr(y), _ptr(hf),
+                             batch, dim, N, L, G, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_scan rejected its arguments (code {rc})")
+    return (y, hf) if return_final_state else y
+
+
+def state_update(state, u, delta, A, B, C, z=None, Dskip=None, dt_bias=None):
+    """One decode step in fp64.  Returns (new_state, y); the input is not modified.
+
+    state: [batch, dim, N]; u, delta, z: [batch, dim]; B, C: [batch, G, N].
+    """
+    st = np.array(state, dtype=np.float64, copy=True, order="C")
+    batch, dim, N = st.shape
+    u = _f64(u, (batch, dim))
+    delta = _f64(delta, (batch, dim))
+    z = _f64(z, (batch, dim))
+    A = _f64(A, (dim, N))
+    B = _f64(B)
+    if B.ndim != 3 or B.shape[0] != batch or B.shape[2] != N:
+        raise ValueError("B must be [batch, G, N]")
+    G = B.shape[1]
+    C = _f64(C, B.shape)
+    Dskip = _f64(Dskip, (dim,))
+    dt_bias = _f64(dt_bias, (dim,))
+    y = np.empty((batch, dim), dtype=np.float64)
+    rc = _load().oracle_state_update(_ptr(st), _ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B),
+                                     _ptr(C), _ptr(Dskip), _ptr(dt_bias), _ptr(y),
+                                     batch, dim, N, G)
+    if rc != 0:
+        raise ValueError(f"oracle_state_update rejected its arguments (code {rc})")
+    return st, y

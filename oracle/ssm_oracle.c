@@ -1,0 +1,188 @@
+/*
+ * ssm_oracle.c -- plain, slow, fp64 CPU oracle for the selective scan (S6).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: it exists so that tests, the smoke check and the CPU
+ * baseline leg of the benchmark can compare the CUDA library against an
+ * obviously correct sequential recurrence.  It shares no code, header,
+ * table or helper with the CUDA library.
+ *
+ * What it computes (the plain definition, written out):
+ *
+ *   Discretisation (intvml.com "DL0170 Mamba Selective SSM vs Attention",
+ *   Mathematical Formulation: zero-order-hold decay Abar = exp(Delta*A) for a
+ *   diagonal A, and the simplified input term Bbar = Delta*B used in place of
+ *   the exact zero-order-hold input matrix):
+ *       Delta_t   = softplus(delta_t + dt_bias[d])
+ *       Abar_t[n] = exp(Delta_t * A[d,n])
+ *       Bbar_t[n] * x_t = Delta_t * B_t[n] * u_t
+ *
+ *   Recurrence and readout (eightmm.github.io "Mamba", Main Claim and Scan
+ *   View; portpowered.github.io "Mamba Selective State-Space Module", Math Or
+ *   Compute Schema, "Selective state-space step"):
+ *       h_t = Abar_t * h_{t-1} + Bbar_t x_t        (elementwise over n)
+ *       y_t = sum_n C_t[n] * h_t[n]
+ *
+ *   Skip and gate: the pages say only that a gate path modulates the block
+ *   output (eightmm.github.io "Mamba", Block Structure).  The reading taken is
+ *       y_t = (sum_n C_t[n] h_t[n] + Dskip[d] * u_t) * silu(z_t),
+ *   with the gate dropped when z is NULL.
+ *
+ *   Initial condition: h_0 = 0 unless the caller passes h0 (intvml.com, where
+ *   the formulation names a required initial condition whose value was lost).
+ *
+ *   Decode (cuishuaiwen.com "Mamba & State-Space Sequence Models", Core
+ *   mechanics: inference runs the recurrence one token at a time with a state
+ *   of constant size): the same body for a single t, with h read from and
+ *   written back to the caller's state.
+ *
+ * Layouts (all row-major, contiguous, last index fastest):
+ *   u, delta, z, y : [batch, dim, seqlen]
+ *   A              : [dim, dstate]
+ *   B, C           : [batch, ngroups, dstate, seqlen]   (decode: [batch, ngroups, dstate])
+ *   Dskip, dt_bias : [dim]
+ *   h0, h_final, state : [batch, dim, dstate]
+ *   channel d reads group g = d / (dim / ngroups).
+ *
+ * Everything is double precision; inputs that the GPU sees as bf16 or fp32
+ * arrive here widened exactly.  softplus has no threshold: it is evaluated as
+ * max(x, 0) + log1p(exp(-|x|)).
+ *
+ * Parallelism: (batch, channel) pairs are split over POSIX threads; each
+ * channel remains one sequential loop over time.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stddef.h>
+#include <stdlib.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+
+static double softplus(double x) {
+    return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+}
+
+static double silu(double z) {
+    return z / (1.0 + exp(-z));
+}
+
+typedef struct {
+    const double *u, *delta, *z, *A, *B, *C, *Dskip, *dt_bias, *h0;
+    double *y, *h_final;
+    int batch, dim, dstate, seqlen, ngroups;
+    long first, last; /* range of flattened (b, d) handled by one worker */
+} scan_job;
+
+/* One channel: the sequential recurrence over time, state in a local array. */
+static void scan_channel(const scan_job *J, int b, int d, double *h) {
+    const int N = J->dstate, L = J->seqlen;
+    const int g = d / (J->dim / J->ngroups);
+    const size_t row = ((size_t)b * J->dim + d) * (size_t)L;
+    const size_t bc = ((size_t)b * J->ngroups + g) * (size_t)N * (size_t)L;
+    const double dskip = J->Dskip ? J->Dskip[d] : 0.0;
+    const double bias = J->dt_bias ? J->dt_bias[d] : 0.0;
+
+    for (int n = 0; n < N; n++)
+        h[n] = J->h0 ? J->h0[((size_t)b * J->dim + d) * N + n] : 0.0;
+
+    for (int t = 0; t < L; t++) {
+        const double ut = J->u[row + t];
+        const double dt = softplus(J->delta[row + t] + bias);
+        double acc = 0.0;
+        for (int n = 0; n < N; n++) {
+            const double abar = exp(dt * J->A[(size_t)d * N + n]);
+            const double bx = dt * J->B[bc + (size_t)n * L + t] * ut;
+            h[n] = abar * h[n] + bx;
+            acc += J->C[bc + (size_t)n * L + t] * h[n];
+        }
+        double yt = acc + dskip * ut;
+        if (J->z) yt *= silu(J->z[row + t]);
+        J->y[row + t] = yt;
+    }
+    if (J->h_final)
+        for (int n = 0; n < N; n++)
+            J->h_final[((size_t)b * J->dim + d) * N + n] = h[n];
+}
+
+static void *scan_worker(void *arg) {
+    const scan_job *J = (const scan_job *)arg;
+    double *h = (double *)malloc(sizeof(double) * (size_t)J->dstate);
+    if (!h) return NULL;
+    for (long i = J->first; i < J->last; i++)
+        scan_channel(J, (int)(i / J->dim), (int)(i % J->dim), h);
+    free(h);
+    return NULL;
+}
+
+static int check_dims(int batch, int dim, int dstate, int seqlen, int ngroups) {
+    if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || ngroups <= 0) return 0;
+    if (dim % ngroups != 0) return 0;
+    return 1;
+}
+
+/* Selective scan over a whole sequence.  z, Dskip, dt_bias, h0 and h_final
+ * may be NULL.  Returns ORACLE_OK or ORACLE_BAD_ARG. */
+int oracle_scan(const double *u, const double *delta, const double *z,
+                const double *A, const double *B, const double *C,
+                const double *Dskip, const double *dt_bias, const double *h0,
+                double *y, double *h_final,
+                int batch, int dim, int dstate, int seqlen, int ngroups,
+                int nthreads) {
+    if (!check_dims(batch, dim, dstate, seqlen, ngroups)) return ORACLE_BAD_ARG;
+    if (!u || !delta || !A || !B || !C || !y) return ORACLE_BAD_ARG;
+    const long total = (long)batch * dim;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > total) nthreads = (int)total;
+
+    scan_job *jobs = (scan_job *)malloc(sizeof(scan_job) * (size_t)nthreads);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!jobs || !tid) { free(jobs); free(tid); return ORACLE_BAD_ARG; }
+    for (int k = 0; k < nthreads; k++) {
+        scan_job J = {u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final,
+                      batch, dim, dstate, seqlen, ngroups,
+                      total * k / nthreads, total * (k + 1) / nthreads};
+        jobs[k] = J;
+    }
+    if (nthreads == 1) {
+        scan_worker(&jobs[0]);
+    } else {
+        for (int k = 0; k < nthreads; k++) pthread_create(&tid[k], NULL, scan_worker, &jobs[k]);
+        for (int k = 0; k < nthreads; k++) pthread_join(tid[k], NULL);
+    }
+    free(jobs);
+    free(tid);
+    return ORACLE_OK;
+}
+
+/* One decode step: state[b,d,:] is read, advanced by one token and written
+ * back; y[b,d] receives the gated readout.  Token tensors are u, delta, z:
+ * [batch, dim]; B, C: [batch, ngroups, dstate]. */
+int oracle_state_update(double *state, const double *u, const double *delta,
+                        const double *z, const double *A, const double *B,
+                        const double *C, const double *Dskip,
+                        const double *dt_bias, double *y,
+                        int batch, int dim, int dstate, int ngroups) {
+    if (!check_dims(batch, dim, dstate, 1, ngroups)) return ORACLE_BAD_ARG;
+    if (!state || !u || !delta || !A || !B || !C || !y) return ORACLE_BAD_ARG;
+    const int N = dstate;
+    for (int b = 0; b < batch; b++) {
+        for (int d = 0; d < dim; d++) {
+            const int g = d / (dim / ngroups);
+            const size_t bd = (size_t)b * dim + d;
+            const size_t bc = ((size_t)b * ngroups + g) * (size_t)N;
+            const double ut = u[bd];
+            const double dt = softplus(delta[bd] + (dt_bias ? dt_bias[d] : 0.0));
+            double acc = 0.0;
+            for (int n = 0; n < N; n++) {
+                double *h = &state[bd * N + n];
+                *h = exp(dt * A[(size_t)d * N + n]) * (*h) + dt * B[bc + n] * ut;
+                acc += C[bc + n] * (*h);
+            }
+            double yt = acc + (Dskip ? Dskip[d] : 0.0) * ut;
+            if (z) yt *= silu(z[bd]);
+            y[bd] = yt;
+        }
+    }
+    return ORACLE_OK;
+}

@@ -1,0 +1,66 @@
+"""The pins must be able to fail: each mutant below is the oracle source with
+one plausible slip planted in it (compiled here, on the CPU).  For every
+mutant at least one pin of tests/test_oracle_pins.py has to raise."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
+
+MUTANTS = {
+    "skip_term_dropped": ("double yt = acc + dskip * ut;", "double yt = acc;"),
+    "bias_after_softplus": ("softplus(J->delta[row + t] + bias)", "(softplus(J->delta[row + t]) + bias)"),
+    "decay_sign_flipped": ("exp(dt * J->A[(size_t)d * N + n])", "exp(-dt * J->A[(size_t)d * N + n])"),
+    "readout_uses_B": ("acc += J->C[bc + (size_t)n * L + t] * h[n];", "acc += J->B[bc + (size_t)n * L + t] * h[n];"),
+    "readout_before_update": (
+        "h[n] = abar * h[n] + bx;\n            acc += J->C[bc + (size_t)n * L + t] * h[n];",
+        "acc += J->C[bc + (size_t)n * L + t] * h[n];\n            h[n] = abar * h[n] + bx;"),
+    "gate_skips_the_skip_path": ("if (J->z) yt *= silu(J->z[row + t]);",
+                                 "if (J->z) yt = acc * silu(J->z[row + t]) + dskip * ut;"),
+    "h0_ignored": ("h[n] = J->h0 ? J->h0[((size_t)b * J->dim + d) * N + n] : 0.0;", "h[n] = 0.0;"),
+    "group_index_interleaved": ("const int g = d / (J->dim / J->ngroups);\n    const size_t row",
+                                "const int g = d % J->ngroups;\n    const size_t row"),
+    "B_one_step_late": ("const double bx = dt * J->B[bc + (size_t)n * L + t] * ut;",
+                        "const double bx = dt * J->B[bc + (size_t)n * L + (t > 0 ? t - 1 : 0)] * ut;"),
+    "softplus_without_abs": ("log1p(exp(-fabs(x)))", "log1p(exp(-x))"),
+    "input_term_without_step": ("const double bx = dt * J->B[", "const double bx = J->B["),
+    "decode_gate_dropped": ("if (z) yt *= silu(z[bd]);", ""),
+}
+
+PIN_TESTS = [
+    lambda: pins.test_hand_worked_golden_cases(),
+    lambda: pins.test_single_step_closed_form(False),
+    lambda: pins.test_single_step_closed_form(True),
+    lambda: pins.test_geometric_series_n1_constant_inputs(),
+    lambda: pins.test_matches_causal_matrix_mixer(True, True),
+    lambda: pins.test_groups_read_their_own_B_C(),
+    lambda: pins.test_time_invariant_case_is_a_convolution(),
+    lambda: pins.test_vanishing_step_leaves_only_skip_path(),
+    lambda: pins.test_large_step_overwrites_state(),
+    lambda: pins.test_decode_steps_equal_one_scan(),
+    lambda: pins.test_decode_single_step_from_zero_state(),
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-o",
+                    str(lib), str(mutated), "-lm"], check=True)
+    failures = 0
+    with oracle._use_library(str(lib)):
+        for pin in PIN_TESTS:
+            try:
+                pin()
+            except AssertionError:
+                failures += 1
+    assert failures > 0, f"no pin caught mutant {name}"
