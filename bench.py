@@ -1,0 +1,580 @@
+#!/usr/bin/env python
+"""Benchmark of the B300 selective scan (S6).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one forward selective scan (fused discretisation, recurrence,
+readout, skip and gate) over one batch of the headline workload: bf16 I/O,
+fp32 state, batch 2, 1536 channels, N 16, L 2048, G 1.  Rank 0 prints one
+JSON line.  `value` is the whole-job rate of compulsory bytes (u, delta, z, y
+plus B, C) per second, device-timed with CUDA events around a CUDA graph of K
+launches over rotating input sets that together exceed 3x the L2 cache.  The
+same line carries the end-to-end rate through the public API with host
+buffers, the decode-step rate (tokens/s), the roofline of the scan kernel and
+the fp64 CPU oracle timed on this host as a baseline.
+
+--impl reference times the fp64 CPU oracle instead (the reference arm: no
+GPU code exists on the pages), on a bounded sample of the same workload.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+batches (weak scaling, no data-path collective); the time is the max over
+ranks and `value` sums the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "scan_bf16_b2_d1536_l2048"
+DECODE = "decode_b256_d5120"
+METRIC = "selective-scan fwd GB/s and % of B300 HBM roofline; decode tokens/s"
+FALLBACK_HBM_GBS = 6400.0
+# Measured on this B300 (probe of MUFU.EX2 and FFMA/FFMA2 issue): 32 ex2 and
+# 128 fp32 lane-ops per SM per clock.  One state update (b, d, l, n) needs one
+# ex2 and four fp32 ops (Delta*A, Delta*u*B, the FMA of the recurrence, the FMA
+# of the readout): 32 updates per SM per clock from either pipe.
+UPDATES_PER_SM_CLK = 32.0
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host-side; tested with gloo on CPU)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        sm, mx, reasons, power = [], None, set(), []
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"], parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "sm_max_mhz": 2032.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_109_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def n_rotating_sets(bytes_per_set: int, l2_bytes: int) -> int:
+    return max(2, math.ceil(3 * l2_bytes / max(1, bytes_per_set)))
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def bench_scan_device(ssm, I, torch, w, steps, warmup, sampler=None, preroll_s=1.0):
+    """Device-timed forward scan over rotating input sets (> 3x L2)."""
+    dev = torch.device("cuda")
+    props = torch.cuda.get_device_properties(dev)
+    nbytes = I.compulsory_bytes_scan(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], w["io"])
+    nsets = n_rotating_sets(nbytes, props.L2_cache_size)
+    sets = [I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                               recipe=w["recipe"], seed=s, device=dev) for s in range(nsets)]
+    outs = [torch.empty_like(x.u) for x in sets]
+    final = w.get("final_state", False)
+    hfs = [torch.empty((w["batch"], w["dim"], w["dstate"]), dtype=torch.float32, device=dev)
+           for _ in range(nsets)] if final else None
+    ws = None
+    if final:
+        need = ssm.chunked_workspace_size(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"],
+                                          sets[0].u.dtype)
+        ws = [ssm.alloc_workspace(need, dev) for _ in range(nsets)]
+
+    def launch(i):
+        x = sets[i]
+        if final:
+            ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias,
+                                 out=outs[i], h_final=hfs[i], workspace=ws[i])
+        else:
+            ssm.scan_fwd(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias, out=outs[i])
+
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(stream):
+        for i in range(nsets):
+            launch(i)  # eager warm-up (also loads the module)
+    torch.cuda.synchronize(dev)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                launch(i % nsets)
+        return g
+
+    full = capture(nsets)
+    rem = steps % nsets
+    part = capture(rem) if rem else None
+    for _ in range(max(1, math.ceil(warmup / nsets))):
+        full.replay()
+    torch.cuda.synchronize(dev)
+    t_pre = time.time()
+    if preroll_s > 0:  # keeps the GPU busy while the clock sampler settles
+        while time.time() - t_pre < preroll_s:
+            full.replay()
+            torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // nsets):
+            full.replay()
+        if part is not None:
+            part.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    ms = e0.elapsed_time(e1)
+    return dict(ms_total=ms, ms_per_launch=ms / steps, bytes_per_step=nbytes, nsets=nsets,
+                t_window=(t_pre, t_end), upd_per_step=w["batch"] * w["dim"] * w["seqlen"] * w["dstate"],
+                bdl_per_step=w["batch"] * w["dim"] * w["seqlen"])
+
+
+def bench_scan_e2e(ssm, I, torch, w, steps, warmup):
+    """End to end through the public API: pinned host inputs -> device -> scan -> host y."""
+    dev = torch.device("cuda")
+    x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                           recipe=w["recipe"], seed=100, device="cpu")
+    names = ["u", "delta", "z", "B", "C"]
+    host = {n: getattr(x, n).pin_memory() for n in names}
+    devt = {n: torch.empty_like(host[n], device=dev) for n in names}
+    params = {n: getattr(x, n).to(dev) for n in ["A", "D", "dt_bias"]}
+    y_dev = torch.empty_like(devt["u"])
+    y_host = torch.empty_like(host["u"]).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_host.numel() * y_host.element_size()
+
+    def step():
+        for n in names:
+            devt[n].copy_(host[n], non_blocking=True)
+        ssm.scan_fwd(devt["u"], devt["delta"], params["A"], devt["B"], devt["C"], z=devt["z"],
+                     D=params["D"], dt_bias=params["dt_bias"], out=y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    return dict(ms_per_step=ms / steps, h2d=h2d, d2h=d2h)
+
+
+def bench_decode_device(ssm, I, torch, w, steps, warmup):
+    """Decode step on the full batch; states rotate so the 80 MiB state is
+    read from HBM each step (cold); also a warm figure on one state."""
+    dev = torch.device("cuda")
+    props = torch.cuda.get_device_properties(dev)
+    b, d, n = w["batch"], w["dim"], w["dstate"]
+    per = I.compulsory_bytes_decode(b, d, n)
+    nsets = n_rotating_sets(per, props.L2_cache_size)
+    prm = I.decode_params(d, n, recipe=w["recipe"], seed=0, device=dev)
+    states = [I.make_decode_state(b, d, n, seed=s, device=dev) for s in range(nsets)]
+    toks = [I.make_decode_token(b, d, n, s, io=w["io"], recipe=w["recipe"], seed=0, device=dev)
+            for s in range(nsets)]
+    ys = [torch.empty((b, d), dtype=toks[0]["u"].dtype, device=dev) for _ in range(nsets)]
+
+    def launch(i, k):
+        t = toks[k]
+        ssm.state_update(states[i], t["u"], t["delta"], prm["A"], t["B"], t["C"], z=t["z"],
+                         D=prm["D"], dt_bias=prm["dt_bias"], out=ys[k])
+
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    res = {}
+    for mode in ("cold", "warm"):
+        with torch.cuda.stream(stream):
+            for i in range(nsets):
+                launch(i if mode == "cold" else 0, i)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsets):
+                launch(i if mode == "cold" else 0, i)
+        reps = max(1, steps // nsets)
+        for _ in range(max(1, math.ceil(warmup / nsets))):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / (reps * nsets)
+        res[mode] = dict(us_per_step=ms * 1e3, tokens_per_s=b / (ms * 1e-3),
+                         state_gbs=per / (ms * 1e-3) / 1e9, launches=reps * nsets)
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_baseline(I, w, budget_s=10.0):
+    import oracle
+    x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                           recipe=w["recipe"], seed=0, device="cpu").as_f64()
+    threads = oracle.default_threads()
+    nbytes = I.compulsory_bytes_scan(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], w["io"])
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.scan(**x, nthreads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = reps * nbytes / el / 1e9
+    return dict(value=gbs, unit="GB/s", cores=threads, kind="oracle",
+                sample=f"{reps} full passes of the {HEADLINE} workload (fp64 C oracle, "
+                       f"{threads} threads over channels) in {el:.1f} s",
+                seconds=el, passes=reps)
+
+
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    from selective_state_space_109_b300 import inputs as I
+    from selective_state_space_109_b300 import ssm
+
+    w = I.WORKLOADS[HEADLINE]
+    peaks, peak_src = measured_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    r = bench_scan_device(ssm, I, torch, w, args.steps, args.warmup)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    sampler.stop()
+    clocks = sampler.summary(*r["t_window"])
+    ms_total = max_over_ranks(r["ms_total"], world, dev)
+    total_bytes = sum_over_ranks(r["bytes_per_step"] * args.steps, world, dev)
+    value = total_bytes / (ms_total * 1e-3) / 1e9
+    per_launch_s = r["ms_per_launch"] * 1e-3
+    achieved = r["bytes_per_step"] / per_launch_s / 1e9
+
+    e2e = bench_scan_e2e(ssm, I, torch, w, max(3, min(args.steps, 50)), 3)
+    e2e_ms = max_over_ranks(e2e["ms_per_step"], world, dev)
+    e2e_value = sum_over_ranks(r["bytes_per_step"], world, dev) / (e2e_ms * 1e-3) / 1e9
+
+    dec = None
+    if not args.skip_decode:
+        dec = bench_decode_device(ssm, I, torch, I.WORKLOADS[DECODE], max(args.steps, 64), args.warmup)
+
+    extra = {}
+    if not args.skip_extra and world == 1:
+        for name in ("scan_bf16_b8_d2048_l4096", "scan_bf16_b1_d5120_l65536_final_state"):
+            wx = I.WORKLOADS[name]
+            rx = bench_scan_device(ssm, I, torch, wx, max(4, min(args.steps, 40)), 3, preroll_s=0.0)
+            extra[name] = dict(GBps=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3) / 1e9, 1),
+                               us_per_launch=round(rx["ms_per_launch"] * 1e3, 2),
+                               frac_of_hbm_measured=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3)
+                                                          / 1e9 / peaks["hbm_gbs"], 4))
+
+    base = None
+    if rank == 0 and world == 1 and not args.skip_cpu_baseline:
+        base = oracle_baseline(I, w, budget_s=args.cpu_seconds)
+
+    if rank != 0:
+        return
+    sm_max = peaks.get("sm_max_mhz", 2032.0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = sms * sm_max * 1e6 * UPDATES_PER_SM_CLK / 1e9  # Gupd/s
+    alu_achieved = r["upd_per_step"] / per_launch_s / 1e9
+    traffic = ncu_traffic("scan_fwd_kernel/" + HEADLINE)
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "batch": w["batch"], "dim": w["dim"], "dstate": w["dstate"],
+                   "seqlen": w["seqlen"], "ngroups": w["ngroups"], "io": "bf16", "state": "f32",
+                   "recipe": w["recipe"], "l2": f"inputs larger than L2: {r['nsets']} rotating input sets "
+                                                f"({r['nsets'] * r['bytes_per_step'] / 1e6:.0f} MB)",
+                   "timing": "CUDA events around a CUDA graph of the K launches",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "frac_of_hbm": round(value / world / peaks["hbm_gbs"], 4),
+        "tokens_channels_per_s": round(r["bdl_per_step"] / per_launch_s, 1),
+        "roofline": {"bound": "alu", "achieved": round(alu_achieved, 1), "peak": round(alu_peak, 1),
+                     "unit": "Gupd/s", "frac": round(alu_achieved / alu_peak, 4), "traffic": traffic,
+                     "kernel": "scan_fwd_kernel",
+                     "peak_basis": f"{sms} SMs x {sm_max:.0f} MHz x 32 state updates/SM/clk "
+                                   "(MUFU.EX2 32/clk; FP32 128 lane-ops/clk at 4 per update)"},
+        "hbm_roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "peak_source": peak_src, "traffic": traffic},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if dec is not None:
+        out["decode"] = {"workload": DECODE, "tokens_per_s": round(dec["cold"]["tokens_per_s"], 1),
+                         "us_per_step": round(dec["cold"]["us_per_step"], 3),
+                         "state_GBps": round(dec["cold"]["state_gbs"], 1),
+                         "frac_of_hbm": round(dec["cold"]["state_gbs"] / peaks["hbm_gbs"], 4),
+                         "warm_l2_us_per_step": round(dec["warm"]["us_per_step"], 3),
+                         "warm_l2_tokens_per_s": round(dec["warm"]["tokens_per_s"], 1)}
+    if extra:
+        out["other_workloads"] = extra
+    if base is not None:
+        out["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        out["cpu_baseline"]["value"] = round(base["value"], 3)
+    print(json.dumps(out), flush=True)
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from selective_state_space_109_b300 import inputs as I
+    w = I.WORKLOADS[HEADLINE]
+    import oracle
+    x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                           recipe=w["recipe"], seed=0, device="cpu").as_f64()
+    threads = oracle.default_threads()
+    nbytes = I.compulsory_bytes_scan(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], w["io"])
+    # Each step: the oracle over a bounded sample (a slice of channels) of the
+    # workload, sized so K + W steps end within a few minutes.
+    frac = float(os.environ.get("SSM_REF_SAMPLE", "0.25"))
+    nd = max(1, int(w["dim"] * frac))
+    sub = {k: (v[:, :nd] if k in ("u", "delta", "z") else v[:nd] if k in ("A", "Dskip", "dt_bias") else v)
+           for k, v in x.items() if v is not None}
+    sub_bytes = nbytes * nd / w["dim"]
+    for _ in range(args.warmup):
+        oracle.scan(**sub, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan(**sub, nthreads=threads)
+    el = time.perf_counter() - t0
+    value = sub_bytes * args.steps / el / 1e9
+    sample = f"{nd} of {w['dim']} channels x batch {w['batch']} x L {w['seqlen']} per step"
+    out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": HEADLINE, "batch": w["batch"], "dim": w["dim"], "dstate": w["dstate"],
+                      "seqlen": w["seqlen"], "ngroups": w["ngroups"], "io": "bf16-rounded values in fp64"},
+           "impl": "reference",
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_profile_case(args):
+    """W + K eager launches of one workload on one input set, nothing else:
+    the command profiled by ncu."""
+    import torch
+    from selective_state_space_109_b300 import inputs as I
+    from selective_state_space_109_b300 import ssm
+    w = I.WORKLOADS[args.profile]
+    dev = torch.device("cuda")
+    if w["kind"] == "decode":
+        prm = I.decode_params(w["dim"], w["dstate"], recipe=w["recipe"], device=dev)
+        st = I.make_decode_state(w["batch"], w["dim"], w["dstate"], device=dev)
+        tok = I.make_decode_token(w["batch"], w["dim"], w["dstate"], 0, io=w["io"], recipe=w["recipe"],
+                                  device=dev)
+        for _ in range(args.warmup + args.steps):
+            ssm.state_update(st, tok["u"], tok["delta"], prm["A"], tok["B"], tok["C"], z=tok["z"],
+                             D=prm["D"], dt_bias=prm["dt_bias"])
+    else:
+        x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                               recipe=w["recipe"], device=dev)
+        for _ in range(args.warmup + args.steps):
+            if w.get("final_state"):
+                ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias)
+            else:
+                ssm.scan_fwd(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", metavar="WORKLOAD", default=None,
+                    help="only run W+K launches of one named workload (for ncu)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 selective-scan (S6) library, libssmscan.so.
+ *
+ * The library computes, per channel d of every sequence b, the selective
+ * state-space recurrence and its gated readout:
+ *
+ *   Delta_t   = softplus(delta_t + dt_bias[d])
+ *   Abar_t[n] = exp(Delta_t * A[d,n])                  zero-order-hold decay of a diagonal A
+ *   h_t[n]    = Abar_t[n] * h_{t-1}[n] + Delta_t * B_t[n] * u_t
+ *   y_t       = (sum_n C_t[n] * h_t[n] + Dskip[d] * u_t) * silu(z_t)
+ *
+ * Sources: the recurrence h_t = Abar_t h_{t-1} + Bbar_t x_t and readout
+ * y_t = C_t h_t are stated in eightmm.github.io "Mamba" (Main Claim; Scan View)
+ * and portpowered.github.io "Mamba Selective State-Space Module" (Math Or
+ * Compute Schema, "Selective state-space step").  The zero-order-hold decay
+ * exp(Delta A) and the simplified input term Bbar = Delta B, used in place of
+ * the exact zero-order-hold input matrix, are glossed in intvml.com "DL0170
+ * Mamba Selective SSM vs Attention" (Mathematical Formulation).  Delta, B and C
+ * depend on the token (aipedia.org "Mamba: State Space Models", The Key
+ * Innovation: Selectivity); here they arrive precomputed as tensors.  The
+ * softplus step, the Dskip term and the silu gate are this library's reading
+ * of the "gate path modulates output" stage (eightmm.github.io "Mamba", Block
+ * Structure), whose formula the pages do not print.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) on the
+ *   current device, except where stated.  The caller owns every buffer; the
+ *   library allocates nothing and keeps no pointer after a call returns.
+ * - Every tensor is dense and contiguous, row-major, last index fastest:
+ *     u, delta, z, y  : [batch, dim, seqlen]          (io type)
+ *     A               : [dim, dstate]                 (fp32)
+ *     B, C            : [batch, ngroups, dstate, seqlen] (io type)
+ *     Dskip, dt_bias  : [dim]                         (fp32)
+ *     h0, h_final     : [batch, dim, dstate]          (fp32)
+ *   Channel d reads the B/C rows of group g = d / (dim / ngroups).
+ * - io: SSM_F32 or SSM_BF16 selects the element type of u, delta, z, B, C, y
+ *   (and of the decode token tensors).  Arithmetic and the state are fp32.
+ *   bf16 outputs are rounded to nearest even.
+ * - Every pointer must be 16-byte aligned (SSM_ERR_MISALIGNED otherwise).
+ *   Any seqlen is accepted; rows whose length is not a multiple of the
+ *   vector width take a slower element-wise path.
+ * - Outputs (y, h_final) must not overlap any input.
+ * - stream is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *   asynchronous on that stream; argument errors are returned before anything
+ *   is enqueued.
+ * - Supported dstate: 4, 8, 16 (others return SSM_ERR_UNSUPPORTED).
+ * - batch == 0 is an empty problem: the call returns SSM_OK without touching
+ *   any pointer.  seqlen == 0 is accepted: nothing is read or written except
+ *   h_final (which then equals h0, or zeros).
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSM_ABI_VERSION 1
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,        /* null required pointer, bad size, dim % ngroups != 0 */
+    SSM_ERR_UNSUPPORTED = 2,        /* dstate not in {4, 8, 16}, unknown io type */
+    SSM_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+    SSM_ERR_WORKSPACE_TOO_SMALL = 4,/* workspace_bytes below the size query's answer */
+    SSM_ERR_TIMEOUT = 5,            /* a bounded device-side wait gave up (see ssm_workspace_status) */
+    SSM_ERR_CUDA = 6                /* a CUDA runtime call or launch failed (see ssm_last_cuda_error) */
+} ssm_status_t;
+
+typedef enum {
+    SSM_F32 = 0,
+    SSM_BF16 = 1
+} ssm_dtype_t;
+
+/* SSM_ABI_VERSION of the built library. */
+int ssm_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char *ssm_status_string(ssm_status_t status);
+
+/* The cudaError_t of the most recent SSM_ERR_CUDA returned on this host
+ * thread (0 if none). */
+int ssm_last_cuda_error(void);
+
+/*
+ * ssm_scan_fwd -- selective scan over whole sequences, state starting at 0.
+ *
+ * Discretisation, recurrence, readout, skip and gate run fused in one kernel;
+ * the state h stays in registers and is never written to memory.
+ *   u, delta : [batch, dim, seqlen] io type              (required)
+ *   z        : [batch, dim, seqlen] io type, or NULL (no gate)
+ *   A        : [dim, dstate] fp32                          (required)
+ *   B, C     : [batch, ngroups, dstate, seqlen] io type    (required)
+ *   Dskip    : [dim] fp32, or NULL (treated as 0)
+ *   dt_bias  : [dim] fp32, or NULL (treated as 0)
+ *   y        : [batch, dim, seqlen] io type, written       (required)
+ * Returns SSM_OK once the work is enqueued on stream.
+ */
+ssm_status_t ssm_scan_fwd(const void *u, const void *delta, const void *z,
+                          const float *A, const void *B, const void *C,
+                          const float *Dskip, const float *dt_bias, void *y,
+                          int batch, int dim, int dstate, int seqlen, int ngroups,
+                          ssm_dtype_t io, void *stream);
+
+/*
+ * Bytes of device workspace ssm_scan_fwd_chunked needs for this problem
+ * (0 for invalid arguments).  The answer depends only on the arguments.
+ */
+size_t ssm_scan_fwd_chunked_workspace_size(int batch, int dim, int dstate, int seqlen,
+                                           int ngroups, ssm_dtype_t io);
+
+/*
+ * ssm_scan_fwd_chunked -- selective scan with a caller-supplied initial state
+ * and the final state returned; long sequences are split into time chunks
+ * that run in parallel and are stitched by carrying each chunk's state into
+ * the next (eightmm.github.io "Mamba", Scan View: the recurrence is a scan
+ * over the pairs (Abar_t, Bbar_t x_t), so chunk results compose).
+ *
+ * Same tensors as ssm_scan_fwd, plus:
+ *   h0        : [batch, dim, dstate] fp32 initial state, or NULL (zeros)
+ *   h_final   : [batch, dim, dstate] fp32, written with h at t = seqlen-1
+ *               (or NULL if not wanted)
+ *   workspace : device buffer of at least
+ *               ssm_scan_fwd_chunked_workspace_size(...) bytes, 16-byte
+ *               aligned; owned by the caller, contents need not be
+ *               initialised, must not be shared by calls that may run
+ *               concurrently.  May be NULL when the size query returns 0.
+ * Cross-chunk waits on the device are bounded; if one gives up, the kernel
+ * records SSM_ERR_TIMEOUT in the workspace, which ssm_workspace_status
+ * reports.
+ */
+ssm_status_t ssm_scan_fwd_chunked(const void *u, const void *delta, const void *z,
+                                  const float *A, const void *B, const void *C,
+                                  const float *Dskip, const float *dt_bias,
+                                  const float *h0, void *y, float *h_final,
+                                  int batch, int dim, int dstate, int seqlen, int ngroups,
+                                  ssm_dtype_t io, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
+ * Synchronises stream, then returns the device-side status that the last
+ * ssm_scan_fwd_chunked call on this workspace recorded: SSM_OK or
+ * SSM_ERR_TIMEOUT (SSM_ERR_CUDA if the read itself failed).
+ */
+ssm_status_t ssm_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * ssm_state_update -- one decode step: every sequence of the batch consumes
+ * one token (cuishuaiwen.com "Mamba & State-Space Sequence Models", Core
+ * mechanics: inference runs the recurrence, O(1) per step, with a state whose
+ * size does not grow with the context; intvml.com, point (5)).
+ *   state   : [batch, dim, dstate] fp32, read and overwritten in place
+ *   u, delta: [batch, dim] io type                       (required)
+ *   z       : [batch, dim] io type, or NULL
+ *   A       : [dim, dstate] fp32
+ *   B, C    : [batch, ngroups, dstate] io type
+ *   Dskip, dt_bias : [dim] fp32, or NULL
+ *   y       : [batch, dim] io type, written
+ */
+ssm_status_t ssm_state_update(float *state, const void *u, const void *delta, const void *z,
+                              const float *A, const void *B, const void *C,
+                              const float *Dskip, const float *dt_bias, void *y,
+                              int batch, int dim, int dstate, int ngroups,
+                              ssm_dtype_t io, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

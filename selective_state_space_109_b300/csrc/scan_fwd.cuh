@@ -1,0 +1,279 @@
+// scan_fwd.cuh -- fused selective-scan forward kernel for sm_103a.
+//
+// One kernel does the whole path for a block of channels over time:
+// softplus step -> zero-order-hold decay exp(Delta A) -> input term
+// Delta B u -> diagonal recurrence h = Abar h + Bbar x -> readout C.h ->
+// skip D u -> silu(z) gate -> y.  The state never leaves registers.
+// (Recurrence and readout: eightmm.github.io "Mamba", Main Claim / Scan
+// View; discretisation: intvml.com "DL0170 Mamba Selective SSM vs
+// Attention", Mathematical Formulation; the fused, state-in-on-chip-memory
+// design goal: intvml.com, engineering paragraph after point (6).)
+//
+// Work decomposition
+//   * A channel's N states are split over LANES consecutive lanes of a warp
+//     (S = N / LANES states per lane, updated as fp32x2 pairs with FFMA2 /
+//     FMUL2).  A warp holds 32 / LANES channels; a CTA holds WARPS warps.
+//   * Time advances in warp blocks of TB = LANES * V steps.  In a block, lane
+//     j of a channel owns steps [j*V, j*V + V): it loads delta/u/z for them,
+//     computes Delta and Delta*u once (shared with the channel's other lanes
+//     through shared memory), and after the scan it receives their full
+//     readout through a butterfly reduce-scatter and writes y.
+//   * B and C are shared by every channel of a group; the CTA stages them in
+//     shared memory per tile of TT steps as fp32 quads (B_n, B_n+1, C_n,
+//     C_n+1), double-buffered with one CTA barrier per tile.
+//   * A time range [t_begin, t_end) and an initial state let the same kernel
+//     run a whole sequence or one chunk of it.
+#pragma once
+
+#include "ssm_device.cuh"
+
+namespace ssm {
+
+struct ScanParams {
+    const void* u;
+    const void* delta;
+    const void* z;        // nullable
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;       // nullable
+    const float* dt_bias; // nullable
+    void* y;
+    const float* h0;      // nullable
+    float* h_final;       // nullable
+    int batch, dim, seqlen, ngroups;
+    int dim_per_group;    // dim / ngroups
+    int blocks_per_group; // CTAs along the channels of one group
+    int vec_ok;           // seqlen is a multiple of the activation packet width
+    int bc_vec_ok;        // seqlen is a multiple of the 16-byte B/C packet width
+};
+
+template <typename T, int LANES>
+struct ScanShape {
+    // Steps owned by one lane per block: a 16-byte packet when few lanes share
+    // a channel, 4 steps otherwise (keeps TB = LANES * V <= 32 registers).
+    static constexpr int V = (LANES <= 2) ? (16 / static_cast<int>(sizeof(T))) : 4;
+    static constexpr int TB = LANES * V;
+};
+
+// Butterfly reduce-scatter over the LANES lanes of a channel: on entry slot
+// q*V+v of lane j holds its partial readout of step q*V+v; on exit slots
+// [0, V) hold the full sum (over all lanes) of steps j*V + [0, V).
+template <int LANES, int V>
+__device__ __forceinline__ void reduce_scatter(float (&acc)[LANES * V], int j) {
+#pragma unroll
+    for (int m = LANES / 2; m >= 1; m >>= 1) {
+        const bool upper = (j & m) != 0;
+#pragma unroll
+        for (int q = 0; q < m; ++q) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float lo = acc[q * V + v];
+                const float hi = acc[(q + m) * V + v];
+                const float send = upper ? lo : hi;
+                const float keep = upper ? hi : lo;
+                acc[q * V + v] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+        }
+    }
+}
+
+template <typename T, int N, int LANES, int WARPS, int TT, bool ACCURATE>
+__global__ void __launch_bounds__(WARPS * 32)
+scan_fwd_kernel(const ScanParams p) {
+    constexpr int S = N / LANES;   // states per lane
+    constexpr int P = S / 2;       // fp32x2 state pairs per lane
+    static_assert(S >= 2 && S % 2 == 0, "each lane holds an even number of states");
+    constexpr int CPW = 32 / LANES;  // channels per warp
+    constexpr int CH = WARPS * CPW;  // channels per CTA
+    constexpr int V = ScanShape<T, LANES>::V;
+    constexpr int TB = ScanShape<T, LANES>::TB;
+    static_assert(TT % TB == 0, "tile must hold whole warp blocks");
+    constexpr int NQ = N / 2;        // (B,B,C,C) quads per step
+    constexpr int VE = Elem<T>::kPer16B;
+    constexpr int THREADS = WARPS * 32;
+    constexpr int BC_ITEMS = 2 * N * (TT / VE);  // 16-byte B/C packets per tile
+    constexpr int BC_PER_THREAD = (BC_ITEMS + THREADS - 1) / THREADS;
+
+    __shared__ __align__(16) float4 bc_s[2][TT][NQ];
+    // (Delta, Delta*u) per warp channel and step; one float2 of padding per
+    // row spreads the rows of a warp over distinct banks.
+    __shared__ __align__(16) float2 dd_s[WARPS][CPW][TB + 1];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int cw = lane / LANES;  // channel within warp
+    const int j = lane % LANES;   // sub-lane within channel
+
+    const int cb = blockIdx.x % p.blocks_per_group;
+    const int bg = blockIdx.x / p.blocks_per_group;
+    const int g = bg % p.ngroups;
+    const int b = bg / p.ngroups;
+    const int dloc = cb * CH + warp * CPW + cw;
+    const bool active = dloc < p.dim_per_group;
+    const int d = g * p.dim_per_group + (active ? dloc : 0);
+    const int L = p.seqlen;
+
+    const long long row = (static_cast<long long>(b) * p.dim + d) * L;
+    const T* __restrict__ u_row = static_cast<const T*>(p.u) + row;
+    const T* __restrict__ dl_row = static_cast<const T*>(p.delta) + row;
+    const T* __restrict__ z_row = p.z ? static_cast<const T*>(p.z) + row : nullptr;
+    T* __restrict__ y_row = static_cast<T*>(p.y) + row;
+    const long long bc_off = (static_cast<long long>(b) * p.ngroups + g) * N * static_cast<long long>(L);
+    const T* __restrict__ Bg = static_cast<const T*>(p.B) + bc_off;
+    const T* __restrict__ Cg = static_cast<const T*>(p.C) + bc_off;
+    const bool vec_ok = p.vec_ok != 0;
+    const bool bc_vec_ok = p.bc_vec_ok != 0;
+    const bool has_z = z_row != nullptr;
+
+    // Per-lane constants: A (scaled for the exp form in use) for this lane's
+    // states, bias, skip.
+    float2 a2[P], h[P];
+    {
+        const float* Ad = p.A + static_cast<long long>(d) * N + j * S;
+        const float* h0 = p.h0 ? p.h0 + (static_cast<long long>(b) * p.dim + d) * N + j * S : nullptr;
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            const float2 av = __ldg(reinterpret_cast<const float2*>(Ad) + k);
+            a2[k] = make_float2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
+            h[k] = (h0 && active) ? __ldg(reinterpret_cast<const float2*>(h0) + k) : make_float2(0.f, 0.f);
+        }
+    }
+    const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
+    const float dsk = p.D ? __ldg(p.D + d) : 0.f;
+
+    // ---- B/C tile staging: global -> registers -> shared (fp32 quads) ----
+    Packet<T, VE> bc_reg[BC_PER_THREAD];
+    auto load_bc = [&](int t0) {
+#pragma unroll
+        for (int i = 0; i < BC_PER_THREAD; ++i) {
+            const int item = threadIdx.x + i * THREADS;
+            if (item < BC_ITEMS) {
+                const int r = item % (2 * N);  // (n, B|C) row, fastest across threads
+                const int tv = item / (2 * N);
+                const int n = r >> 1;
+                const T* src = ((r & 1) ? Cg : Bg) + static_cast<long long>(n) * L + t0 + tv * VE;
+                const int valid = L - (t0 + tv * VE);
+                if (bc_vec_ok && valid >= VE) bc_reg[i].load_cached(src);
+                else if (valid > 0) bc_reg[i].load_partial(src, valid);
+                else bc_reg[i].zero();
+            }
+        }
+    };
+    auto store_bc = [&](int buf) {
+        float* base = reinterpret_cast<float*>(&bc_s[buf][0][0]);
+#pragma unroll
+        for (int i = 0; i < BC_PER_THREAD; ++i) {
+            const int item = threadIdx.x + i * THREADS;
+            if (item < BC_ITEMS) {
+                const int r = item % (2 * N);
+                const int tv = item / (2 * N);
+                const int n = r >> 1;
+                const int isC = r & 1;
+                const int off = (n >> 1) * 4 + isC * 2 + (n & 1);
+                float f[VE];
+                bc_reg[i].to_float(f);
+#pragma unroll
+                for (int k = 0; k < VE; ++k) base[(tv * VE + k) * (2 * N) + off] = f[k];
+            }
+        }
+    };
+
+    // ---- per-lane activation packets, prefetched one warp block ahead ----
+    Packet<T, V> pd_cur, pu_cur, pz_cur, pd_nxt, pu_nxt, pz_nxt;
+    auto load_act = [&](int tb0, Packet<T, V>& pd, Packet<T, V>& pu, Packet<T, V>& pz) {
+        const int t = tb0 + j * V;
+        const int valid = active ? (L - t) : 0;
+        load_row<T, V>(pd, dl_row + t, valid, vec_ok);
+        load_row<T, V>(pu, u_row + t, valid, vec_ok);
+        if (has_z) load_row<T, V>(pz, z_row + t, valid, vec_ok);
+        else pz.zero();
+    };
+
+    const int ntiles = (L + TT - 1) / TT;
+    if (ntiles > 0) {
+        load_bc(0);
+        store_bc(0);
+        load_act(0, pd_cur, pu_cur, pz_cur);
+    }
+    __syncthreads();
+
+    for (int tile = 0; tile < ntiles; ++tile) {
+        const int buf = tile & 1;
+        const int t0 = tile * TT;
+        if (tile + 1 < ntiles) load_bc(t0 + TT);
+
+#pragma unroll 1
+        for (int blk = 0; blk < TT / TB; ++blk) {
+            const int tb0 = t0 + blk * TB;
+            if (tb0 >= L) break;  // uniform over the CTA
+            if (tb0 + TB < L) load_act(tb0 + TB, pd_nxt, pu_nxt, pz_nxt);
+
+            // Prologue: Delta and Delta*u for this lane's V steps.
+            float uu[V], zz[V];
+            {
+                float dv[V];
+                pd_cur.to_float(dv);
+                pu_cur.to_float(uu);
+                pz_cur.to_float(zz);
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const bool in = active && (tb0 + j * V + k < L);
+                    const float dt = in ? softplus<ACCURATE>(dv[k] + bias) : 0.f;
+                    dd_s[warp][cw][j * V + k] = make_float2(dt, dt * uu[k]);
+                }
+            }
+            __syncwarp();
+
+            // Scan: every lane advances its S states through all TB steps.
+            float acc[TB];
+            const float4* bcq = &bc_s[buf][blk * TB][j * P];
+#pragma unroll
+            for (int st = 0; st < TB; ++st) {
+                const float2 dd = dd_s[warp][cw][st];
+                const float2 dt2 = make_float2(dd.x, dd.x);
+                const float2 du2 = make_float2(dd.y, dd.y);
+                float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < P; ++k) {
+                    const float4 q = bcq[st * NQ + k];
+                    const float2 x = __fmul2_rn(dt2, a2[k]);
+                    const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+                    const float2 bx = __fmul2_rn(du2, make_float2(q.x, q.y));
+                    h[k] = __ffma2_rn(abar, h[k], bx);
+                    y2 = __ffma2_rn(make_float2(q.z, q.w), h[k], y2);
+                }
+                acc[st] = y2.x + y2.y;
+            }
+
+            // Readout of the channel's other lanes -> owner lane; skip, gate, store.
+            reduce_scatter<LANES, V>(acc, j);
+            if (active) {
+                float out[V];
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    float yv = acc[k] + dsk * uu[k];
+                    if (has_z) yv *= silu<ACCURATE>(zz[k]);
+                    out[k] = yv;
+                }
+                const int t = tb0 + j * V;
+                store_row<T, V>(y_row + t, out, L - t, vec_ok);
+            }
+            pd_cur = pd_nxt;
+            pu_cur = pu_nxt;
+            pz_cur = pz_nxt;
+            __syncwarp();
+        }
+
+        if (tile + 1 < ntiles) store_bc(buf ^ 1);
+        __syncthreads();
+    }
+
+    if (p.h_final && active) {
+        float* hf = p.h_final + (static_cast<long long>(b) * p.dim + d) * N + j * S;
+#pragma unroll
+        for (int k = 0; k < P; ++k) reinterpret_cast<float2*>(hf)[k] = h[k];
+    }
+}
+
+}  // namespace ssm

@@ -1,0 +1,204 @@
+"""Python binding of libssmscan.so (the C ABI in include/ssm_scan.h).
+
+Argument marshalling only: shapes and dtypes are checked, outputs are
+allocated with torch on the inputs' device, and the C entry point is called
+with raw device pointers on the current torch CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels.  Importing this module loads
+the library and raises ImportError if it is missing; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssmscan.so")
+
+SSM_F32 = 0
+SSM_BF16 = 1
+STATUS_NAMES = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
+                3: "SSM_ERR_MISALIGNED", 4: "SSM_ERR_WORKSPACE_TOO_SMALL",
+                5: "SSM_ERR_TIMEOUT", 6: "SSM_ERR_CUDA"}
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = STATUS_NAMES.get(status, f"status {status}")
+        extra = ""
+        if status == 6:
+            extra = f" (cudaError {lib.ssm_last_cuda_error()})"
+        super().__init__(f"{where}: {name}{extra}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m selective_state_space_109_b300.build` "
+            "(there is no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.ssm_abi_version.argtypes = []
+    L.ssm_abi_version.restype = I
+    L.ssm_status_string.argtypes = [I]
+    L.ssm_status_string.restype = ctypes.c_char_p
+    L.ssm_last_cuda_error.argtypes = []
+    L.ssm_last_cuda_error.restype = I
+    L.ssm_scan_fwd.argtypes = [P] * 9 + [I] * 6 + [P]
+    L.ssm_scan_fwd.restype = I
+    L.ssm_scan_fwd_chunked_workspace_size.argtypes = [I] * 6
+    L.ssm_scan_fwd_chunked_workspace_size.restype = Z
+    L.ssm_scan_fwd_chunked.argtypes = [P] * 11 + [I] * 6 + [P, Z, P]
+    L.ssm_scan_fwd_chunked.restype = I
+    L.ssm_workspace_status.argtypes = [P, Z, P]
+    L.ssm_workspace_status.restype = I
+    L.ssm_state_update.argtypes = [P] * 10 + [I] * 5 + [P]
+    L.ssm_state_update.restype = I
+    return L
+
+
+lib = _load()
+
+
+def _io_code(dtype: torch.dtype) -> int:
+    if dtype == torch.float32:
+        return SSM_F32
+    if dtype == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported I/O dtype {dtype} (float32 or bfloat16)")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _scan_shapes(u, A, B):
+    if u.dim() != 3 or A.dim() != 2 or B.dim() != 4:
+        raise ValueError("expected u [batch, dim, L], A [dim, N], B [batch, G, N, L]")
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    G = B.shape[1]
+    return batch, dim, N, L, G
+
+
+def _validate_scan(u, delta, z, A, B, C, D, dt_bias):
+    if u.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    batch, dim, N, L, G = _scan_shapes(u, A, B)
+    dev, io = u.device, u.dtype
+    _io_code(io)
+    _check(u, "u", (batch, dim, L), io, dev)
+    _check(delta, "delta", (batch, dim, L), io, dev)
+    _check(z, "z", (batch, dim, L), io, dev)
+    _check(A, "A", (dim, N), torch.float32, dev)
+    _check(B, "B", (batch, G, N, L), io, dev)
+    _check(C, "C", (batch, G, N, L), io, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(dt_bias, "dt_bias", (dim,), torch.float32, dev)
+    return batch, dim, N, L, G
+
+
+def scan_fwd(u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None) -> torch.Tensor:
+    """y = selective scan of (u, delta, A, B, C) with skip D and gate silu(z); h0 = 0."""
+    batch, dim, N, L, G = _validate_scan(u, delta, z, A, B, C, D, dt_bias)
+    y = torch.empty_like(u) if out is None else out
+    _check(y, "out", u.shape, u.dtype, u.device)
+    with torch.cuda.device(u.device):
+        st = lib.ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                              _ptr(dt_bias), _ptr(y), batch, dim, N, L, G, _io_code(u.dtype),
+                              _stream_handle(u.device))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_fwd")
+    return y
+
+
+def chunked_workspace_size(batch, dim, dstate, seqlen, ngroups, dtype) -> int:
+    return int(lib.ssm_scan_fwd_chunked_workspace_size(batch, dim, dstate, seqlen, ngroups,
+                                                       _io_code(dtype)))
+
+
+def alloc_workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    return torch.empty(int(nbytes), dtype=torch.uint8, device=device)
+
+
+def scan_fwd_chunked(u, delta, A, B, C, z=None, D=None, dt_bias=None, h0=None, *, out=None,
+                     h_final=None, workspace=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Selective scan from initial state h0 (zeros if None); returns (y, h_final)."""
+    batch, dim, N, L, G = _validate_scan(u, delta, z, A, B, C, D, dt_bias)
+    _check(h0, "h0", (batch, dim, N), torch.float32, u.device)
+    y = torch.empty_like(u) if out is None else out
+    _check(y, "out", u.shape, u.dtype, u.device)
+    hf = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device) if h_final is None else h_final
+    _check(hf, "h_final", (batch, dim, N), torch.float32, u.device)
+    need = chunked_workspace_size(batch, dim, N, L, G, u.dtype)
+    ws = alloc_workspace(need, u.device) if workspace is None else workspace
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    with torch.cuda.device(u.device):
+        st = lib.ssm_scan_fwd_chunked(_ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C),
+                                      _ptr(D), _ptr(dt_bias), _ptr(h0), _ptr(y), _ptr(hf),
+                                      batch, dim, N, L, G, _io_code(u.dtype), _ptr(ws), ws_bytes,
+                                      _stream_handle(u.device))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_fwd_chunked")
+    return y, hf
+
+
+def workspace_status(workspace: torch.Tensor) -> int:
+    """Synchronises the current stream and returns the device-side status code."""
+    with torch.cuda.device(workspace.device):
+        return int(lib.ssm_workspace_status(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            _stream_handle(workspace.device)))
+
+
+def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None) -> torch.Tensor:
+    """One decode step: updates ``state`` [batch, dim, N] in place, returns y [batch, dim]."""
+    if state.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    if state.dim() != 3 or B.dim() != 3:
+        raise ValueError("expected state [batch, dim, N], B [batch, G, N]")
+    batch, dim, N = state.shape
+    G = B.shape[1]
+    dev, io = state.device, u.dtype
+    _io_code(io)
+    _check(state, "state", (batch, dim, N), torch.float32, dev)
+    _check(u, "u", (batch, dim), io, dev)
+    _check(delta, "delta", (batch, dim), io, dev)
+    _check(z, "z", (batch, dim), io, dev)
+    _check(A, "A", (dim, N), torch.float32, dev)
+    _check(B, "B", (batch, G, N), io, dev)
+    _check(C, "C", (batch, G, N), io, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(dt_bias, "dt_bias", (dim,), torch.float32, dev)
+    y = torch.empty((batch, dim), dtype=io, device=dev) if out is None else out
+    _check(y, "out", (batch, dim), io, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_state_update(_ptr(state), _ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B),
+                                  _ptr(C), _ptr(D), _ptr(dt_bias), _ptr(y), batch, dim, N, G,
+                                  _io_code(io), _stream_handle(dev))
+    if st != 0:
+        raise SsmError(st, "ssm_state_update")
+    return y

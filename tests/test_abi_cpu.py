@@ -1,0 +1,110 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/*.h declares, and rejects bad arguments before anything touches the
+device (these calls return from the host-side checks; no kernel is launched)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from selective_state_space_109_b300 import build
+    build.build()
+    from selective_state_space_109_b300 import ssm
+    return ssm.lib
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(ssm_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["ssm_scan_fwd", "ssm_scan_fwd_chunked", "ssm_scan_fwd_chunked_workspace_size",
+                     "ssm_state_update", "ssm_workspace_status", "ssm_status_string",
+                     "ssm_abi_version", "ssm_last_cuda_error"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.ssm_abi_version() == 1
+    for code, name in [(0, b"SSM_OK"), (1, b"SSM_ERR_INVALID_ARG"), (2, b"SSM_ERR_UNSUPPORTED"),
+                       (3, b"SSM_ERR_MISALIGNED"), (4, b"SSM_ERR_WORKSPACE_TOO_SMALL"),
+                       (5, b"SSM_ERR_TIMEOUT"), (6, b"SSM_ERR_CUDA")]:
+        assert lib.ssm_status_string(code) == name
+
+
+# Fake, never-dereferenced pointer values: the checks only look at their
+# presence and alignment.
+P = 0x10000
+MIS = 0x10008
+
+
+def scan(lib, u=P, delta=P, z=None, A=P, B=P, C=P, D=None, bias=None, y=P,
+         batch=1, dim=4, N=16, L=8, G=1, io=1):
+    return lib.ssm_scan_fwd(u, delta, z, A, B, C, D, bias, y, batch, dim, N, L, G, io, None)
+
+
+def test_scan_argument_errors(lib):
+    assert scan(lib, u=None) == 1
+    assert scan(lib, A=None) == 1
+    assert scan(lib, y=None) == 1
+    assert scan(lib, dim=0) == 1
+    assert scan(lib, batch=-1) == 1
+    assert scan(lib, L=-5) == 1
+    assert scan(lib, dim=6, G=4) == 1          # dim % ngroups
+    assert scan(lib, N=12) == 2                # unsupported state size
+    assert scan(lib, N=32) == 2
+    assert scan(lib, io=7) == 2
+    assert scan(lib, B=MIS) == 3               # misaligned
+    assert scan(lib, z=MIS) == 3
+    assert scan(lib, batch=0, u=None, y=None) == 0  # empty problem: nothing to do
+
+
+def test_chunked_workspace_rules(lib):
+    need = lib.ssm_scan_fwd_chunked_workspace_size(1, 4, 16, 8, 1, 1)
+    assert need >= 0
+    assert lib.ssm_scan_fwd_chunked_workspace_size(1, 4, 12, 8, 1, 1) == 0  # invalid -> 0
+    if need > 0:
+        st = lib.ssm_scan_fwd_chunked(P, P, None, P, P, P, None, None, None, P, P,
+                                      1, 4, 16, 8, 1, 1, P, need - 1, None)
+        assert st == 4
+        st = lib.ssm_scan_fwd_chunked(P, P, None, P, P, P, None, None, None, P, P,
+                                      1, 4, 16, 8, 1, 1, None, 0, None)
+        assert st == 4
+    st = lib.ssm_scan_fwd_chunked(P, P, None, P, P, P, None, None, MIS, P, P,
+                                  1, 4, 16, 8, 1, 1, P, need, None)
+    assert st == 3  # misaligned h0
+
+
+def test_state_update_argument_errors(lib):
+    def call(state=P, u=P, delta=P, z=None, A=P, B=P, C=P, y=P, batch=2, dim=4, N=16, G=1, io=1):
+        return lib.ssm_state_update(state, u, delta, z, A, B, C, None, None, y, batch, dim, N, G, io, None)
+    assert call(state=None) == 1
+    assert call(y=None) == 1
+    assert call(dim=0) == 1
+    assert call(dim=6, G=4) == 1
+    assert call(N=6) == 2
+    assert call(state=MIS) == 3
+    assert call(batch=0, state=None) == 0
+
+
+def test_workspace_status_argument_errors(lib):
+    assert lib.ssm_workspace_status(None, 256, None) == 1
+    assert lib.ssm_workspace_status(P, 8, None) == 1
+    assert lib.ssm_workspace_status(MIS, 256, None) == 3
