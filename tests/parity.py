@@ -38,7 +38,7 @@ def max_rel(x, ref, guard=MAX_REL_GUARD):
     if ref.size == 0:
         return 0.0
     rms = float(np.sqrt(np.mean(ref * ref)))
-    den = np.maximum(np.abs(ref), 1e-3 * rms if rms > 0 else 1e-30)
+    den = np.maximum(np.abs(ref), guard * rms if rms > 0 else 1e-30)
     return float(np.max(np.abs(x - ref) / den))
 
 
