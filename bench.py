@@ -212,22 +212,18 @@ def bench_scan_device(ssm, I, torch, w, steps, warmup, sampler=None, preroll_s=1
     sets = [I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
                                recipe=w["recipe"], seed=s, device=dev) for s in range(nsets)]
     outs = [torch.empty_like(x.u) for x in sets]
-    final = w.get("final_state", False)
+    # The timed call is the chunked entry point (time-parallel chunks with the
+    # carried state, final state returned): the whole forward path.
     hfs = [torch.empty((w["batch"], w["dim"], w["dstate"]), dtype=torch.float32, device=dev)
-           for _ in range(nsets)] if final else None
-    ws = None
-    if final:
-        need = ssm.chunked_workspace_size(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"],
-                                          sets[0].u.dtype)
-        ws = [ssm.alloc_workspace(need, dev) for _ in range(nsets)]
+           for _ in range(nsets)]
+    need = ssm.chunked_workspace_size(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"],
+                                      sets[0].u.dtype)
+    ws = [ssm.alloc_workspace(need, dev) for _ in range(nsets)]
 
     def launch(i):
         x = sets[i]
-        if final:
-            ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias,
-                                 out=outs[i], h_final=hfs[i], workspace=ws[i])
-        else:
-            ssm.scan_fwd(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias, out=outs[i])
+        ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias,
+                             out=outs[i], h_final=hfs[i], workspace=ws[i])
 
     stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
@@ -283,14 +279,18 @@ def bench_scan_e2e(ssm, I, torch, w, steps, warmup):
     params = {n: getattr(x, n).to(dev) for n in ["A", "D", "dt_bias"]}
     y_dev = torch.empty_like(devt["u"])
     y_host = torch.empty_like(host["u"]).pin_memory()
+    hf_dev = torch.empty((w["batch"], w["dim"], w["dstate"]), dtype=torch.float32, device=dev)
+    ws = ssm.alloc_workspace(ssm.chunked_workspace_size(w["batch"], w["dim"], w["dstate"], w["seqlen"],
+                                                        w["ngroups"], host["u"].dtype), dev)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = y_host.numel() * y_host.element_size()
 
     def step():
         for n in names:
             devt[n].copy_(host[n], non_blocking=True)
-        ssm.scan_fwd(devt["u"], devt["delta"], params["A"], devt["B"], devt["C"], z=devt["z"],
-                     D=params["D"], dt_bias=params["dt_bias"], out=y_dev)
+        ssm.scan_fwd_chunked(devt["u"], devt["delta"], params["A"], devt["B"], devt["C"], z=devt["z"],
+                             D=params["D"], dt_bias=params["dt_bias"], out=y_dev, h_final=hf_dev,
+                             workspace=ws)
         y_host.copy_(y_dev, non_blocking=True)
 
     for _ in range(warmup):

@@ -124,12 +124,18 @@ size_t ssm_scan_fwd_chunked_workspace_size(int batch, int dim, int dstate, int s
  *   h_final   : [batch, dim, dstate] fp32, written with h at t = seqlen-1
  *               (or NULL if not wanted)
  *   workspace : device buffer of at least
- *               ssm_scan_fwd_chunked_workspace_size(...) bytes, 16-byte
- *               aligned; owned by the caller, contents need not be
- *               initialised, must not be shared by calls that may run
- *               concurrently.  May be NULL when the size query returns 0.
- * Cross-chunk waits on the device are bounded; if one gives up, the kernel
- * records SSM_ERR_TIMEOUT in the workspace, which ssm_workspace_status
+ *               ssm_scan_fwd_chunked_workspace_size(...) bytes (always at
+ *               least 256), 16-byte aligned; owned by the caller, contents
+ *               need not be initialised, must not be shared by calls that
+ *               may run concurrently.  It holds a status word and, for
+ *               time-chunked runs, one summary (P, E) per channel and chunk:
+ *               P[n] = exp(A[d,n] * sum of Delta over the chunk) and E = the
+ *               chunk's end state from a zero start.
+ * When the sequence is long relative to the number of channels, the call
+ * enqueues two kernels: a summary pass over every chunk but the last, then
+ * the fused pass, where chunk c starts from h0 folded through the summaries
+ * of chunks 0..c-1.  Device-side waits are bounded; if one gives up, the
+ * kernel records SSM_ERR_TIMEOUT in the workspace, which ssm_workspace_status
  * reports.
  */
 ssm_status_t ssm_scan_fwd_chunked(const void *u, const void *delta, const void *z,
@@ -146,6 +152,15 @@ ssm_status_t ssm_scan_fwd_chunked(const void *u, const void *delta, const void *
  * SSM_ERR_TIMEOUT (SSM_ERR_CUDA if the read itself failed).
  */
 ssm_status_t ssm_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises stream, then returns the library's device-wide error word for
+ * the current device: SSM_OK, or SSM_ERR_TIMEOUT if any kernel of this library
+ * gave up on a bounded device-side wait since the word was last cleared (its
+ * outputs are then unreliable).  clear != 0 resets the word afterwards.
+ * SSM_ERR_CUDA if the read itself failed.
+ */
+ssm_status_t ssm_device_status(int clear, void *stream);
 
 /*
  * ssm_state_update -- one decode step: every sequence of the batch consumes

@@ -56,28 +56,6 @@ struct ScanShape {
     static constexpr int TB = LANES * V;
 };
 
-// Butterfly reduce-scatter over the LANES lanes of a channel: on entry slot
-// q*V+v of lane j holds its partial readout of step q*V+v; on exit slots
-// [0, V) hold the full sum (over all lanes) of steps j*V + [0, V).
-template <int LANES, int V>
-__device__ __forceinline__ void reduce_scatter(float (&acc)[LANES * V], int j) {
-#pragma unroll
-    for (int m = LANES / 2; m >= 1; m >>= 1) {
-        const bool upper = (j & m) != 0;
-#pragma unroll
-        for (int q = 0; q < m; ++q) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float lo = acc[q * V + v];
-                const float hi = acc[(q + m) * V + v];
-                const float send = upper ? lo : hi;
-                const float keep = upper ? hi : lo;
-                acc[q * V + v] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-        }
-    }
-}
-
 template <typename T, int N, int LANES, int WARPS, int TT, bool ACCURATE>
 __global__ void __launch_bounds__(WARPS * 32)
 scan_fwd_kernel(const ScanParams p) {

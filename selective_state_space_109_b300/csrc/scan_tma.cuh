@@ -1,0 +1,435 @@
+// scan_tma.cuh -- TMA-staged selective-scan kernels for sm_103a.
+//
+// The same kernel template runs two passes of the scan:
+//
+//   Full       softplus step -> zero-order-hold decay exp(Delta A) -> input
+//              term Delta B u -> diagonal recurrence h = Abar h + Bbar x ->
+//              readout C.h -> skip D u -> silu(z) gate -> y, with the state
+//              in registers (eightmm.github.io "Mamba", Main Claim and Scan
+//              View; intvml.com "DL0170 Mamba Selective SSM vs Attention",
+//              Mathematical Formulation).  A time chunk c > 0 starts from the
+//              state carried into it, folded from the chunk summaries below.
+//   Aggregate  the same recurrence over one time chunk from a zero state,
+//              without readout: it writes the chunk's summary, the pair
+//              (P, E) with P[n] = prod_t Abar_t[n] = exp(A[n] sum_t Delta_t)
+//              and E[n] = the chunk's end state.  Because the recurrence is a
+//              scan over the pairs (Abar_t, Bbar_t x_t) (eightmm.github.io
+//              "Mamba", Scan View), the state entering chunk c is
+//              h_c = P_{c-1} (... (P_0 h0 + E_0) ...) + E_{c-1}.
+//
+// Data movement: every operand tile arrives by TMA into shared memory.  A CTA
+// owns CH consecutive channels of one (sequence, group) and one time chunk; it
+// walks the chunk in tiles of TS steps (64 bytes of each channel row), through
+// a 4-stage ring of mbarrier-tracked stages.  Activation tiles (u, delta, z)
+// are [CH rows x 64 B] with 64-byte swizzle, so that the lanes of a warp, each
+// reading its own row, hit distinct banks.  B and C tiles ([N rows x 64 B],
+// shared by all channels of the group) are widened once per tile into fp32
+// (B_n, B_n+1, C_n, C_n+1) quads that every lane reads by broadcast.  y is
+// written back in place over the u tile and leaves by a TMA store.
+//
+// Lanes: LANES consecutive lanes share one channel, S = N / LANES states each.
+// Per 16-byte chunk of a row (VPC steps) lane j computes Delta and Delta*u for
+// H = VPC / LANES of the steps and posts them, as ready-made fp32 pairs, to a
+// per-warp scratch row that all lanes of the channel read; after the chunk's
+// recurrence a butterfly reduce-scatter leaves lane j with the full readout
+// of its H steps, which it gates and stores.
+#pragma once
+
+#include <type_traits>
+
+#include "ssm_device.cuh"
+#include "tma.cuh"
+
+namespace ssm {
+
+struct TmaScanParams {
+    const float* A;
+    const float* D;        // nullable
+    const float* dt_bias;  // nullable
+    const float* h0;       // nullable
+    float* h_final;        // nullable
+    float* agg;            // chunk summaries [nchunks - 1][batch * dim][2][N] (P then E)
+    unsigned int* status;  // nullable caller status word (timeouts)
+    int batch, dim, seqlen, ngroups, dim_per_group;
+    int blocks_per_group;  // CTAs along the channels of one group
+    int nchunks;           // time chunks of the Full pass
+    int ntiles;            // ceil(seqlen / TS)
+    int has_z;
+};
+
+enum class ScanMode { Full, Aggregate };
+
+template <typename T>
+struct TileShape {
+    static constexpr int kRowBytes = 64;
+    static constexpr int TS = kRowBytes / static_cast<int>(sizeof(T));  // steps per tile
+    static constexpr int VPC = 16 / static_cast<int>(sizeof(T));        // steps per 16-byte chunk
+    static constexpr int CHUNKS = kRowBytes / 16;
+};
+
+template <typename T, int N, int LANES, int WARPS, ScanMode MODE>
+struct TmaScanLayout {
+    static constexpr bool FULL = MODE == ScanMode::Full;
+    static constexpr int CH = WARPS * 32 / LANES;
+    static constexpr int ACT_BYTES = CH * TileShape<T>::kRowBytes;  // one activation tile
+    static constexpr int BC_BYTES = N * TileShape<T>::kRowBytes;    // one B or C tile
+    static constexpr int NACT = FULL ? 3 : 2;                       // u, delta (, z)
+    static constexpr int NBC = FULL ? 2 : 1;                        // B (, C)
+    static constexpr int STAGES = 3;
+    static constexpr int STAGE_BYTES = ((NACT * ACT_BYTES + NBC * BC_BYTES) + 1023) / 1024 * 1024;
+    static constexpr int BCF_BYTES = TileShape<T>::TS * N * 4 * NBC;  // widened B (, C)
+    // Per-warp scratch through which the lanes of a channel share (Delta,
+    // Delta u) for one 16-byte chunk: two buffers (alternating chunks) of one
+    // padded row of VPC float4 per channel.
+    static constexpr int XS_STRIDE = TileShape<T>::VPC * 16 + 16;
+    static constexpr int XS_BUF = (32 / LANES) * XS_STRIDE;
+    static constexpr int XS_BYTES = LANES > 1 ? WARPS * 2 * XS_BUF : 0;
+    static constexpr int XS_OFFSET = STAGES * STAGE_BYTES + BCF_BYTES;
+    static constexpr int BAR_OFFSET = XS_OFFSET + XS_BYTES;
+    static constexpr int SMEM_BYTES = BAR_OFFSET + STAGES * 8 + 1024;  // + alignment slack
+    static_assert(ACT_BYTES % 512 == 0, "activation tiles must keep the 64-byte swizzle phase");
+};
+
+// Loads H consecutive elements (H * sizeof(T) = 4, 8 or 16 bytes) from shared memory.
+template <typename T, int H>
+__device__ __forceinline__ void lds_row(const unsigned char* p, float (&f)[H]) {
+    constexpr int BYTES = H * static_cast<int>(sizeof(T));
+    uint32_t w[BYTES / 4];
+    if constexpr (BYTES == 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (BYTES == 8) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        static_assert(BYTES == 4, "4, 8 or 16 bytes");
+        w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int k = 0; k < H; ++k) f[k] = __uint_as_float(w[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < BYTES / 4; ++k) {
+            f[2 * k] = __uint_as_float(w[k] << 16);
+            f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    }
+}
+
+// Rounds H floats to T (bf16: nearest even) and stores them to shared memory.
+template <typename T, int H>
+__device__ __forceinline__ void sts_row(unsigned char* p, const float (&f)[H]) {
+    constexpr int BYTES = H * static_cast<int>(sizeof(T));
+    uint32_t w[BYTES / 4];
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int k = 0; k < H; ++k) w[k] = __float_as_uint(f[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < BYTES / 4; ++k) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+    }
+    if constexpr (BYTES == 16) {
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (BYTES == 8) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+    } else {
+        *reinterpret_cast<uint32_t*>(p) = w[0];
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float lds_elem(const unsigned char* p) {
+    if constexpr (sizeof(T) == 4) {
+        return *reinterpret_cast<const float*>(p);
+    } else {
+        return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+    }
+}
+
+template <typename T, int N, int LANES, int WARPS, ScanMode MODE, bool ACCURATE>
+__global__ void __launch_bounds__(WARPS * 32)
+scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
+                const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_y,
+                const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
+                const TmaScanParams p) {
+    using Lay = TmaScanLayout<T, N, LANES, WARPS, MODE>;
+    using Sh = TileShape<T>;
+    constexpr bool FULL = Lay::FULL;
+    constexpr int TS = Sh::TS;
+    constexpr int VPC = Sh::VPC;
+    constexpr int S = N / LANES;       // states per lane
+    constexpr int P = S / 2;           // fp32x2 state pairs per lane
+    constexpr int NQ = N / 2;          // state pairs per step
+    constexpr int H = VPC / LANES;     // steps per lane per 16-byte chunk
+    constexpr int CH = Lay::CH;
+    constexpr int THREADS = WARPS * 32;
+    constexpr int STAGES = Lay::STAGES;
+    static_assert(S >= 2 && S % 2 == 0, "each lane holds an even number of states");
+    static_assert(H >= 1, "a lane owns at least one step of each chunk");
+
+    // Align the dynamic shared memory to 1024 bytes by offsetting the shared
+    // array itself, so that every access below stays a shared-memory access.
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    float* bcf = reinterpret_cast<float*>(smem + STAGES * Lay::STAGE_BYTES);
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFFSET);
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int r = warp * (32 / LANES) + lane / LANES;  // channel row within the CTA
+    const int j = lane % LANES;                        // sub-lane within the channel
+    const int cw = lane / LANES;                       // channel within the warp
+    unsigned char* xs_warp = smem + Lay::XS_OFFSET + warp * 2 * Lay::XS_BUF;
+
+    const int cb = blockIdx.x % p.blocks_per_group;
+    const int bg = blockIdx.x / p.blocks_per_group;  // b * ngroups + g
+    const int g = bg % p.ngroups;
+    const int b = bg / p.ngroups;
+    const int dloc0 = cb * CH;
+    const int dloc = dloc0 + r;
+    const bool active = dloc < p.dim_per_group;
+    const int d = g * p.dim_per_group + (active ? dloc : 0);
+    const long long bd = static_cast<long long>(b) * p.dim + d;
+    const long long BD = static_cast<long long>(p.batch) * p.dim;
+
+    const int chunk = blockIdx.y;
+    const int tb = static_cast<int>(static_cast<long long>(chunk) * p.ntiles / p.nchunks);
+    const int te = static_cast<int>(static_cast<long long>(chunk + 1) * p.ntiles / p.nchunks);
+    const int nt = te - tb;
+
+    // ---- per-lane constants and the state entering this chunk ----
+    float2 a2[P], h[P];
+    {
+        const float* Ad = p.A + static_cast<long long>(d) * N + j * S;
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            const float2 av = __ldg(reinterpret_cast<const float2*>(Ad) + k);
+            a2[k] = make_float2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
+            h[k] = make_float2(0.f, 0.f);
+        }
+        if constexpr (FULL) {
+            if (p.h0 && active) {
+                const float2* h0v = reinterpret_cast<const float2*>(p.h0 + bd * N + j * S);
+#pragma unroll
+                for (int k = 0; k < P; ++k) h[k] = __ldg(h0v + k);
+            }
+            // Fold the summaries of the chunks before this one.
+            for (int c = 0; c < chunk; ++c) {
+                const float* agg = p.agg + (static_cast<long long>(c) * BD + bd) * (2 * N) + j * S;
+#pragma unroll
+                for (int k = 0; k < P; ++k) {
+                    const float2 Pc = __ldcg(reinterpret_cast<const float2*>(agg) + k);
+                    const float2 Ec = __ldcg(reinterpret_cast<const float2*>(agg + N) + k);
+                    h[k] = __ffma2_rn(Pc, h[k], Ec);
+                }
+            }
+        }
+    }
+    const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
+    const float dsk = p.D ? __ldg(p.D + d) : 0.f;
+    const bool has_z = FULL && p.has_z;
+
+    // ---- barriers and the TMA prologue ----
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full_bar[s], 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_u);
+        prefetch_tensormap(&tm_d);
+        prefetch_tensormap(&tm_B);
+        if constexpr (FULL) {
+            prefetch_tensormap(&tm_y);
+            prefetch_tensormap(&tm_C);
+            if (has_z) prefetch_tensormap(&tm_z);
+        }
+    }
+    __syncthreads();
+
+    const uint32_t stage_tx =
+        static_cast<uint32_t>((2 + (has_z ? 1 : 0)) * Lay::ACT_BYTES + Lay::NBC * Lay::BC_BYTES);
+    auto stage_ptr = [&](int s) { return smem + s * Lay::STAGE_BYTES; };
+    auto issue = [&](int i) {  // thread 0 only: load tile tb + i into its stage
+        const int s = i % STAGES;
+        unsigned char* st = stage_ptr(s);
+        const int x = (tb + i) * TS;
+        mbar_arrive_expect_tx(&full_bar[s], stage_tx);
+        tma_load_3d(st, &tm_u, x, dloc0, bg, &full_bar[s]);
+        tma_load_3d(st + Lay::ACT_BYTES, &tm_d, x, dloc0, bg, &full_bar[s]);
+        if (has_z) tma_load_3d(st + 2 * Lay::ACT_BYTES, &tm_z, x, dloc0, bg, &full_bar[s]);
+        unsigned char* bc = st + Lay::NACT * Lay::ACT_BYTES;
+        tma_load_2d(bc, &tm_B, x, bg * N, &full_bar[s]);
+        if constexpr (FULL) tma_load_2d(bc + Lay::BC_BYTES, &tm_C, x, bg * N, &full_bar[s]);
+    };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES && i < nt; ++i) issue(i);
+    }
+
+    float dsum = 0.f;  // sum of Delta over the chunk (Aggregate)
+
+#pragma unroll 1
+    for (int i = 0; i < nt; ++i) {
+        const int s = i % STAGES;
+        unsigned char* st = stage_ptr(s);
+        mbar_wait(&full_bar[s], static_cast<uint32_t>((i / STAGES) & 1), p.status);
+
+        // Widen this tile's B (and C) rows into per-step fp32 pairs/quads.
+        {
+            const unsigned char* bsrc = st + Lay::NACT * Lay::ACT_BYTES;
+            for (int item = threadIdx.x; item < TS * NQ; item += THREADS) {
+                const int t = item / NQ;
+                const int q = item % NQ;
+                const unsigned char* b0 = bsrc + (2 * q) * Sh::kRowBytes + t * static_cast<int>(sizeof(T));
+                const float B0 = lds_elem<T>(b0);
+                const float B1 = lds_elem<T>(b0 + Sh::kRowBytes);
+                if constexpr (FULL) {
+                    const unsigned char* c0 = b0 + Lay::BC_BYTES;
+                    reinterpret_cast<float4*>(bcf)[item] =
+                        make_float4(B0, B1, lds_elem<T>(c0), lds_elem<T>(c0 + Sh::kRowBytes));
+                } else {
+                    reinterpret_cast<float2*>(bcf)[item] = make_float2(B0, B1);
+                }
+            }
+        }
+        __syncthreads();
+
+        const int t0 = (tb + i) * TS;
+        unsigned char* u_t = st;
+        const unsigned char* d_t = st + Lay::ACT_BYTES;
+        const unsigned char* z_t = st + 2 * Lay::ACT_BYTES;
+
+        // One 16-byte chunk (VPC steps) of this lane's channel row.  MASKED:
+        // the tile runs past the sequence end, so steps beyond it get Delta = 0
+        // (Abar = 1, no input: the state passes through unchanged).
+        auto run_chunk = [&](const int c, auto masked) {
+            constexpr bool MASKED = decltype(masked)::value;
+            const uint32_t off = swz64(r, c) + j * H * static_cast<int>(sizeof(T));
+            float uu[H], dt[H], du[H];
+            {
+                float dv[H];
+                lds_row<T, H>(u_t + off, uu);
+                lds_row<T, H>(d_t + off, dv);
+#pragma unroll
+                for (int k = 0; k < H; ++k) {
+                    dt[k] = softplus<ACCURATE>(dv[k] + bias);
+                    if constexpr (MASKED) {
+                        if (t0 + c * VPC + j * H + k >= p.seqlen) dt[k] = 0.f;
+                    }
+                    du[k] = dt[k] * uu[k];
+                }
+            }
+            // The channel's lanes share (Delta, Delta, Delta u, Delta u) for
+            // every step of the chunk through the warp's scratch rows.
+            [[maybe_unused]] float4* xrow = nullptr;
+            if constexpr (LANES > 1) {
+                xrow = reinterpret_cast<float4*>(xs_warp + (c & 1) * Lay::XS_BUF + cw * Lay::XS_STRIDE);
+#pragma unroll
+                for (int k = 0; k < H; ++k) xrow[j * H + k] = make_float4(dt[k], dt[k], du[k], du[k]);
+                __syncwarp();
+            }
+
+            [[maybe_unused]] float acc[VPC];
+#pragma unroll
+            for (int kk = 0; kk < VPC; ++kk) {
+                float2 dt2, du2;
+                if constexpr (LANES == 1) {
+                    dt2 = make_float2(dt[kk], dt[kk]);
+                    du2 = make_float2(du[kk], du[kk]);
+                } else {
+                    const float4 e = xrow[kk];
+                    dt2 = make_float2(e.x, e.y);
+                    du2 = make_float2(e.z, e.w);
+                }
+                const int row = c * VPC + kk;
+                if constexpr (!FULL) dsum += dt2.x;
+                if constexpr (FULL) {
+                    const float4* q4 = reinterpret_cast<const float4*>(bcf) + row * NQ + j * P;
+                    float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < P; ++k) {
+                        const float4 q = q4[k];
+                        const float2 x = __fmul2_rn(dt2, a2[k]);
+                        const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+                        const float2 bx = __fmul2_rn(du2, make_float2(q.x, q.y));
+                        h[k] = __ffma2_rn(abar, h[k], bx);
+                        y2 = __ffma2_rn(make_float2(q.z, q.w), h[k], y2);
+                    }
+                    acc[kk] = y2.x + y2.y;
+                } else {
+                    const float2* q2 = reinterpret_cast<const float2*>(bcf) + row * NQ + j * P;
+#pragma unroll
+                    for (int k = 0; k < P; ++k) {
+                        const float2 bq = q2[k];
+                        const float2 x = __fmul2_rn(dt2, a2[k]);
+                        const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+                        h[k] = __ffma2_rn(abar, h[k], __fmul2_rn(du2, bq));
+                    }
+                }
+            }
+
+            if constexpr (FULL) {
+                reduce_scatter<LANES, H>(acc, j);
+                float zz[H];
+                if (has_z) lds_row<T, H>(z_t + off, zz);
+                float out[H];
+#pragma unroll
+                for (int k = 0; k < H; ++k) {
+                    float yv = fmaf(dsk, uu[k], acc[k]);
+                    if (has_z) yv *= silu<ACCURATE>(zz[k]);
+                    out[k] = yv;
+                }
+                sts_row<T, H>(u_t + off, out);  // y in place of u
+            }
+        };
+
+        if (t0 + TS <= p.seqlen) {
+#pragma unroll
+            for (int c = 0; c < Sh::CHUNKS; ++c) run_chunk(c, std::false_type{});
+        } else {
+#pragma unroll 1
+            for (int c = 0; c < Sh::CHUNKS; ++c) run_chunk(c, std::true_type{});
+        }
+
+        if constexpr (FULL) fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if constexpr (FULL) {
+                tma_store_3d(&tm_y, t0, dloc0, bg, st);
+                bulk_commit();
+                // The stage of tile i-1 is free once its y store has read it.
+                if (i >= 1 && i - 1 + STAGES < nt) {
+                    bulk_wait_read<1>();
+                    issue(i - 1 + STAGES);
+                }
+            } else {
+                if (i + STAGES < nt) issue(i + STAGES);
+            }
+        }
+    }
+    if constexpr (FULL) {
+        if (threadIdx.x == 0) bulk_wait<0>();
+    }
+
+    if (!active) return;
+    if constexpr (FULL) {
+        if (p.h_final && chunk == p.nchunks - 1) {
+            float2* hf = reinterpret_cast<float2*>(p.h_final + bd * N + j * S);
+#pragma unroll
+            for (int k = 0; k < P; ++k) hf[k] = h[k];
+        }
+    } else {
+        float* agg = p.agg + (static_cast<long long>(chunk) * BD + bd) * (2 * N) + j * S;
+        const float2 ds2 = make_float2(dsum, dsum);
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            const float2 x = __fmul2_rn(ds2, a2[k]);
+            reinterpret_cast<float2*>(agg)[k] = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+            reinterpret_cast<float2*>(agg + N)[k] = h[k];
+        }
+    }
+}
+
+}  // namespace ssm

@@ -3,15 +3,19 @@
 // Each entry point validates its arguments without touching the GPU, picks a
 // kernel variant for the shape (lanes per channel, chunking), and enqueues the
 // launch on the caller's stream.  Nothing here computes on the host.
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched from the driver at run time
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
 
 #include "../../include/ssm_scan.h"
 #include "scan_fwd.cuh"
+#include "scan_tma.cuh"
 #include "state_update.cuh"
 
 namespace {
@@ -118,6 +122,263 @@ cudaError_t launch_scan_t(const ssm::ScanParams& p, int dstate, int lanes, cudaS
     }
 }
 
+// ---------------------------------------------------------------------------
+// TMA-staged path
+// ---------------------------------------------------------------------------
+
+constexpr int kTmaWarps = 4;
+// The time-chunk plan aims to fill a B300 (148 SMs).  It is a function of the
+// problem's arguments only, so the workspace size query needs no device.
+constexpr int kPlanSms = 148;
+constexpr int kMaxChunks = 16;
+
+// Workspace header: the device-side status word written by kernels that wait.
+constexpr size_t kWorkspaceHeader = 256;
+
+int tma_steps_per_tile(ssm_dtype_t io) { return io == SSM_F32 ? 16 : 32; }
+
+// Rows of every tensor must start on 16-byte boundaries for TMA.
+bool tma_eligible(int seqlen, ssm_dtype_t io) {
+    const int es = io == SSM_F32 ? 4 : 2;
+    return seqlen > 0 && (static_cast<long long>(seqlen) * es) % 16 == 0;
+}
+
+int max_chunks_for(int seqlen, ssm_dtype_t io) {
+    const int ntiles = (seqlen + tma_steps_per_tile(io) - 1) / tma_steps_per_tile(io);
+    return std::max(1, std::min(kMaxChunks, ntiles));
+}
+
+struct ScanPlan {
+    int lanes;
+    int chunks;
+};
+
+template <typename T, int N, ssm::ScanMode MODE>
+int tma_smem_bytes(int lanes) {
+    switch (lanes) {
+        case 1: return ssm::TmaScanLayout<T, N, 1, kTmaWarps, MODE>::SMEM_BYTES;
+        case 2: return ssm::TmaScanLayout<T, N, 2, kTmaWarps, MODE>::SMEM_BYTES;
+        default: return ssm::TmaScanLayout<T, N, (N >= 8 ? 4 : 2), kTmaWarps, MODE>::SMEM_BYTES;
+    }
+}
+
+template <ssm::ScanMode MODE>
+int tma_smem_for(ssm_dtype_t io, int dstate, int lanes) {
+    if (io == SSM_F32)
+        return dstate == 4 ? tma_smem_bytes<float, 4, MODE>(lanes)
+                           : dstate == 8 ? tma_smem_bytes<float, 8, MODE>(lanes) : tma_smem_bytes<float, 16, MODE>(lanes);
+    return dstate == 4 ? tma_smem_bytes<__nv_bfloat16, 4, MODE>(lanes)
+                       : dstate == 8 ? tma_smem_bytes<__nv_bfloat16, 8, MODE>(lanes)
+                                     : tma_smem_bytes<__nv_bfloat16, 16, MODE>(lanes);
+}
+
+// CTAs that fit on one SM by shared memory (228 KB per SM, 1 KB of it
+// reserved per CTA).
+int ctas_per_sm(int smem_bytes) { return std::max(1, (228 * 1024) / (smem_bytes + 1024)); }
+
+// Relative SM throughput with c resident CTAs (c warps per scheduler), from a
+// measurement of the scan's update mix on B300: one warp per scheduler
+// reaches about half the saturated rate, two about 0.8, three 0.9.
+double sm_efficiency(long long c) {
+    static const double e[5] = {0.0, 0.48, 0.8, 0.9, 1.0};
+    return c >= 4 ? 1.0 : e[c];
+}
+
+// Time (arbitrary units) of one pass: `ctas` CTAs of `work` each over kPlanSms
+// SMs, `cap` resident per SM; the busiest SM runs full waves of `cap` CTAs and
+// then its remainder.
+double pass_time(long long ctas, int cap, double work) {
+    const long long nmax = (ctas + kPlanSms - 1) / kPlanSms;
+    const long long full = nmax / cap, rest = nmax % cap;
+    double t = static_cast<double>(full) * cap * work / sm_efficiency(cap);
+    if (rest > 0) t += static_cast<double>(rest) * work / sm_efficiency(rest);
+    return t;
+}
+
+// Picks lanes per channel and time chunks by a wave model of the two passes.
+// Per-update cost of sharing a channel's states over 2 or 4 lanes (measured
+// on B300 against one lane at equal occupancy): 1.4 and 2.0; the summary pass
+// costs 0.9 of a full pass; a second kernel launch costs about 2 us.
+ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io,
+                   bool allow_chunks) {
+    const int dpg = dim / ngroups;
+    const int kmax = allow_chunks ? max_chunks_for(seqlen, io) : 1;
+    const int lmax = dstate >= 8 ? 4 : 2;
+    // Time units: one unit ~ one channel-step of a 16-state lane at full rate;
+    // ~0.54 ns per unit on B300 at N = 16.
+    const double launch_units = 2000.0 / 0.54 * (16.0 / dstate);
+    ScanPlan best{1, 1};
+    double best_cost = 1e300;
+    for (int lanes = 1; lanes <= lmax; lanes *= 2) {
+        const double lane_cost = lanes == 1 ? 1.0 : (lanes == 2 ? 1.4 : 2.0);
+        const int ch = kTmaWarps * 32 / lanes;
+        const long long blocks = static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
+        const int cap_full = ctas_per_sm(tma_smem_for<ssm::ScanMode::Full>(io, dstate, lanes));
+        const int cap_agg = ctas_per_sm(tma_smem_for<ssm::ScanMode::Aggregate>(io, dstate, lanes));
+        for (int k = 1; k <= kmax; ++k) {
+            const double work = lane_cost * ch * (static_cast<double>(seqlen) / k) * (dstate / 16.0);
+            double cost = pass_time(blocks * k, cap_full, work);
+            if (k > 1) cost += pass_time(blocks * (k - 1), cap_agg, 0.9 * work) + launch_units;
+            if (cost < best_cost * 0.999) {
+                best_cost = cost;
+                best = {lanes, k};
+            }
+        }
+    }
+    const int fl = env_int("SSM_FORCE_LANES", 0);
+    if ((fl == 1 || fl == 2 || fl == 4) && fl <= lmax) best.lanes = fl;
+    const int fk = env_int("SSM_FORCE_CHUNKS", 0);
+    if (fk >= 1) best.chunks = std::min(fk, kmax);
+    return best;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+struct ScanMaps {
+    CUtensorMap u, d, z, y, B, C;
+};
+
+// [batch * ngroups, dim_per_group, seqlen] activation view; box = one tile of
+// 64 bytes per row times `rows` channels, 64-byte swizzle.
+bool encode_act(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, int dpg, long long bg, int rows) {
+    const cuuint64_t es = io == SSM_F32 ? 4 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(dpg),
+                                static_cast<cuuint64_t>(bg)};
+    const cuuint64_t strides[2] = {seqlen * es, seqlen * es * dpg};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(64 / es), static_cast<cuuint32_t>(rows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode_tiled()(m, io == SSM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [batch * ngroups * dstate, seqlen] view of B or C; box = one tile x dstate rows.
+bool encode_bc(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, long long rows, int dstate) {
+    const cuuint64_t es = io == SSM_F32 ? 4 : 2;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {seqlen * es};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / es), static_cast<cuuint32_t>(dstate)};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode_tiled()(m, io == SSM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Opts a kernel into its dynamic shared memory once per device.
+template <typename K>
+cudaError_t ensure_smem(K kern, int bytes, unsigned long long* done_mask) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
+    return e;
+}
+
+template <typename T, int N, int LANES, ssm::ScanMode MODE>
+cudaError_t launch_tma(const ScanMaps& m, const ssm::TmaScanParams& p, int grid_y, cudaStream_t st) {
+    using Lay = ssm::TmaScanLayout<T, N, LANES, kTmaWarps, MODE>;
+    auto kern = ssm::scan_tma_kernel<T, N, LANES, kTmaWarps, MODE, sizeof(T) == 4>;
+    static unsigned long long done = 0;
+    cudaError_t e = ensure_smem(kern, Lay::SMEM_BYTES, &done);
+    if (e != cudaSuccess) return e;
+    const long long gx = static_cast<long long>(p.blocks_per_group) * p.ngroups * p.batch;
+    if (gx > 0x7fffffffLL || grid_y > 65535) return cudaErrorInvalidConfiguration;
+    kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(grid_y)), kTmaWarps * 32, Lay::SMEM_BYTES, st>>>(
+        m.u, m.d, m.z, m.y, m.B, m.C, p);
+    return cudaGetLastError();
+}
+
+template <typename T, int N, ssm::ScanMode MODE>
+cudaError_t launch_tma_lanes(const ScanMaps& m, const ssm::TmaScanParams& p, int lanes, int grid_y,
+                             cudaStream_t st) {
+    switch (lanes) {
+        case 1: return launch_tma<T, N, 1, MODE>(m, p, grid_y, st);
+        case 2: return launch_tma<T, N, 2, MODE>(m, p, grid_y, st);
+        case 4: if constexpr (N >= 8) return launch_tma<T, N, 4, MODE>(m, p, grid_y, st); break;
+        default: break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T, ssm::ScanMode MODE>
+cudaError_t launch_tma_n(const ScanMaps& m, const ssm::TmaScanParams& p, int dstate, int lanes, int grid_y,
+                         cudaStream_t st) {
+    switch (dstate) {
+        case 4: return launch_tma_lanes<T, 4, MODE>(m, p, lanes, grid_y, st);
+        case 8: return launch_tma_lanes<T, 8, MODE>(m, p, lanes, grid_y, st);
+        case 16: return launch_tma_lanes<T, 16, MODE>(m, p, lanes, grid_y, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Enqueues the staged scan: with plan.chunks > 1 the summary pass over all
+// chunks but the last, then the full pass over every chunk.
+ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const float* A, const void* B,
+                          const void* C, const float* Dskip, const float* dt_bias, const float* h0, void* y,
+                          float* h_final, int batch, int dim, int dstate, int seqlen, int ngroups,
+                          ssm_dtype_t io, const ScanPlan& plan, float* agg, unsigned int* status,
+                          cudaStream_t st) {
+    if (!encode_tiled()) return cuda_fail(cudaErrorNotSupported);
+    const int dpg = dim / ngroups;
+    const long long bg = static_cast<long long>(batch) * ngroups;
+    const int ch = kTmaWarps * 32 / plan.lanes;
+    ScanMaps m;
+    const bool ok = encode_act(&m.u, u, io, seqlen, dpg, bg, ch) && encode_act(&m.d, delta, io, seqlen, dpg, bg, ch) &&
+                    encode_act(&m.y, y, io, seqlen, dpg, bg, ch) &&
+                    (z ? encode_act(&m.z, z, io, seqlen, dpg, bg, ch) : true) &&
+                    encode_bc(&m.B, B, io, seqlen, bg * dstate, dstate) &&
+                    encode_bc(&m.C, C, io, seqlen, bg * dstate, dstate);
+    if (!ok) return cuda_fail(cudaErrorInvalidValue);
+    if (!z) m.z = m.u;  // never read: has_z = 0
+
+    ssm::TmaScanParams p{};
+    p.A = A; p.D = Dskip; p.dt_bias = dt_bias; p.h0 = h0; p.h_final = h_final;
+    p.agg = agg; p.status = status;
+    p.batch = batch; p.dim = dim; p.seqlen = seqlen; p.ngroups = ngroups; p.dim_per_group = dpg;
+    p.blocks_per_group = (dpg + ch - 1) / ch;
+    p.nchunks = plan.chunks;
+    p.ntiles = (seqlen + tma_steps_per_tile(io) - 1) / tma_steps_per_tile(io);
+    p.has_z = z != nullptr;
+
+    cudaError_t e = cudaSuccess;
+    if (plan.chunks > 1) {
+        e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Aggregate>(m, p, dstate, plan.lanes, plan.chunks - 1, st)
+                          : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Aggregate>(m, p, dstate, plan.lanes,
+                                                                                  plan.chunks - 1, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st)
+                      : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return SSM_OK;
+}
+
+bool force_generic() {
+    const char* s = std::getenv("SSM_FORCE_PATH");
+    return s && std::strcmp(s, "generic") == 0;
+}
+
 // Writes h_final = h0 (or zeros) for an empty sequence.
 __global__ void copy_or_zero_state_kernel(const float* __restrict__ h0, float* __restrict__ hf, long long n) {
     const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -127,7 +388,7 @@ __global__ void copy_or_zero_state_kernel(const float* __restrict__ h0, float* _
 ssm_status_t run_scan(const void* u, const void* delta, const void* z, const float* A,
                       const void* B, const void* C, const float* Dskip, const float* dt_bias,
                       const float* h0, void* y, float* h_final, int batch, int dim, int dstate,
-                      int seqlen, int ngroups, ssm_dtype_t io, cudaStream_t st) {
+                      int seqlen, int ngroups, ssm_dtype_t io, void* workspace, cudaStream_t st) {
     if (batch == 0) return SSM_OK;
     if (seqlen == 0) {
         if (h_final) {
@@ -137,6 +398,14 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
             if (e != cudaSuccess) return cuda_fail(e);
         }
         return SSM_OK;
+    }
+    if (tma_eligible(seqlen, io) && !force_generic()) {
+        const bool chunks_ok = workspace != nullptr;
+        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunks_ok);
+        float* agg = chunks_ok ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader) : nullptr;
+        unsigned int* status = chunks_ok ? static_cast<unsigned int*>(workspace) : nullptr;
+        return run_scan_tma(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen,
+                            ngroups, io, plan, agg, status, st);
     }
     ssm::ScanParams p{};
     p.u = u; p.delta = delta; p.z = z; p.A = A; p.B = B; p.C = C; p.D = Dskip;
@@ -153,8 +422,6 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
     return SSM_OK;
 }
 
-// Workspace header: a device-side status word written by kernels that wait.
-constexpr size_t kWorkspaceHeader = 256;
 
 }  // namespace
 
@@ -185,14 +452,21 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const void* z, const
                                            batch, dim, dstate, seqlen, ngroups, io);
     if (s != SSM_OK) return s;
     return run_scan(u, delta, z, A, B, C, Dskip, dt_bias, nullptr, y, nullptr, batch, dim, dstate,
-                    seqlen, ngroups, io, static_cast<cudaStream_t>(stream));
+                    seqlen, ngroups, io, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 size_t ssm_scan_fwd_chunked_workspace_size(int batch, int dim, int dstate, int seqlen, int ngroups,
                                            ssm_dtype_t io) {
     if (batch < 0 || dim <= 0 || seqlen < 0 || ngroups <= 0 || dim % ngroups != 0) return 0;
     if (!supported_dstate(dstate) || (io != SSM_F32 && io != SSM_BF16)) return 0;
-    return kWorkspaceHeader;
+    size_t bytes = kWorkspaceHeader;
+    if (tma_eligible(seqlen, io)) {
+        // Summaries (P, E) of up to kMaxChunks - 1 chunks for every channel.
+        const size_t chunks = static_cast<size_t>(max_chunks_for(seqlen, io)) - 1;
+        bytes += chunks * static_cast<size_t>(batch) * static_cast<size_t>(dim) * 2u * static_cast<size_t>(dstate) *
+                 sizeof(float);
+    }
+    return bytes;
 }
 
 ssm_status_t ssm_scan_fwd_chunked(const void* u, const void* delta, const void* z, const float* A,
@@ -213,7 +487,7 @@ ssm_status_t ssm_scan_fwd_chunked(const void* u, const void* delta, const void* 
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return run_scan(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate,
-                    seqlen, ngroups, io, st);
+                    seqlen, ngroups, io, workspace, st);
 }
 
 ssm_status_t ssm_workspace_status(const void* workspace, size_t workspace_bytes, void* stream) {
@@ -223,6 +497,21 @@ ssm_status_t ssm_workspace_status(const void* workspace, size_t workspace_bytes,
     uint32_t word = 0;
     cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return word == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
+}
+
+ssm_status_t ssm_device_status(int clear, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&word, ssm::g_ssm_device_error, sizeof(word), 0,
+                                              cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && clear && word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbolAsync(ssm::g_ssm_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return word == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
 }

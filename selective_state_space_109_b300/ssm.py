@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
     L.ssm_scan_fwd_chunked.restype = I
     L.ssm_workspace_status.argtypes = [P, Z, P]
     L.ssm_workspace_status.restype = I
+    L.ssm_device_status.argtypes = [I, P]
+    L.ssm_device_status.restype = I
     L.ssm_state_update.argtypes = [P] * 10 + [I] * 5 + [P]
     L.ssm_state_update.restype = I
     return L
@@ -172,6 +174,14 @@ def workspace_status(workspace: torch.Tensor) -> int:
     with torch.cuda.device(workspace.device):
         return int(lib.ssm_workspace_status(_ptr(workspace), workspace.numel() * workspace.element_size(),
                                             _stream_handle(workspace.device)))
+
+
+def device_status(clear: bool = False, device=None) -> int:
+    """Synchronises the current stream and returns the library's device error
+    status (0 = no bounded device-side wait has given up)."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib.ssm_device_status(int(bool(clear)), _stream_handle(dev)))
 
 
 def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None) -> torch.Tensor:
