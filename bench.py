@@ -263,7 +263,8 @@ def bench_scan_device(ssm, I, torch, w, steps, warmup, sampler=None, preroll_s=1
     torch.cuda.synchronize(dev)
     t_end = time.time()
     ms = e0.elapsed_time(e1)
-    return dict(ms_total=ms, ms_per_launch=ms / steps, bytes_per_step=nbytes, nsets=nsets,
+    plan = ssm.scan_plan(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], sets[0].u.dtype)
+    return dict(ms_total=ms, ms_per_launch=ms / steps, bytes_per_step=nbytes, nsets=nsets, plan=plan,
                 t_window=(t_pre, t_end), upd_per_step=w["batch"] * w["dim"] * w["seqlen"] * w["dstate"],
                 bdl_per_step=w["batch"] * w["dim"] * w["seqlen"])
 
@@ -437,7 +438,7 @@ def run_ours(args):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     alu_peak = sms * sm_max * 1e6 * UPDATES_PER_SM_CLK / 1e9  # Gupd/s
     alu_achieved = r["upd_per_step"] / per_launch_s / 1e9
-    traffic = ncu_traffic("scan_fwd_kernel/" + HEADLINE)
+    traffic = ncu_traffic("scan_chunked_call/" + HEADLINE)
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -461,7 +462,9 @@ def run_ours(args):
         "tokens_channels_per_s": round(r["bdl_per_step"] / per_launch_s, 1),
         "roofline": {"bound": "alu", "achieved": round(alu_achieved, 1), "peak": round(alu_peak, 1),
                      "unit": "Gupd/s", "frac": round(alu_achieved / alu_peak, 4), "traffic": traffic,
-                     "kernel": "scan_fwd_kernel",
+                     "kernel": ("scan_tma_kernel: summary pass + fused pass of one chunked call"
+                                if r["plan"]["kernels"] == 2 else "scan_tma_kernel: fused pass"),
+                     "plan": r["plan"],
                      "peak_basis": f"{sms} SMs x {sm_max:.0f} MHz x 32 state updates/SM/clk "
                                    "(MUFU.EX2 32/clk; FP32 128 lane-ops/clk at 4 per update)"},
         "hbm_roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
@@ -469,7 +472,7 @@ def run_ours(args):
                          "peak_source": peak_src, "traffic": traffic},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * r["plan"]["kernels"],
         "clocks": clocks,
     }
     if dec is not None:
@@ -542,15 +545,63 @@ def run_profile_case(args):
             ssm.state_update(st, tok["u"], tok["delta"], prm["A"], tok["B"], tok["C"], z=tok["z"],
                              D=prm["D"], dt_bias=prm["dt_bias"])
     else:
+        # The same call the benchmark times: the chunked entry point with a
+        # preallocated workspace and final-state buffer.
         x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
                                recipe=w["recipe"], device=dev)
+        y = torch.empty_like(x.u)
+        hf = torch.empty((w["batch"], w["dim"], w["dstate"]), dtype=torch.float32, device=dev)
+        ws = ssm.alloc_workspace(ssm.chunked_workspace_size(w["batch"], w["dim"], w["dstate"], w["seqlen"],
+                                                            w["ngroups"], x.u.dtype), dev)
         for _ in range(args.warmup + args.steps):
-            if w.get("final_state"):
-                ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias)
-            else:
-                ssm.scan_fwd(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias)
+            ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias, out=y,
+                                 h_final=hf, workspace=ws)
     torch.cuda.synchronize(dev)
     print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
+
+
+def write_traffic(csv_path, workload):
+    """Reads an ncu --csv metrics log (dram__bytes_read.sum, dram__bytes_write.sum
+    per launch) of `bench.py --profile <workload>` and records the DRAM bytes of
+    one chunked call (all of its kernels) in profiles/traffic.json, keyed by the
+    current kernel-source hash so that a later kernel change voids it."""
+    import csv
+    per_kernel = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if r]
+    hdr = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    cols = rows[hdr]
+    launches = {}
+    for r in rows[hdr + 1:]:
+        if len(r) != len(cols):
+            continue
+        d = dict(zip(cols, r))
+        if "scan_tma_kernel" not in d["Kernel Name"] and "scan_fwd_kernel" not in d["Kernel Name"]:
+            continue
+        name = d["Kernel Name"].split("(")[0]
+        unit = d.get("Metric Unit", "byte")
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(unit, 1)
+        key = (d["ID"], name)
+        launches.setdefault(key, 0.0)
+        if d["Metric Name"] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            launches[key] += float(d["Metric Value"].replace(",", "")) * scale
+    for (_, name), b in launches.items():
+        per_kernel.setdefault(name, []).append(b)
+    kernels = {k: sum(v) / len(v) for k, v in per_kernel.items()}
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    data["scan_chunked_call/" + workload] = {
+        "dram_bytes_per_launch": round(sum(kernels.values())),
+        "kernels": {k: round(v) for k, v in kernels.items()},
+        "source_hash": kernel_source_hash(),
+        "from": os.path.basename(csv_path)}
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+    print(json.dumps(data["scan_chunked_call/" + workload]))
 
 
 def main(argv=None):
@@ -565,7 +616,12 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", metavar="WORKLOAD", default=None,
                     help="only run W+K launches of one named workload (for ncu)")
+    ap.add_argument("--write-traffic", metavar="NCU_CSV", default=None,
+                    help="record the DRAM bytes of the headline call from an ncu metrics log")
     args = ap.parse_args(argv)
+    if args.write_traffic:
+        write_traffic(args.write_traffic, args.profile or HEADLINE)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.profile:

@@ -113,6 +113,18 @@ size_t ssm_scan_fwd_chunked_workspace_size(int batch, int dim, int dstate, int s
                                            int ngroups, ssm_dtype_t io);
 
 /*
+ * The launch plan ssm_scan_fwd_chunked (chunked != 0) or ssm_scan_fwd
+ * (chunked == 0) uses for this problem on the current process environment:
+ * *lanes = lanes sharing one channel's states, *chunks = time chunks, and
+ * *kernels = kernels one call enqueues (2 when chunks > 1: the summary pass
+ * and the fused pass; 1 otherwise).  *staged = 1 if the TMA-staged kernels
+ * run (row byte length a multiple of 16), 0 for the register-staged fallback.
+ * Host-only; returns SSM_ERR_INVALID_ARG / SSM_ERR_UNSUPPORTED like the scan.
+ */
+ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io,
+                           int chunked, int *lanes, int *chunks, int *kernels, int *staged);
+
+/*
  * ssm_scan_fwd_chunked -- selective scan with a caller-supplied initial state
  * and the final state returned; long sequences are split into time chunks
  * that run in parallel and are stitched by carrying each chunk's state into

@@ -165,6 +165,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     constexpr int P = S / 2;           // fp32x2 state pairs per lane
     constexpr int NQ = N / 2;          // state pairs per step
     constexpr int H = VPC / LANES;     // steps per lane per 16-byte chunk
+    // Per-step scalar work (softplus, Delta u, gate) in fp32x2 pairs of steps.
+    constexpr bool PACKED = !ACCURATE && (H % 2 == 0);
     constexpr int CH = Lay::CH;
     constexpr int THREADS = WARPS * 32;
     constexpr int STAGES = Lay::STAGES;
@@ -312,13 +314,29 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 float dv[H];
                 lds_row<T, H>(u_t + off, uu);
                 lds_row<T, H>(d_t + off, dv);
+                if constexpr (PACKED) {
 #pragma unroll
-                for (int k = 0; k < H; ++k) {
-                    dt[k] = softplus<ACCURATE>(dv[k] + bias);
-                    if constexpr (MASKED) {
-                        if (t0 + c * VPC + j * H + k >= p.seqlen) dt[k] = 0.f;
+                    for (int k = 0; k < H; k += 2) {
+                        const float2 v = __fadd2_rn(make_float2(dv[k], dv[k + 1]), make_float2(bias, bias));
+                        float2 d2 = softplus2_fast(v);
+                        if constexpr (MASKED) {
+                            const int t = t0 + c * VPC + j * H + k;
+                            if (t >= p.seqlen) d2.x = 0.f;
+                            if (t + 1 >= p.seqlen) d2.y = 0.f;
+                        }
+                        const float2 u2 = __fmul2_rn(d2, make_float2(uu[k], uu[k + 1]));
+                        dt[k] = d2.x; dt[k + 1] = d2.y;
+                        du[k] = u2.x; du[k + 1] = u2.y;
                     }
-                    du[k] = dt[k] * uu[k];
+                } else {
+#pragma unroll
+                    for (int k = 0; k < H; ++k) {
+                        dt[k] = softplus<ACCURATE>(dv[k] + bias);
+                        if constexpr (MASKED) {
+                            if (t0 + c * VPC + j * H + k >= p.seqlen) dt[k] = 0.f;
+                        }
+                        du[k] = dt[k] * uu[k];
+                    }
                 }
             }
             // The channel's lanes share (Delta, Delta, Delta u, Delta u) for
@@ -375,11 +393,21 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 float zz[H];
                 if (has_z) lds_row<T, H>(z_t + off, zz);
                 float out[H];
+                if constexpr (PACKED) {
 #pragma unroll
-                for (int k = 0; k < H; ++k) {
-                    float yv = fmaf(dsk, uu[k], acc[k]);
-                    if (has_z) yv *= silu<ACCURATE>(zz[k]);
-                    out[k] = yv;
+                    for (int k = 0; k < H; k += 2) {
+                        float2 y2 = __ffma2_rn(make_float2(dsk, dsk), make_float2(uu[k], uu[k + 1]),
+                                               make_float2(acc[k], acc[k + 1]));
+                        if (has_z) y2 = __fmul2_rn(y2, silu2_fast(make_float2(zz[k], zz[k + 1])));
+                        out[k] = y2.x; out[k + 1] = y2.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < H; ++k) {
+                        float yv = fmaf(dsk, uu[k], acc[k]);
+                        if (has_z) yv *= silu<ACCURATE>(zz[k]);
+                        out[k] = yv;
+                    }
                 }
                 sts_row<T, H>(u_t + off, out);  // y in place of u
             }

@@ -92,6 +92,30 @@ __device__ __forceinline__ float silu(float z) {
     }
 }
 
+// Two-lane (fp32x2) forms of the fast softplus and silu above, for two steps
+// at once: the same operations element by element, issued as packed FMA-pipe
+// instructions where the operation has a packed form.
+__device__ __forceinline__ float2 softplus2_fast(float2 v) {
+    const float w0 = ex2_approx(fabsf(v.x) * -kLog2e);
+    const float w1 = ex2_approx(fabsf(v.y) * -kLog2e);
+    const float2 w = make_float2(w0, w1);
+    float2 p = __ffma2_rn(w, make_float2(0.2f, 0.2f), make_float2(-0.25f, -0.25f));
+    p = __ffma2_rn(w, p, make_float2(0.33333334f, 0.33333334f));
+    p = __ffma2_rn(w, p, make_float2(-0.5f, -0.5f));
+    p = __ffma2_rn(w, p, make_float2(1.f, 1.f));
+    const float2 series = __fmul2_rn(w, p);
+    const float2 w1p = __fadd2_rn(w, make_float2(1.f, 1.f));
+    const float2 viaLog = __fmul2_rn(make_float2(lg2_approx(w1p.x), lg2_approx(w1p.y)), make_float2(kLn2, kLn2));
+    const float2 tail = make_float2(w0 < 0.03125f ? series.x : viaLog.x, w1 < 0.03125f ? series.y : viaLog.y);
+    return __fadd2_rn(make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f)), tail);
+}
+
+__device__ __forceinline__ float2 silu2_fast(float2 z) {
+    const float2 x = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
+    const float2 d = __fadd2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), make_float2(1.f, 1.f));
+    return __fmul2_rn(z, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
 // ---------------------------------------------------------------------------
 // Element conversion
 // ---------------------------------------------------------------------------

@@ -427,6 +427,27 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
 
 extern "C" {
 
+ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io, int chunked,
+                           int* lanes, int* chunks, int* kernels, int* staged) {
+    if (!lanes || !chunks || !kernels || !staged) return SSM_ERR_INVALID_ARG;
+    if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || ngroups <= 0 || dim % ngroups != 0)
+        return SSM_ERR_INVALID_ARG;
+    if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+    if (!supported_dstate(dstate)) return SSM_ERR_UNSUPPORTED;
+    *lanes = 0; *chunks = 0; *kernels = 0; *staged = 0;
+    if (batch == 0 || seqlen == 0) {
+        *kernels = (batch > 0 && chunked) ? 1 : 0;  // h_final copy for an empty sequence
+        return SSM_OK;
+    }
+    if (tma_eligible(seqlen, io) && !force_generic()) {
+        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunked != 0);
+        *lanes = plan.lanes; *chunks = plan.chunks; *kernels = plan.chunks > 1 ? 2 : 1; *staged = 1;
+    } else {
+        *lanes = 0; *chunks = 1; *kernels = 1; *staged = 0;
+    }
+    return SSM_OK;
+}
+
 int ssm_abi_version(void) { return SSM_ABI_VERSION; }
 
 const char* ssm_status_string(ssm_status_t s) {

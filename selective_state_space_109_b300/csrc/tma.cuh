@@ -1,8 +1,8 @@
 // tma.cuh -- thin inline-PTX wrappers for the sm_90+/sm_100 asynchronous copy
 // machinery used by the staged scan kernels: shared-memory mbarriers, tiled
 // TMA tensor loads and stores (cp.async.bulk.tensor), bulk-group completion
-// and the generic->async proxy fence.  Every wait here is bounded: a wait
-// that gives up records SSM_DEVICE_ERR_TIMEOUT in the library's device error
+// and the generic->async proxy fence.  Every wait here is bounded in wall
+// time: a wait that gives up records kDeviceErrTimeout in the library's device error
 // word (and, if given, in a caller status word) and returns false, so that a
 // kernel always runs to its end instead of hanging.
 #pragma once
@@ -20,10 +20,15 @@ constexpr unsigned kDeviceErrTimeout = 1u;
 // so this is its only definition); read and cleared by ssm_device_status.
 __device__ unsigned int g_ssm_device_error = 0;
 
-// Iterations of mbarrier.try_wait (each of which may itself suspend the
-// thread for a hardware-chosen interval) before a wait gives up.  A healthy
-// wait here lasts microseconds; the cap is many seconds of polling.
-constexpr uint32_t kWaitSpinLimit = 1u << 26;
+// Wall-clock budget of one wait (ns, read from %globaltimer).  A healthy wait
+// here lasts microseconds; after two seconds the wait gives up.
+constexpr unsigned long long kWaitBudgetNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,13 +62,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
-// Waits for the phase with the given parity to complete; bounded.
+// Waits for the phase with the given parity to complete; bounded by
+// kWaitBudgetNs of wall time.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
-    for (uint32_t i = 0; i < kWaitSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    atomicOr(&g_ssm_device_error, kDeviceErrTimeout);
-    if (status) atomicOr(status, kDeviceErrTimeout);
-    return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long start = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - start > kWaitBudgetNs) {
+            atomicOr(&g_ssm_device_error, kDeviceErrTimeout);
+            if (status) atomicOr(status, kDeviceErrTimeout);
+            return false;
+        }
+    }
+    return true;
 }
 
 // 2-D / 3-D tiled tensor loads global -> shared, completing on `bar`.

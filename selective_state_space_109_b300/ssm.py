@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
     L.ssm_scan_fwd_chunked.restype = I
     L.ssm_workspace_status.argtypes = [P, Z, P]
     L.ssm_workspace_status.restype = I
+    L.ssm_scan_plan.argtypes = [I] * 7 + [P] * 4
+    L.ssm_scan_plan.restype = I
     L.ssm_device_status.argtypes = [I, P]
     L.ssm_device_status.restype = I
     L.ssm_state_update.argtypes = [P] * 10 + [I] * 5 + [P]
@@ -134,6 +136,17 @@ def scan_fwd(u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None) -> to
     if st != 0:
         raise SsmError(st, "ssm_scan_fwd")
     return y
+
+
+def scan_plan(batch, dim, dstate, seqlen, ngroups, dtype, chunked=True) -> dict:
+    """The library's launch plan for this problem: lanes per channel, time
+    chunks, kernels per call and whether the TMA-staged kernels run."""
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    st = lib.ssm_scan_plan(batch, dim, dstate, seqlen, ngroups, _io_code(dtype), int(bool(chunked)),
+                           *[ctypes.byref(v) for v in vals])
+    if st != 0:
+        raise SsmError(st, "ssm_scan_plan")
+    return dict(lanes=vals[0].value, chunks=vals[1].value, kernels=vals[2].value, staged=bool(vals[3].value))
 
 
 def chunked_workspace_size(batch, dim, dstate, seqlen, ngroups, dtype) -> int:
