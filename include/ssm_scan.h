@@ -166,6 +166,44 @@ ssm_status_t ssm_scan_fwd_chunked(const void *u, const void *delta, const void *
 ssm_status_t ssm_workspace_status(const void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * ssm_scan_fwd_chunked_static -- ssm_scan_fwd_chunked for callers that cannot
+ * allocate device memory.  The source pages have no counterpart to this entry
+ * point; it exists for integration only.
+ *
+ * Who needs it: code that is handed only input and output pointers and has no
+ * way to obtain a scratch buffer.  Examples are a plugin inside an inference
+ * runtime or graph executor whose memory planner owns every device allocation
+ * (allocating behind its back breaks its budget, or fails once the pool is
+ * reserved), and latency-critical decode or streaming loops that must not call
+ * cudaMalloc/cudaFree, which can block until in-flight GPU work finishes.
+ *
+ * Arguments and results are exactly those of ssm_scan_fwd_chunked without
+ * workspace / workspace_bytes; inputs and outputs are still the caller's.  The
+ * chunk summaries and the status word live instead in one library-owned
+ * scratch array of SSM_STATIC_SCRATCH_BYTES in device global memory:
+ *   - every GPU that loads the library holds that array until the process exits;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current, so make the first call on
+ *     a device before any stream capture;
+ *   - all calls share the array, which keeps the previous call's contents (each
+ *     call clears the status word; the summaries are rewritten before they are
+ *     read): calls that can overlap on the GPU -- other streams, other host
+ *     threads -- race on it and must be serialised by the caller;
+ *   - the call allocates nothing: no cudaMalloc, cudaFree or allocating library.
+ * Problems whose summaries would exceed the array are rejected with
+ * SSM_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (the summaries take
+ * (chunks - 1) * batch * dim * 2 * dstate * 4 bytes, chunks <= 16, plus 256).
+ * A device-side timeout is reported by ssm_device_status.
+ */
+#define SSM_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+ssm_status_t ssm_scan_fwd_chunked_static(const void *u, const void *delta, const void *z,
+                                         const float *A, const void *B, const void *C,
+                                         const float *Dskip, const float *dt_bias,
+                                         const float *h0, void *y, float *h_final,
+                                         int batch, int dim, int dstate, int seqlen, int ngroups,
+                                         ssm_dtype_t io, void *stream);
+
+/*
  * Synchronises stream, then returns the library's device-wide error word for
  * the current device: SSM_OK, or SSM_ERR_TIMEOUT if any kernel of this library
  * gave up on a bounded device-side wait since the word was last cleared (its

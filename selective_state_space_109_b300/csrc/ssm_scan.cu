@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -423,6 +424,49 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
 }
 
 
+// ---------------------------------------------------------------------------
+// Scratch for the entry point that allocates nothing (ssm_scan_fwd_chunked_static)
+// ---------------------------------------------------------------------------
+
+// File-scope device array: loaded with the module on every device that uses the
+// library, held until exit.  Host code must not pass its name to a kernel (in
+// host code it is only a stand-in); the device address comes from
+// cudaGetSymbolAddress below.
+__device__ __align__(256) unsigned char g_static_scratch[SSM_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device; looked up once per
+// device, with that device current.
+ssm_status_t static_scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return SSM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_static_scratch_ptr[dev] = p;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return SSM_OK;
+}
+
+// Workspace bytes one chunked call actually uses (its own plan's chunks).
+size_t workspace_used(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io) {
+    size_t bytes = kWorkspaceHeader;
+    if (batch > 0 && tma_eligible(seqlen, io) && !force_generic()) {
+        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, true);
+        bytes += static_cast<size_t>(plan.chunks - 1) * static_cast<size_t>(batch) * static_cast<size_t>(dim) *
+                 2u * static_cast<size_t>(dstate) * sizeof(float);
+    }
+    return bytes;
+}
+
 }  // namespace
 
 extern "C" {
@@ -447,6 +491,28 @@ ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngrou
     }
     return SSM_OK;
 }
+
+ssm_status_t ssm_scan_fwd_chunked_static(const void* u, const void* delta, const void* z, const float* A,
+                                         const void* B, const void* C, const float* Dskip,
+                                         const float* dt_bias, const float* h0, void* y, float* h_final,
+                                         int batch, int dim, int dstate, int seqlen, int ngroups,
+                                         ssm_dtype_t io, void* stream) {
+    const ssm_status_t s = check_scan_args(u, delta, z, A, B, C, Dskip, dt_bias, y, h0, h_final,
+                                           batch, dim, dstate, seqlen, ngroups, io);
+    if (s != SSM_OK) return s;
+    if (batch == 0) return SSM_OK;
+    if (workspace_used(batch, dim, dstate, seqlen, ngroups, io) > SSM_STATIC_SCRATCH_BYTES)
+        return SSM_ERR_WORKSPACE_TOO_SMALL;
+    void* scratch = nullptr;
+    const ssm_status_t a = static_scratch_address(&scratch);
+    if (a != SSM_OK) return a;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, kWorkspaceHeader, st);  // status word starts at 0
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run_scan(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen, ngroups,
+                    io, scratch, st);
+}
+
 
 int ssm_abi_version(void) { return SSM_ABI_VERSION; }
 

@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
     L.ssm_scan_fwd_chunked.restype = I
     L.ssm_workspace_status.argtypes = [P, Z, P]
     L.ssm_workspace_status.restype = I
+    L.ssm_scan_fwd_chunked_static.argtypes = [P] * 11 + [I] * 6 + [P]
+    L.ssm_scan_fwd_chunked_static.restype = I
     L.ssm_scan_plan.argtypes = [I] * 7 + [P] * 4
     L.ssm_scan_plan.restype = I
     L.ssm_device_status.argtypes = [I, P]
