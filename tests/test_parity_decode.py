@@ -21,11 +21,20 @@ def run_step(ssm, state, tok, prm, **kw):
                             z=tok["z"], D=prm["D"], dt_bias=prm["dt_bias"], **kw)
 
 
+@pytest.fixture
+def path(request, monkeypatch):
+    if request.param is not None:
+        monkeypatch.setenv("SSM_FORCE_PATH", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("path", [None, "generic"], indirect=True)
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("N", [4, 8, 16])
 @pytest.mark.parametrize("G", [1, 2])
-def test_small_steps_whole_tensor(ssm, io, N, G):
-    batch, dim = 11, 70  # 70 channels: a partial CTA; 11 sequences: a partial batch chunk
+def test_small_steps_whole_tensor(ssm, io, N, G, path):
+    """Both decode kernels: bulk-staged (default) and register-staged."""
+    batch, dim = 11, 70  # 70 channels: a partial channel block; 11 sequences: a partial batch chunk
     prm = I.decode_params(dim, N, recipe="scaled", seed=1, device="cuda")
     state = I.make_decode_state(batch, dim, N, seed=1, device="cuda")
     ref_state = to_np(state)
@@ -71,3 +80,26 @@ def test_decode_b256_d5120_1024_steps_sampled(ssm):
     es = rel_l2(to_np(state[bs_t][:, ds_t]), ref_state)
     print(f"worst per-step y rel_l2 {worst:.3e}; state rel_l2 after {w['steps']} steps {es:.3e}")
     assert es <= STATE_REL_L2
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("dim,G", [(200, 1), (512, 2), (384, 1)])
+def test_staged_decode_steps(ssm, io, dim, G):
+    """Shapes the TMA-staged decode takes (N 16, 16-byte token rows, 128-channel
+    blocks inside a group): a ragged last block (200), two groups (512), and
+    full blocks (384); several consecutive steps on one state."""
+    batch, N = 13, 16
+    prm = I.decode_params(dim, N, recipe="scaled", seed=3, device="cuda")
+    state = I.make_decode_state(batch, dim, N, seed=3, device="cuda")
+    ref_state = to_np(state)
+    f = {k: to_np(v) for k, v in prm.items()}
+    for step in range(4):
+        tok = I.make_decode_token(batch, dim, N, step, ngroups=G, io=io, seed=3, device="cuda")
+        y = run_step(ssm, state, tok, prm)
+        torch.cuda.synchronize()
+        t = {k: to_np(v) for k, v in tok.items()}
+        ref_state, ref_y = oracle.state_update(ref_state, t["u"], t["delta"], f["A"], t["B"], t["C"],
+                                               z=t["z"], Dskip=f["D"], dt_bias=f["dt_bias"])
+        assert_close(to_np(y), ref_y, io, f"step {step}")
+        assert rel_l2(to_np(state), ref_state) <= STATE_REL_L2
+    assert ssm.device_status() == 0
