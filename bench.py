@@ -462,8 +462,9 @@ def run_ours(args):
         "tokens_channels_per_s": round(r["bdl_per_step"] / per_launch_s, 1),
         "roofline": {"bound": "alu", "achieved": round(alu_achieved, 1), "peak": round(alu_peak, 1),
                      "unit": "Gupd/s", "frac": round(alu_achieved / alu_peak, 4), "traffic": traffic,
-                     "kernel": ("scan_tma_kernel: summary pass + fused pass of one chunked call"
-                                if r["plan"]["kernels"] == 2 else "scan_tma_kernel: fused pass"),
+                     "kernel": ("scan_tma_kernel summary pass + scan_carry_kernel + scan_tma_kernel fused "
+                                "pass (one chunked call)" if r["plan"]["kernels"] > 1
+                                else "scan_tma_kernel fused pass"),
                      "plan": r["plan"],
                      "peak_basis": f"{sms} SMs x {sm_max:.0f} MHz x 32 state updates/SM/clk "
                                    "(MUFU.EX2 32/clk; FP32 128 lane-ops/clk at 4 per update)"},

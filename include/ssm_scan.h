@@ -116,8 +116,8 @@ size_t ssm_scan_fwd_chunked_workspace_size(int batch, int dim, int dstate, int s
  * The launch plan ssm_scan_fwd_chunked (chunked != 0) or ssm_scan_fwd
  * (chunked == 0) uses for this problem on the current process environment:
  * *lanes = lanes sharing one channel's states, *chunks = time chunks, and
- * *kernels = kernels one call enqueues (2 when chunks > 1: the summary pass
- * and the fused pass; 1 otherwise).  *staged = 1 if the TMA-staged kernels
+ * *kernels = kernels one call enqueues (3 when chunks > 1: the summary pass,
+ * the carry pass and the fused pass; 1 otherwise).  *staged = 1 if the TMA-staged kernels
  * run (row byte length a multiple of 16), 0 for the register-staged fallback.
  * Host-only; returns SSM_ERR_INVALID_ARG / SSM_ERR_UNSUPPORTED like the scan.
  */
@@ -142,11 +142,12 @@ ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngrou
  *               may run concurrently.  It holds a status word and, for
  *               time-chunked runs, one summary (P, E) per channel and chunk:
  *               P[n] = exp(A[d,n] * sum of Delta over the chunk) and E = the
- *               chunk's end state from a zero start.
+ *               chunk's end state from a zero start (after the call, E of
+ *               chunk c holds the state entering chunk c + 1).
  * When the sequence is long relative to the number of channels, the call
- * enqueues two kernels: a summary pass over every chunk but the last, then
- * the fused pass, where chunk c starts from h0 folded through the summaries
- * of chunks 0..c-1.  Device-side waits are bounded; if one gives up, the
+ * enqueues three kernels: a summary pass over every chunk but the last, a
+ * carry pass that turns the summaries into the state entering each chunk
+ * (h0 folded through the summaries of chunks 0..c-1), then the fused pass.  Device-side waits are bounded; if one gives up, the
  * kernel records SSM_ERR_TIMEOUT in the workspace, which ssm_workspace_status
  * reports.
  */

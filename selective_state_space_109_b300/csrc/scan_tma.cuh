@@ -8,7 +8,8 @@
 //              in registers (eightmm.github.io "Mamba", Main Claim and Scan
 //              View; intvml.com "DL0170 Mamba Selective SSM vs Attention",
 //              Mathematical Formulation).  A time chunk c > 0 starts from the
-//              state carried into it, folded from the chunk summaries below.
+//              state carried into it (computed by scan_carry_kernel from the
+//              chunk summaries below).
 //   Aggregate  the same recurrence over one time chunk from a zero state,
 //              without readout: it writes the chunk's summary, the pair
 //              (P, E) with P[n] = prod_t Abar_t[n] = exp(A[n] sum_t Delta_t)
@@ -219,15 +220,13 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
                 for (int k = 0; k < P; ++k) h[k] = __ldg(h0v + k);
             }
-            // Fold the summaries of the chunks before this one.
-            for (int c = 0; c < chunk; ++c) {
-                const float* agg = p.agg + (static_cast<long long>(c) * BD + bd) * (2 * N) + j * S;
+            // A later chunk starts from the state carried into it, which the
+            // carry pass left in the E slot of the previous chunk's summary.
+            if (chunk > 0 && active) {
+                const float2* carry = reinterpret_cast<const float2*>(
+                    p.agg + (static_cast<long long>(chunk - 1) * BD + bd) * (2 * N) + N + j * S);
 #pragma unroll
-                for (int k = 0; k < P; ++k) {
-                    const float2 Pc = __ldcg(reinterpret_cast<const float2*>(agg) + k);
-                    const float2 Ec = __ldcg(reinterpret_cast<const float2*>(agg + N) + k);
-                    h[k] = __ffma2_rn(Pc, h[k], Ec);
-                }
+                for (int k = 0; k < P; ++k) h[k] = __ldcg(carry + k);
             }
         }
     }
@@ -456,6 +455,39 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             const float2 x = __fmul2_rn(ds2, a2[k]);
             reinterpret_cast<float2*>(agg)[k] = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
             reinterpret_cast<float2*>(agg + N)[k] = h[k];
+        }
+    }
+}
+
+// Carry pass between the summary pass and the full pass.  For every channel
+// and state it turns the chunk summaries (P_c, E_c), c = 0..nchunks-2, into
+// the state entering each chunk, h_{c+1} = P_c * h_c + E_c from h_0 = h0 (or
+// zero), and stores h_{c+1} over E_c.  One thread per (channel, state pair)
+// issues every load before the short dependent chain of FMAs, so the chain
+// costs one memory latency instead of one per chunk.
+template <int N, int MAXC>
+__global__ void __launch_bounds__(256)
+scan_carry_kernel(float* __restrict__ agg, const float* __restrict__ h0, long long BD, int nchunks) {
+    constexpr int NP = N / 2;
+    const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (i >= BD * NP) return;
+    const long long bd = i / NP;
+    const int k = static_cast<int>(i % NP);
+    float2 Pc[MAXC - 1], Ec[MAXC - 1];
+#pragma unroll
+    for (int c = 0; c < MAXC - 1; ++c) {
+        if (c < nchunks - 1) {
+            const float2* a = reinterpret_cast<const float2*>(agg + (c * BD + bd) * (2 * N));
+            Pc[c] = __ldcg(a + k);
+            Ec[c] = __ldcg(a + NP + k);
+        }
+    }
+    float2 h = h0 ? __ldg(reinterpret_cast<const float2*>(h0 + bd * N) + k) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < MAXC - 1; ++c) {
+        if (c < nchunks - 1) {
+            h = __ffma2_rn(Pc[c], h, Ec[c]);
+            reinterpret_cast<float2*>(agg + (c * BD + bd) * (2 * N))[NP + k] = h;
         }
     }
 }

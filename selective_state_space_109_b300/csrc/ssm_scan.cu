@@ -370,6 +370,14 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
                           : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Aggregate>(m, p, dstate, plan.lanes,
                                                                                   plan.chunks - 1, st);
         if (e != cudaSuccess) return cuda_fail(e);
+        const long long BD = static_cast<long long>(batch) * dim;
+        const long long threads = BD * (dstate / 2);
+        const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+        if (dstate == 4) ssm::scan_carry_kernel<4, kMaxChunks><<<blocks, 256, 0, st>>>(agg, h0, BD, plan.chunks);
+        else if (dstate == 8) ssm::scan_carry_kernel<8, kMaxChunks><<<blocks, 256, 0, st>>>(agg, h0, BD, plan.chunks);
+        else ssm::scan_carry_kernel<16, kMaxChunks><<<blocks, 256, 0, st>>>(agg, h0, BD, plan.chunks);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st)
                       : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st);
@@ -578,7 +586,7 @@ ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngrou
     }
     if (tma_eligible(seqlen, io) && !force_generic()) {
         const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunked != 0);
-        *lanes = plan.lanes; *chunks = plan.chunks; *kernels = plan.chunks > 1 ? 2 : 1; *staged = 1;
+        *lanes = plan.lanes; *chunks = plan.chunks; *kernels = plan.chunks > 1 ? 3 : 1; *staged = 1;
     } else {
         *lanes = 0; *chunks = 1; *kernels = 1; *staged = 0;
     }
