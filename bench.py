@@ -577,7 +577,7 @@ def write_traffic(csv_path, workload):
         if len(r) != len(cols):
             continue
         d = dict(zip(cols, r))
-        if "scan_tma_kernel" not in d["Kernel Name"] and "scan_fwd_kernel" not in d["Kernel Name"]:
+        if not any(k in d["Kernel Name"] for k in ("scan_tma_kernel", "scan_fwd_kernel", "scan_carry_kernel")):
             continue
         name = d["Kernel Name"].split("(")[0]
         unit = d.get("Metric Unit", "byte")
