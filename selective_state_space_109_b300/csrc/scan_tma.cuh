@@ -220,14 +220,6 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
                 for (int k = 0; k < P; ++k) h[k] = __ldg(h0v + k);
             }
-            // A later chunk starts from the state carried into it, which the
-            // carry pass left in the E slot of the previous chunk's summary.
-            if (chunk > 0 && active) {
-                const float2* carry = reinterpret_cast<const float2*>(
-                    p.agg + (static_cast<long long>(chunk - 1) * BD + bd) * (2 * N) + N + j * S);
-#pragma unroll
-                for (int k = 0; k < P; ++k) h[k] = __ldcg(carry + k);
-            }
         }
     }
     const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
@@ -267,6 +259,21 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     };
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES && i < nt; ++i) issue(i);
+    }
+    if constexpr (FULL) {
+        // A later chunk starts from the state carried into it, which the carry
+        // pass left in the E slot of the previous chunk's summary.  This kernel
+        // may have started while that pass still ran (its input tiles are
+        // already on their way): wait for it before reading the carry.
+        if (chunk > 0) {
+            grid_dep_wait();
+            if (active) {
+                const float2* carry = reinterpret_cast<const float2*>(
+                    p.agg + (static_cast<long long>(chunk - 1) * BD + bd) * (2 * N) + N + j * S);
+#pragma unroll
+                for (int k = 0; k < P; ++k) h[k] = __ldcg(carry + k);
+            }
+        }
     }
 
     float dsum = 0.f;  // sum of Delta over the chunk (Aggregate)
@@ -436,6 +443,9 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             }
         }
     }
+    // Let the kernel that follows in the stream begin launching (it waits for
+    // this one's results before it reads them).
+    grid_dep_launch();
     if constexpr (FULL) {
         if (threadIdx.x == 0) bulk_wait<0>();
     }
@@ -469,6 +479,8 @@ template <int N, int MAXC>
 __global__ void __launch_bounds__(256)
 scan_carry_kernel(float* __restrict__ agg, const float* __restrict__ h0, long long BD, int nchunks) {
     constexpr int NP = N / 2;
+    grid_dep_launch();
+    grid_dep_wait();  // the summaries of the summary pass
     const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (i >= BD * NP) return;
     const long long bd = i / NP;

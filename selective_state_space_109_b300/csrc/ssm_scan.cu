@@ -307,9 +307,21 @@ cudaError_t launch_tma(const ScanMaps& m, const ssm::TmaScanParams& p, int grid_
     if (e != cudaSuccess) return e;
     const long long gx = static_cast<long long>(p.blocks_per_group) * p.ngroups * p.batch;
     if (gx > 0x7fffffffLL || grid_y > 65535) return cudaErrorInvalidConfiguration;
-    kern<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(grid_y)), kTmaWarps * 32, Lay::SMEM_BYTES, st>>>(
-        m.u, m.d, m.z, m.y, m.B, m.C, p);
-    return cudaGetLastError();
+    // The full pass of a chunked call follows the carry pass: launch it with
+    // programmatic stream serialization so that its prologue (barriers, the
+    // first input tiles) overlaps that pass; it waits before reading the carry.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(grid_y));
+    cfg.blockDim = dim3(kTmaWarps * 32);
+    cfg.dynamicSmemBytes = Lay::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    const bool pdl = MODE == ssm::ScanMode::Full && p.nchunks > 1;
+    cfg.attrs = pdl ? &attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, m.u, m.d, m.z, m.y, m.B, m.C, p);
 }
 
 template <typename T, int N, ssm::ScanMode MODE>
@@ -373,10 +385,20 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
         const long long BD = static_cast<long long>(batch) * dim;
         const long long threads = BD * (dstate / 2);
         const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-        if (dstate == 4) ssm::scan_carry_kernel<4, kMaxChunks><<<blocks, 256, 0, st>>>(agg, h0, BD, plan.chunks);
-        else if (dstate == 8) ssm::scan_carry_kernel<8, kMaxChunks><<<blocks, 256, 0, st>>>(agg, h0, BD, plan.chunks);
-        else ssm::scan_carry_kernel<16, kMaxChunks><<<blocks, 256, 0, st>>>(agg, h0, BD, plan.chunks);
-        e = cudaGetLastError();
+        // The carry pass waits for the summary pass in-kernel (programmatic
+        // stream serialization), so its launch overlaps the summary pass's tail.
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (dstate == 4) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<4, kMaxChunks>, agg, h0, BD, plan.chunks);
+        else if (dstate == 8) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<8, kMaxChunks>, agg, h0, BD, plan.chunks);
+        else e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<16, kMaxChunks>, agg, h0, BD, plan.chunks);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st)

@@ -136,6 +136,14 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream still runs;
+// grid_dep_wait() blocks until that kernel has completed and its writes are
+// visible (a no-op without the launch attribute), and grid_dep_launch() lets
+// the next such kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Byte offset of 16-byte chunk c (0..3) of row r inside a tile whose rows are
 // 64 bytes and which TMA wrote with CU_TENSOR_MAP_SWIZZLE_64B: address bits
 // [4:5] are XOR-ed with bits [7:8], i.e. with (r >> 1) & 3.  The tile base must
