@@ -276,7 +276,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         }
     }
 
-    float dsum = 0.f;  // sum of Delta over the chunk (Aggregate)
+    float dsum = 0.f;   // sum of Delta over the chunk (Aggregate)
+    float dcomp = 0.f;  // its running compensation (fp32 I/O)
 
 #pragma unroll 1
     for (int i = 0; i < nt; ++i) {
@@ -368,7 +369,18 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                     du2 = make_float2(e.z, e.w);
                 }
                 const int row = c * VPC + kk;
-                if constexpr (!FULL) dsum += dt2.x;
+                if constexpr (!FULL) {
+                    if constexpr (ACCURATE) {
+                        // Compensated (Kahan) sum: P = exp(A * sum Delta) must match
+                        // the product of the per-step decays to fp32 accuracy.
+                        const float yk = dt2.x - dcomp;
+                        const float tk = dsum + yk;
+                        dcomp = (tk - dsum) - yk;
+                        dsum = tk;
+                    } else {
+                        dsum += dt2.x;
+                    }
+                }
                 if constexpr (FULL) {
                     const float4* q4 = reinterpret_cast<const float4*>(bcf) + row * NQ + j * P;
                     float2 y2 = make_float2(0.f, 0.f);

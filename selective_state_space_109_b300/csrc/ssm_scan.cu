@@ -154,6 +154,7 @@ int max_chunks_for(int seqlen, ssm_dtype_t io) {
 struct ScanPlan {
     int lanes;
     int chunks;
+    int agg_lanes;  // lanes of the summary pass (chunks > 1)
 };
 
 template <typename T, int N, ssm::ScanMode MODE>
@@ -210,21 +211,37 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
     // Time units: one unit ~ one channel-step of a 16-state lane at full rate;
     // ~0.54 ns per unit on B300 at N = 16.
     const double launch_units = 2000.0 / 0.54 * (16.0 / dstate);
-    ScanPlan best{1, 1};
+    ScanPlan best{1, 1, 1};
     double best_cost = 1e300;
     for (int lanes = 1; lanes <= lmax; lanes *= 2) {
         const double lane_cost = lanes == 1 ? 1.0 : (lanes == 2 ? 1.4 : 2.0);
         const int ch = kTmaWarps * 32 / lanes;
         const long long blocks = static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
         const int cap_full = ctas_per_sm(tma_smem_for<ssm::ScanMode::Full>(io, dstate, lanes));
-        const int cap_agg = ctas_per_sm(tma_smem_for<ssm::ScanMode::Aggregate>(io, dstate, lanes));
         for (int k = 1; k <= kmax; ++k) {
-            const double work = lane_cost * ch * (static_cast<double>(seqlen) / k) * (dstate / 16.0);
-            double cost = pass_time(blocks * k, cap_full, work);
-            if (k > 1) cost += pass_time(blocks * (k - 1), cap_agg, 0.9 * work) + launch_units;
+            const double steps = (static_cast<double>(seqlen) / k) * (dstate / 16.0);
+            double cost = pass_time(blocks * k, cap_full, lane_cost * ch * steps);
+            int best_agg = lanes;
+            if (k > 1) {
+                // The summary pass picks its own lanes (no readout to reduce:
+                // cheaper lane sharing, 1.0 / 1.2 / 1.6 measured).
+                double agg_cost = 1e300;
+                for (int la = 1; la <= lmax; la *= 2) {
+                    const double la_cost = la == 1 ? 1.0 : (la == 2 ? 1.2 : 1.6);
+                    const int cha = kTmaWarps * 32 / la;
+                    const long long blocks_a = static_cast<long long>((dpg + cha - 1) / cha) * ngroups * batch;
+                    const int cap_agg = ctas_per_sm(tma_smem_for<ssm::ScanMode::Aggregate>(io, dstate, la));
+                    const double c = pass_time(blocks_a * (k - 1), cap_agg, 0.9 * la_cost * cha * steps);
+                    if (c < agg_cost * 0.999) {
+                        agg_cost = c;
+                        best_agg = la;
+                    }
+                }
+                cost += agg_cost + launch_units;
+            }
             if (cost < best_cost * 0.999) {
                 best_cost = cost;
-                best = {lanes, k};
+                best = {lanes, k, best_agg};
             }
         }
     }
@@ -232,6 +249,9 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
     if ((fl == 1 || fl == 2 || fl == 4) && fl <= lmax) best.lanes = fl;
     const int fk = env_int("SSM_FORCE_CHUNKS", 0);
     if (fk >= 1) best.chunks = std::min(fk, kmax);
+    if (fl || fk) best.agg_lanes = best.lanes;
+    const int fa = env_int("SSM_FORCE_AGG_LANES", 0);
+    if ((fa == 1 || fa == 2 || fa == 4) && fa <= lmax) best.agg_lanes = fa;
     return best;
 }
 
@@ -378,8 +398,19 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
 
     cudaError_t e = cudaSuccess;
     if (plan.chunks > 1) {
-        e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Aggregate>(m, p, dstate, plan.lanes, plan.chunks - 1, st)
-                          : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Aggregate>(m, p, dstate, plan.lanes,
+        // The summary pass may share a channel's states over more lanes than
+        // the full pass (it has no readout to reduce): more resident warps.
+        int agg_lanes = plan.agg_lanes;
+        ScanMaps ma = m;
+        ssm::TmaScanParams pa = p;
+        if (agg_lanes != plan.lanes) {
+            const int cha = kTmaWarps * 32 / agg_lanes;
+            if (!encode_act(&ma.u, u, io, seqlen, dpg, bg, cha) || !encode_act(&ma.d, delta, io, seqlen, dpg, bg, cha))
+                return cuda_fail(cudaErrorInvalidValue);
+            pa.blocks_per_group = (dpg + cha - 1) / cha;
+        }
+        e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Aggregate>(ma, pa, dstate, agg_lanes, plan.chunks - 1, st)
+                          : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Aggregate>(ma, pa, dstate, agg_lanes,
                                                                                   plan.chunks - 1, st);
         if (e != cudaSuccess) return cuda_fail(e);
         const long long BD = static_cast<long long>(batch) * dim;
