@@ -151,8 +151,18 @@ __device__ __forceinline__ float lds_elem(const unsigned char* p) {
     }
 }
 
+// CTAs that shared memory lets reside on one SM (228 KB, 1 KB reserved per
+// CTA): passed to __launch_bounds__ so that ptxas may use every register that
+// this residency leaves free.
+template <typename T, int N, int LANES, int WARPS, ScanMode MODE>
+constexpr int tma_min_blocks() {
+    constexpr int per = TmaScanLayout<T, N, LANES, WARPS, MODE>::SMEM_BYTES + 1024;
+    constexpr int b = (228 * 1024) / per;
+    return b < 1 ? 1 : (b > 5 ? 5 : b);
+}
+
 template <typename T, int N, int LANES, int WARPS, ScanMode MODE, bool ACCURATE>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, (tma_min_blocks<T, N, LANES, WARPS, MODE>()))
 scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_y,
                 const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
