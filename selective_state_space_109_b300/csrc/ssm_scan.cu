@@ -224,10 +224,10 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
             int best_agg = lanes;
             if (k > 1) {
                 // The summary pass picks its own lanes (no readout to reduce:
-                // cheaper lane sharing, 1.0 / 1.2 / 1.6 measured).
+                // cheaper lane sharing, 1.0 / 1.3 / 1.7 measured).
                 double agg_cost = 1e300;
                 for (int la = 1; la <= lmax; la *= 2) {
-                    const double la_cost = la == 1 ? 1.0 : (la == 2 ? 1.2 : 1.6);
+                    const double la_cost = la == 1 ? 1.0 : (la == 2 ? 1.3 : 1.7);
                     const int cha = kTmaWarps * 32 / la;
                     const long long blocks_a = static_cast<long long>((dpg + cha - 1) / cha) * ngroups * batch;
                     const int cap_agg = ctas_per_sm(tma_smem_for<ssm::ScanMode::Aggregate>(io, dstate, la));
