@@ -76,7 +76,9 @@ struct TmaScanLayout {
     static constexpr int BC_BYTES = N * TileShape<T>::kRowBytes;    // one B or C tile
     static constexpr int NACT = FULL ? 3 : 2;                       // u, delta (, z)
     static constexpr int NBC = FULL ? 2 : 1;                        // B (, C)
-    static constexpr int STAGES = 3;
+    // The full pass refills a stage only after its y store has read it, so it
+    // runs STAGES - 2 tiles ahead; the summary pass runs STAGES - 1 ahead.
+    static constexpr int STAGES = FULL ? 4 : 3;
     static constexpr int STAGE_BYTES = ((NACT * ACT_BYTES + NBC * BC_BYTES) + 1023) / 1024 * 1024;
     static constexpr int BCF_BYTES = TileShape<T>::TS * N * 4 * NBC;  // widened B (, C)
     // Per-warp scratch through which the lanes of a channel share (Delta,
