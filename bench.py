@@ -270,39 +270,68 @@ def bench_scan_device(ssm, I, torch, w, steps, warmup, sampler=None, preroll_s=1
 
 
 def bench_scan_e2e(ssm, I, torch, w, steps, warmup):
-    """End to end through the public API: pinned host inputs -> device -> scan -> host y."""
+    """End to end through the public API: every step copies its inputs from
+    pinned host memory to the device, runs the chunked scan and copies y back
+    to pinned host memory.  Steps are pipelined over three streams (copy-in,
+    compute, copy-out) with two device buffer sets, so that the copies of one
+    step overlap the compute and copies of its neighbours; every copy of every
+    step is inside the timed region."""
     dev = torch.device("cuda")
     x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
                            recipe=w["recipe"], seed=100, device="cpu")
     names = ["u", "delta", "z", "B", "C"]
     host = {n: getattr(x, n).pin_memory() for n in names}
-    devt = {n: torch.empty_like(host[n], device=dev) for n in names}
     params = {n: getattr(x, n).to(dev) for n in ["A", "D", "dt_bias"]}
-    y_dev = torch.empty_like(devt["u"])
-    y_host = torch.empty_like(host["u"]).pin_memory()
-    hf_dev = torch.empty((w["batch"], w["dim"], w["dstate"]), dtype=torch.float32, device=dev)
-    ws = ssm.alloc_workspace(ssm.chunked_workspace_size(w["batch"], w["dim"], w["dstate"], w["seqlen"],
-                                                        w["ngroups"], host["u"].dtype), dev)
+    nbuf = 2
+    devt = [{n: torch.empty_like(host[n], device=dev) for n in names} for _ in range(nbuf)]
+    y_dev = [torch.empty_like(devt[0]["u"]) for _ in range(nbuf)]
+    y_host = [torch.empty_like(host["u"]).pin_memory() for _ in range(nbuf)]
+    hf_dev = [torch.empty((w["batch"], w["dim"], w["dstate"]), dtype=torch.float32, device=dev)
+              for _ in range(nbuf)]
+    need = ssm.chunked_workspace_size(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"],
+                                      host["u"].dtype)
+    ws = [ssm.alloc_workspace(need, dev) for _ in range(nbuf)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = y_host.numel() * y_host.element_size()
+    d2h = y_host[0].numel() * y_host[0].element_size()
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_cmp = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    for e in ev_cmp + ev_out:
+        e.record(torch.cuda.current_stream(dev))
 
-    def step():
-        for n in names:
-            devt[n].copy_(host[n], non_blocking=True)
-        ssm.scan_fwd_chunked(devt["u"], devt["delta"], params["A"], devt["B"], devt["C"], z=devt["z"],
-                             D=params["D"], dt_bias=params["dt_bias"], out=y_dev, h_final=hf_dev,
-                             workspace=ws)
-        y_host.copy_(y_dev, non_blocking=True)
+    def step(i):
+        k = i % nbuf
+        s_in.wait_event(ev_cmp[k])           # the compute that last read this buffer set is done
+        with torch.cuda.stream(s_in):
+            for n in names:
+                devt[k][n].copy_(host[n], non_blocking=True)
+            ev_in[k].record(s_in)
+        s_cmp.wait_event(ev_in[k])
+        s_cmp.wait_event(ev_out[k])          # y of this buffer set has been read back
+        with torch.cuda.stream(s_cmp):
+            d = devt[k]
+            ssm.scan_fwd_chunked(d["u"], d["delta"], params["A"], d["B"], d["C"], z=d["z"], D=params["D"],
+                                 dt_bias=params["dt_bias"], out=y_dev[k], h_final=hf_dev[k], workspace=ws[k])
+            ev_cmp[k].record(s_cmp)
+        s_out.wait_event(ev_cmp[k])
+        with torch.cuda.stream(s_out):
+            y_host[k].copy_(y_dev[k], non_blocking=True)
+            ev_out[k].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
+    e0.record(s_in)
+    s_cmp.wait_stream(s_in)
+    s_out.wait_stream(s_in)
+    for i in range(steps):
+        step(i)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_cmp)
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1)
     return dict(ms_per_step=ms / steps, h2d=h2d, d2h=d2h)
