@@ -30,7 +30,7 @@ import numpy as np
 import torch
 
 _TENSOR_IDS = {"u": 1, "delta": 2, "z": 3, "B": 4, "C": 5, "D": 6, "dt": 7,
-               "h0": 8, "state": 9}
+               "h0": 8, "state": 9, "A": 10}
 
 
 def _subseed(seed: int, name: str, step: int = 0) -> int:
@@ -68,6 +68,12 @@ def dt_bias_values(dim: int, seed: int, device="cpu") -> torch.Tensor:
 def a_values(dim: int, dstate: int, device="cpu") -> torch.Tensor:
     """A[d, n] = -(n + 1) for every channel."""
     return (-(torch.arange(dstate, dtype=torch.float32) + 1.0)).repeat(dim, 1).to(device)
+
+
+def a_values_random(dim: int, dstate: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """A[d, n] = -U(0.5, 16.5), drawn per element: no structure across n."""
+    g = _gen(seed, "A", "cpu")
+    return (-(0.5 + 16.0 * torch.rand((dim, dstate), generator=g, dtype=torch.float32))).to(device)
 
 
 @dataclass

@@ -155,3 +155,16 @@ def test_summary_pass_with_other_lanes(ssm, env, io, monkeypatch):
     else:
         assert rel_l2(to_np(y), ref_y) <= 1e-5
     assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_random_A(ssm, env, io):
+    """A drawn per element (no pattern across states), time-chunked."""
+    env(chunks=3)
+    x = I.make_scan_inputs(2, 96, 16, 320, 1, io=io, recipe="scaled", seed=38, device="cuda", with_h0=True)
+    x.A = I.a_values_random(96, 16, seed=38, device="cuda")
+    y, hf = chunked(ssm, x, h0=x.h0)
+    torch.cuda.synchronize()
+    ref_y, ref_h = oracle_scan(x, h0=x.h0, final_state=True)
+    assert_close(to_np(y), ref_y, io, "random A")
+    assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
