@@ -191,9 +191,11 @@ ssm_status_t ssm_workspace_status(const void *workspace, size_t workspace_bytes,
  *     read): calls that can overlap on the GPU -- other streams, other host
  *     threads -- race on it and must be serialised by the caller;
  *   - the call allocates nothing: no cudaMalloc, cudaFree or allocating library.
- * Problems whose summaries would exceed the array are rejected with
- * SSM_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (the summaries take
- * (chunks - 1) * batch * dim * 2 * dstate * 4 bytes, chunks <= 16, plus 256).
+ * The launch plan uses at most as many time chunks as the array holds
+ * summaries for ((chunks - 1) * batch * dim * 2 * dstate * 4 bytes plus 256),
+ * down to a single unsplit pass, so no problem is rejected for its size; the
+ * result differs from ssm_scan_fwd_chunked's only where that cap changes the
+ * chunking (fp32 rounding order).
  * A device-side timeout is reported by ssm_device_status.
  */
 #define SSM_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)

@@ -20,10 +20,13 @@
 //
 // Data movement: every operand tile arrives by TMA into shared memory.  A CTA
 // owns CH consecutive channels of one (sequence, group) and one time chunk; it
-// walks the chunk in tiles of TS steps (64 bytes of each channel row), through
-// a 4-stage ring of mbarrier-tracked stages.  Activation tiles (u, delta, z)
-// are [CH rows x 64 B] with 64-byte swizzle, so that the lanes of a warp, each
-// reading its own row, hit distinct banks.  B and C tiles ([N rows x 64 B],
+// walks the chunk in tiles of TS steps (kScanRowBytes = 32 bytes of each
+// channel row), through a 4-stage ring of mbarrier-tracked stages.  Activation
+// tiles (u, delta, z) are [CH rows x 32 B] with the TMA swizzle of that row
+// width, so that the lanes of a warp, each reading its own row, hit distinct
+// banks.  Narrow rows keep a CTA's stages small (13 KB per stage of the full
+// pass), so that four CTAs -- four warps per scheduler -- fit on an SM.  B and
+// C tiles ([N rows x 32 B],
 // shared by all channels of the group) are widened once per tile into fp32
 // (B_n, B_n+1, C_n, C_n+1) quads that every lane reads by broadcast.  y is
 // written back in place over the u tile and leaves by a TMA store.
@@ -60,9 +63,23 @@ struct TmaScanParams {
 
 enum class ScanMode { Full, Aggregate };
 
+// Bytes of each channel row in one tile: 32 (TMA 32-byte swizzle) or 64
+// (64-byte swizzle).  The build may override it to compare the two.
+#ifndef SSM_SCAN_ROW_BYTES
+#define SSM_SCAN_ROW_BYTES 32
+#endif
+constexpr int kScanRowBytes = SSM_SCAN_ROW_BYTES;
+static_assert(kScanRowBytes == 32 || kScanRowBytes == 64, "tile rows are 32 or 64 bytes");
+
+// Byte offset of 16-byte chunk c of row r in an activation tile.
+__device__ __forceinline__ uint32_t swz_act(int r, int c) {
+    if constexpr (kScanRowBytes == 64) return swz64(r, c);
+    else return swz32(r, c);
+}
+
 template <typename T>
 struct TileShape {
-    static constexpr int kRowBytes = 64;
+    static constexpr int kRowBytes = kScanRowBytes;
     static constexpr int TS = kRowBytes / static_cast<int>(sizeof(T));  // steps per tile
     static constexpr int VPC = 16 / static_cast<int>(sizeof(T));        // steps per 16-byte chunk
     static constexpr int CHUNKS = kRowBytes / 16;
@@ -90,7 +107,7 @@ struct TmaScanLayout {
     static constexpr int XS_OFFSET = STAGES * STAGE_BYTES + BCF_BYTES;
     static constexpr int BAR_OFFSET = XS_OFFSET + XS_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFFSET + STAGES * 8 + 1024;  // + alignment slack
-    static_assert(ACT_BYTES % 512 == 0, "activation tiles must keep the 64-byte swizzle phase");
+    static_assert(ACT_BYTES % (8 * TileShape<T>::kRowBytes) == 0, "activation tiles must keep the swizzle phase");
 };
 
 // Loads H consecutive elements (H * sizeof(T) = 4, 8 or 16 bytes) from shared memory.
@@ -153,14 +170,18 @@ __device__ __forceinline__ float lds_elem(const unsigned char* p) {
     }
 }
 
+// Most CTAs of one kernel planned per SM: four (four warps per scheduler)
+// saturate the update mix, and more would cut registers below 128 a thread.
+constexpr int kMaxCtasPerSm = 4;
+
 // CTAs that shared memory lets reside on one SM (228 KB, 1 KB reserved per
-// CTA): passed to __launch_bounds__ so that ptxas may use every register that
-// this residency leaves free.
+// CTA), at most kMaxCtasPerSm: passed to __launch_bounds__ so that ptxas may
+// use every register that this residency leaves free.
 template <typename T, int N, int LANES, int WARPS, ScanMode MODE>
 constexpr int tma_min_blocks() {
     constexpr int per = TmaScanLayout<T, N, LANES, WARPS, MODE>::SMEM_BYTES + 1024;
     constexpr int b = (228 * 1024) / per;
-    return b < 1 ? 1 : (b > 5 ? 5 : b);
+    return b < 1 ? 1 : (b > kMaxCtasPerSm ? kMaxCtasPerSm : b);
 }
 
 template <typename T, int N, int LANES, int WARPS, ScanMode MODE, bool ACCURATE>
@@ -327,7 +348,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         // (Abar = 1, no input: the state passes through unchanged).
         auto run_chunk = [&](const int c, auto masked) {
             constexpr bool MASKED = decltype(masked)::value;
-            const uint32_t off = swz64(r, c) + j * H * static_cast<int>(sizeof(T));
+            const uint32_t off = swz_act(r, c) + j * H * static_cast<int>(sizeof(T));
             float uu[H], dt[H], du[H];
             {
                 float dv[H];

@@ -133,12 +133,12 @@ constexpr int kTmaWarps = 4;
 // The time-chunk plan aims to fill a B300 (148 SMs).  It is a function of the
 // problem's arguments only, so the workspace size query needs no device.
 constexpr int kPlanSms = 148;
-constexpr int kMaxChunks = 16;
+constexpr int kMaxChunks = 32;
 
 // Workspace header: the device-side status word written by kernels that wait.
 constexpr size_t kWorkspaceHeader = 256;
 
-int tma_steps_per_tile(ssm_dtype_t io) { return io == SSM_F32 ? 16 : 32; }
+int tma_steps_per_tile(ssm_dtype_t io) { return ssm::kScanRowBytes / (io == SSM_F32 ? 4 : 2); }
 
 // Rows of every tensor must start on 16-byte boundaries for TMA.
 bool tma_eligible(int seqlen, ssm_dtype_t io) {
@@ -177,8 +177,11 @@ int tma_smem_for(ssm_dtype_t io, int dstate, int lanes) {
 }
 
 // CTAs that fit on one SM by shared memory (228 KB per SM, 1 KB of it
-// reserved per CTA).
-int ctas_per_sm(int smem_bytes) { return std::max(1, (228 * 1024) / (smem_bytes + 1024)); }
+// reserved per CTA), at most the kMaxCtasPerSm that the kernels' launch
+// bounds plan registers for.
+int ctas_per_sm(int smem_bytes) {
+    return std::max(1, std::min(ssm::kMaxCtasPerSm, (228 * 1024) / (smem_bytes + 1024)));
+}
 
 // Relative SM throughput with c resident CTAs (c warps per scheduler), from a
 // measurement of the scan's update mix on B300: one warp per scheduler
@@ -199,22 +202,26 @@ double pass_time(long long ctas, int cap, double work) {
     return t;
 }
 
-// Picks lanes per channel and time chunks by a wave model of the two passes.
-// Per-update cost of sharing a channel's states over 2 or 4 lanes (measured
-// on B300 against one lane at equal occupancy): 1.4 and 2.0; the summary pass
-// costs 0.9 of a full pass; a second kernel launch costs about 2 us.
+// Picks lanes per channel and time chunks by a wave model of the two passes,
+// fitted to B300 timings of the three bf16 scan workloads over plans of 1 to 32
+// chunks and 1, 2 or 4 lanes.  Per-update cost of sharing a channel's states
+// over 2 or 4 lanes: 1.2 and 2.0 in the full pass, 1.1 and 1.7 in the summary
+// pass (no readout to reduce); the summary pass costs 0.9 of a full pass; the
+// two extra kernels cost about 2 us, and each chunk about 0.65 us more (every
+// chunk's CTAs fetch their first tiles at once when the kernel starts).
 ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io,
-                   bool allow_chunks) {
+                   int chunk_cap) {
     const int dpg = dim / ngroups;
-    const int kmax = allow_chunks ? max_chunks_for(seqlen, io) : 1;
+    const int kmax = std::max(1, std::min(chunk_cap, max_chunks_for(seqlen, io)));
     const int lmax = dstate >= 8 ? 4 : 2;
     // Time units: one unit ~ one channel-step of a 16-state lane at full rate;
     // ~0.54 ns per unit on B300 at N = 16.
     const double launch_units = 2000.0 / 0.54 * (16.0 / dstate);
+    const double chunk_units = 650.0 / 0.54 * (16.0 / dstate);
     ScanPlan best{1, 1, 1};
     double best_cost = 1e300;
     for (int lanes = 1; lanes <= lmax; lanes *= 2) {
-        const double lane_cost = lanes == 1 ? 1.0 : (lanes == 2 ? 1.4 : 2.0);
+        const double lane_cost = lanes == 1 ? 1.0 : (lanes == 2 ? 1.2 : 2.0);
         const int ch = kTmaWarps * 32 / lanes;
         const long long blocks = static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
         const int cap_full = ctas_per_sm(tma_smem_for<ssm::ScanMode::Full>(io, dstate, lanes));
@@ -224,10 +231,10 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
             int best_agg = lanes;
             if (k > 1) {
                 // The summary pass picks its own lanes (no readout to reduce:
-                // cheaper lane sharing, 1.0 / 1.3 / 1.7 measured).
+                // cheaper lane sharing).
                 double agg_cost = 1e300;
                 for (int la = 1; la <= lmax; la *= 2) {
-                    const double la_cost = la == 1 ? 1.0 : (la == 2 ? 1.3 : 1.7);
+                    const double la_cost = la == 1 ? 1.0 : (la == 2 ? 1.1 : 1.7);
                     const int cha = kTmaWarps * 32 / la;
                     const long long blocks_a = static_cast<long long>((dpg + cha - 1) / cha) * ngroups * batch;
                     const int cap_agg = ctas_per_sm(tma_smem_for<ssm::ScanMode::Aggregate>(io, dstate, la));
@@ -237,7 +244,7 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
                         best_agg = la;
                     }
                 }
-                cost += agg_cost + launch_units;
+                cost += agg_cost + launch_units + chunk_units * k;
             }
             if (cost < best_cost * 0.999) {
                 best_cost = cost;
@@ -278,17 +285,18 @@ struct ScanMaps {
 };
 
 // [batch * ngroups, dim_per_group, seqlen] activation view; box = one tile of
-// 64 bytes per row times `rows` channels, 64-byte swizzle.
+// kScanRowBytes per row times `rows` channels, swizzled at that row width.
 bool encode_act(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, int dpg, long long bg, int rows) {
     const cuuint64_t es = io == SSM_F32 ? 4 : 2;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(dpg),
                                 static_cast<cuuint64_t>(bg)};
     const cuuint64_t strides[2] = {seqlen * es, seqlen * es * dpg};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(64 / es), static_cast<cuuint32_t>(rows), 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(ssm::kScanRowBytes / es), static_cast<cuuint32_t>(rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle swz = ssm::kScanRowBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     return encode_tiled()(m, io == SSM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -297,7 +305,7 @@ bool encode_bc(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, long
     const cuuint64_t es = io == SSM_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {seqlen * es};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / es), static_cast<cuuint32_t>(dstate)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(ssm::kScanRowBytes / es), static_cast<cuuint32_t>(dstate)};
     const cuuint32_t estr[2] = {1, 1};
     return encode_tiled()(m, io == SSM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                           const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -540,10 +548,22 @@ __global__ void copy_or_zero_state_kernel(const float* __restrict__ h0, float* _
     if (i < n) hf[i] = h0 ? h0[i] : 0.f;
 }
 
+// Time chunks whose summaries fit in `bytes` of workspace (at least 1).
+int chunks_fitting(size_t bytes, int batch, int dim, int dstate) {
+    if (bytes < kWorkspaceHeader) return 1;
+    const size_t per = static_cast<size_t>(batch) * static_cast<size_t>(dim) * 2u * static_cast<size_t>(dstate) *
+                       sizeof(float);
+    const size_t k = 1 + (bytes - kWorkspaceHeader) / std::max<size_t>(per, 1);
+    return static_cast<int>(std::min<size_t>(k, kMaxChunks));
+}
+
+// workspace == nullptr: single pass, no time split.  Otherwise the plan uses
+// at most the chunks whose summaries fit in workspace_bytes.
 ssm_status_t run_scan(const void* u, const void* delta, const void* z, const float* A,
                       const void* B, const void* C, const float* Dskip, const float* dt_bias,
                       const float* h0, void* y, float* h_final, int batch, int dim, int dstate,
-                      int seqlen, int ngroups, ssm_dtype_t io, void* workspace, cudaStream_t st) {
+                      int seqlen, int ngroups, ssm_dtype_t io, void* workspace, size_t workspace_bytes,
+                      cudaStream_t st) {
     if (batch == 0) return SSM_OK;
     if (seqlen == 0) {
         if (h_final) {
@@ -556,7 +576,8 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
     }
     if (tma_eligible(seqlen, io) && !force_generic()) {
         const bool chunks_ok = workspace != nullptr;
-        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunks_ok);
+        const int cap = chunks_ok ? chunks_fitting(workspace_bytes, batch, dim, dstate) : 1;
+        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, cap);
         float* agg = chunks_ok ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader) : nullptr;
         unsigned int* status = chunks_ok ? static_cast<unsigned int*>(workspace) : nullptr;
         return run_scan_tma(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen,
@@ -610,17 +631,6 @@ ssm_status_t static_scratch_address(void** out) {
     return SSM_OK;
 }
 
-// Workspace bytes one chunked call actually uses (its own plan's chunks).
-size_t workspace_used(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io) {
-    size_t bytes = kWorkspaceHeader;
-    if (batch > 0 && tma_eligible(seqlen, io) && !force_generic()) {
-        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, true);
-        bytes += static_cast<size_t>(plan.chunks - 1) * static_cast<size_t>(batch) * static_cast<size_t>(dim) *
-                 2u * static_cast<size_t>(dstate) * sizeof(float);
-    }
-    return bytes;
-}
-
 }  // namespace
 
 extern "C" {
@@ -638,7 +648,7 @@ ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngrou
         return SSM_OK;
     }
     if (tma_eligible(seqlen, io) && !force_generic()) {
-        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunked != 0);
+        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunked != 0 ? kMaxChunks : 1);
         *lanes = plan.lanes; *chunks = plan.chunks; *kernels = plan.chunks > 1 ? 3 : 1; *staged = 1;
     } else {
         *lanes = 0; *chunks = 1; *kernels = 1; *staged = 0;
@@ -655,8 +665,6 @@ ssm_status_t ssm_scan_fwd_chunked_static(const void* u, const void* delta, const
                                            batch, dim, dstate, seqlen, ngroups, io);
     if (s != SSM_OK) return s;
     if (batch == 0) return SSM_OK;
-    if (workspace_used(batch, dim, dstate, seqlen, ngroups, io) > SSM_STATIC_SCRATCH_BYTES)
-        return SSM_ERR_WORKSPACE_TOO_SMALL;
     void* scratch = nullptr;
     const ssm_status_t a = static_scratch_address(&scratch);
     if (a != SSM_OK) return a;
@@ -664,7 +672,7 @@ ssm_status_t ssm_scan_fwd_chunked_static(const void* u, const void* delta, const
     const cudaError_t e = cudaMemsetAsync(scratch, 0, kWorkspaceHeader, st);  // status word starts at 0
     if (e != cudaSuccess) return cuda_fail(e);
     return run_scan(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen, ngroups,
-                    io, scratch, st);
+                    io, scratch, SSM_STATIC_SCRATCH_BYTES, st);
 }
 
 
@@ -693,7 +701,7 @@ ssm_status_t ssm_scan_fwd(const void* u, const void* delta, const void* z, const
                                            batch, dim, dstate, seqlen, ngroups, io);
     if (s != SSM_OK) return s;
     return run_scan(u, delta, z, A, B, C, Dskip, dt_bias, nullptr, y, nullptr, batch, dim, dstate,
-                    seqlen, ngroups, io, nullptr, static_cast<cudaStream_t>(stream));
+                    seqlen, ngroups, io, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
 size_t ssm_scan_fwd_chunked_workspace_size(int batch, int dim, int dstate, int seqlen, int ngroups,
@@ -728,7 +736,7 @@ ssm_status_t ssm_scan_fwd_chunked(const void* u, const void* delta, const void* 
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return run_scan(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate,
-                    seqlen, ngroups, io, workspace, st);
+                    seqlen, ngroups, io, workspace, workspace_bytes, st);
 }
 
 ssm_status_t ssm_workspace_status(const void* workspace, size_t workspace_bytes, void* stream) {

@@ -152,4 +152,11 @@ __device__ __forceinline__ uint32_t swz64(int r, int c) {
     return static_cast<uint32_t>(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
+// The same for 32-byte rows written with CU_TENSOR_MAP_SWIZZLE_32B: address bit
+// 4 is XOR-ed with bit 7, i.e. with (r >> 2) & 1.  The tile base must be
+// 256-byte aligned.
+__device__ __forceinline__ uint32_t swz32(int r, int c) {
+    return static_cast<uint32_t>(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
+}
+
 }  // namespace ssm

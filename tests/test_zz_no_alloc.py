@@ -60,13 +60,34 @@ def test_static_scratch_matches_workspace_entry_point_twice():
     assert ssm.device_status() == 0
 
 
-def test_static_scratch_rejects_problems_beyond_its_size(monkeypatch):
-    """Argument check only (fake pointers, nothing is launched): 16 time chunks
-    over 8 x 2048 channels need 15 * 16384 * 128 bytes of summaries, more than
-    the array holds."""
+def test_static_entry_checks_arguments_before_enqueuing():
+    """Argument checks only (fake pointers; each call returns before anything
+    is enqueued): a misaligned input, a missing output, bad sizes."""
+    ssm = _lib()
+    P, Q = 0x10000, 0x10008
+    f = ssm.lib.ssm_scan_fwd_chunked_static
+    assert f(Q, P, P, P, P, P, P, P, None, P, P, 2, 64, 16, 256, 1, 1, None) == 3  # SSM_ERR_MISALIGNED
+    assert f(P, P, P, P, P, P, P, P, None, None, P, 2, 64, 16, 256, 1, 1, None) == 1  # no y
+    assert f(P, P, P, P, P, P, P, P, None, P, P, 2, 64, 16, 256, 3, 1, None) == 1  # dim % ngroups
+    assert f(P, P, P, P, P, P, P, P, None, P, P, 2, 64, 12, 256, 1, 1, None) == 2  # dstate 12
+
+
+@pytest.mark.gpu
+def test_static_scratch_caps_the_chunk_count(monkeypatch):
+    """8 x 2048 channels with 16 time chunks forced: the summaries of 15 chunks
+    (15 MiB x 2) do not fit the array, so the call plans the 8 chunks whose 7
+    summaries do, and must still agree with the workspace entry point."""
     ssm = _lib()
     monkeypatch.setenv("SSM_FORCE_CHUNKS", "16")
-    P = 0x10000
-    st = ssm.lib.ssm_scan_fwd_chunked_static(P, P, P, P, P, P, P, P, None, P, P,
-                                             8, 2048, 16, 4096, 1, 1, None)
-    assert st == 4  # SSM_ERR_WORKSPACE_TOO_SMALL
+    x = I.make_scan_inputs(8, 2048, 16, 512, 1, io="bf16", recipe="scaled", seed=43, device="cuda",
+                           with_h0=True)
+    per_chunk = 8 * 2048 * 2 * 16 * 4
+    assert 256 + 7 * per_chunk <= STATIC_SCRATCH_BYTES < 256 + 8 * per_chunk
+    y_ref, h_ref = ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias, h0=x.h0)
+    y = torch.full_like(x.u, float("nan"))
+    hf = torch.full((8, 2048, 16), float("nan"), device="cuda")
+    assert _call_static(ssm, x, y, hf, x.h0) == 0
+    torch.cuda.synchronize()
+    assert rel_l2(to_np(y), to_np(y_ref)) <= BF16_REL_L2
+    assert rel_l2(to_np(hf), to_np(h_ref)) <= STATE_REL_L2
+    assert ssm.device_status() == 0
