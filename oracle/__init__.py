@@ -9,8 +9,12 @@ sequential recurrence per channel).  This module only compiles it with gcc on
 first use and marshals numpy arrays to it.  See ``ssm_oracle.c`` for the
 formulas and the passages of the pages they follow.
 
-Pin status: every function here is pinned by ``tests/test_oracle_pins.py``
-against closed forms, brute-force sums and limits that the pages fix.
+Pin status: every function here is pinned -- the scan and its decode step by
+``tests/test_oracle_pins.py`` against closed forms, brute-force sums and limits
+that the pages fix, the short causal convolution and its decode step by
+``tests/test_oracle_conv_pins.py`` against a hand-worked fixture, np.convolve,
+the impulse response and its split and decode identities -- and
+``tests/test_oracle_mutants.py`` checks that the pins catch planted slips.
 """
 from __future__ import annotations
 
@@ -52,8 +56,17 @@ def _load():
             lib.oracle_scan.restype = I
             lib.oracle_state_update.argtypes = [P] * 10 + [I] * 4
             lib.oracle_state_update.restype = I
+            _set_conv_types(lib)
             _lib = lib
     return _lib
+
+
+def _set_conv_types(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_causal_conv1d.argtypes = [P] * 6 + [I] * 5
+    lib.oracle_causal_conv1d.restype = I
+    lib.oracle_causal_conv1d_update.argtypes = [P] * 5 + [I] * 4
+    lib.oracle_causal_conv1d_update.restype = I
 
 
 class _use_library:
@@ -72,6 +85,7 @@ class _use_library:
         lib.oracle_scan.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = self.saved.oracle_state_update.argtypes
         lib.oracle_state_update.restype = ctypes.c_int
+        _set_conv_types(lib)
         _lib = lib
         return lib
 
@@ -159,3 +173,46 @@ def state_update(state, u, delta, A, B, C, z=None, Dskip=None, dt_bias=None):
     if rc != 0:
         raise ValueError(f"oracle_state_update rejected its arguments (code {rc})")
     return st, y
+
+
+def causal_conv1d(x, w, bias=None, x_prev=None, *, silu=True, return_last=False):
+    """Short causal depthwise convolution (+ silu) in fp64, the step in front
+    of the scan.  x: [batch, dim, L]; w: [dim, W]; bias: [dim]; x_prev:
+    [batch, dim, W-1] (the inputs before the sequence, oldest first).
+    Returns out [batch, dim, L] (and the last W-1 inputs when ``return_last``)."""
+    x = _f64(x)
+    if x.ndim != 3:
+        raise ValueError("x must be [batch, dim, L]")
+    batch, dim, L = x.shape
+    w = _f64(w)
+    if w.ndim != 2 or w.shape[0] != dim:
+        raise ValueError("w must be [dim, W]")
+    W = w.shape[1]
+    bias = _f64(bias, (dim,))
+    x_prev = _f64(x_prev, (batch, dim, W - 1))
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    last = np.empty((batch, dim, W - 1), dtype=np.float64) if return_last else None
+    rc = _load().oracle_causal_conv1d(_ptr(x), _ptr(w), _ptr(bias), _ptr(x_prev), _ptr(out), _ptr(last),
+                                      batch, dim, L, W, int(bool(silu)))
+    if rc != 0:
+        raise ValueError(f"oracle_causal_conv1d rejected its arguments (code {rc})")
+    return (out, last) if return_last else out
+
+
+def causal_conv1d_update(conv_state, x, w, bias=None, *, silu=True):
+    """One decode token of the convolution in fp64.  Returns (new_state, out);
+    the input state is not modified.  conv_state: [batch, dim, W-1]; x: [batch, dim]."""
+    x = _f64(x)
+    batch, dim = x.shape
+    w = _f64(w)
+    if w.ndim != 2 or w.shape[0] != dim:
+        raise ValueError("w must be [dim, W]")
+    W = w.shape[1]
+    st = np.array(conv_state, dtype=np.float64, copy=True, order="C").reshape(batch, dim, W - 1)
+    bias = _f64(bias, (dim,))
+    out = np.empty((batch, dim), dtype=np.float64)
+    rc = _load().oracle_causal_conv1d_update(_ptr(st) if W > 1 else None, _ptr(x), _ptr(w), _ptr(bias),
+                                             _ptr(out), batch, dim, W, int(bool(silu)))
+    if rc != 0:
+        raise ValueError(f"oracle_causal_conv1d_update rejected its arguments (code {rc})")
+    return st, out

@@ -186,3 +186,82 @@ int oracle_state_update(double *state, const double *u, const double *delta,
     }
     return ORACLE_OK;
 }
+
+/*
+ * Short causal convolution in front of the scan.
+ *
+ * The pages place a local convolution between the input projection and the
+ * selective SSM (eightmm.github.io "Mamba", Block Structure: it adds
+ * short-range local context; aipedia.org "Mamba: State Space Models", What a
+ * Mamba Block Contains: a short convolution for local mixing) but give
+ * neither its width nor its form.  The reading taken: one filter per channel
+ * (depthwise), causal, W taps, a per-channel bias, then silu, so that its
+ * output is the scan's input u:
+ *
+ *     out[b,d,l] = act( bias[d] + sum_{k=0}^{W-1} w[d,k] * x[b,d,l-(W-1)+k] )
+ *
+ * A time before 0 reads the caller's history x_prev[b,d,:] (the W-1 inputs
+ * that preceded the sequence, oldest first) or 0 without one.  act is silu
+ * when `silu_act` is set, else the identity.  x_last (optional) receives the
+ * last W-1 inputs of history + sequence: the history of the next segment.
+ *
+ * Layouts: x, out [batch, dim, seqlen]; w [dim, W]; bias [dim];
+ * x_prev, x_last [batch, dim, W-1].
+ */
+static double conv_input(const double *x, const double *x_prev, size_t row, size_t prow,
+                         int W, long t) {
+    if (t >= 0) return x[row + (size_t)t];
+    /* t in [-(W-1), -1]: history slot (W-1) + t */
+    return x_prev ? x_prev[prow + (size_t)((W - 1) + t)] : 0.0;
+}
+
+int oracle_causal_conv1d(const double *x, const double *w, const double *bias,
+                         const double *x_prev, double *out, double *x_last,
+                         int batch, int dim, int seqlen, int width, int silu_act) {
+    if (batch <= 0 || dim <= 0 || seqlen < 0 || width < 1) return ORACLE_BAD_ARG;
+    if (!w || (seqlen > 0 && (!x || !out))) return ORACLE_BAD_ARG;
+    const int W = width;
+    for (int b = 0; b < batch; b++) {
+        for (int d = 0; d < dim; d++) {
+            const size_t bd = (size_t)b * dim + d;
+            const size_t row = bd * (size_t)seqlen;
+            const size_t prow = bd * (size_t)(W - 1);
+            for (long l = 0; l < seqlen; l++) {
+                double acc = bias ? bias[d] : 0.0;
+                for (int k = 0; k < W; k++)
+                    acc += w[(size_t)d * W + k] * conv_input(x, x_prev, row, prow, W, l - (W - 1) + k);
+                out[row + (size_t)l] = silu_act ? silu(acc) : acc;
+            }
+            if (x_last) {
+                for (int k = 0; k < W - 1; k++)
+                    x_last[prow + k] = conv_input(x, x_prev, row, prow, W, (long)seqlen - (W - 1) + k);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* One decode token of the convolution: the window is the W-1 inputs held in
+ * conv_state[b,d,:] (oldest first) followed by x[b,d]; out[b,d] = act(bias +
+ * sum_k w[d,k] window[k]), and the state drops its oldest input and appends
+ * x[b,d]. */
+int oracle_causal_conv1d_update(double *conv_state, const double *x, const double *w,
+                                const double *bias, double *out,
+                                int batch, int dim, int width, int silu_act) {
+    if (batch <= 0 || dim <= 0 || width < 1) return ORACLE_BAD_ARG;
+    if (!x || !w || !out || (width > 1 && !conv_state)) return ORACLE_BAD_ARG;
+    const int W = width;
+    for (int b = 0; b < batch; b++) {
+        for (int d = 0; d < dim; d++) {
+            const size_t bd = (size_t)b * dim + d;
+            double *st = conv_state ? conv_state + bd * (size_t)(W - 1) : NULL;
+            double acc = bias ? bias[d] : 0.0;
+            for (int k = 0; k < W - 1; k++) acc += w[(size_t)d * W + k] * st[k];
+            acc += w[(size_t)d * W + (W - 1)] * x[bd];
+            out[bd] = silu_act ? silu(acc) : acc;
+            for (int k = 0; k + 1 < W - 1; k++) st[k] = st[k + 1];
+            if (W > 1) st[W - 2] = x[bd];
+        }
+    }
+    return ORACLE_OK;
+}

@@ -7,6 +7,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_conv_pins as conv_pins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
@@ -29,6 +30,19 @@ MUTANTS = {
     "softplus_without_abs": ("log1p(exp(-fabs(x)))", "log1p(exp(-x))"),
     "input_term_without_step": ("const double bx = dt * J->B[", "const double bx = J->B["),
     "decode_gate_dropped": ("if (z) yt *= silu(z[bd]);", ""),
+    # the short convolution in front of the scan
+    "conv_taps_reversed": ("acc += w[(size_t)d * W + k] * conv_input(x, x_prev, row, prow, W, l - (W - 1) + k);",
+                           "acc += w[(size_t)d * W + (W - 1 - k)] * conv_input(x, x_prev, row, prow, W, l - (W - 1) + k);"),
+    "conv_window_one_step_late": ("conv_input(x, x_prev, row, prow, W, l - (W - 1) + k);",
+                                  "conv_input(x, x_prev, row, prow, W, l - W + k);"),
+    "conv_history_ignored": ("return x_prev ? x_prev[prow + (size_t)((W - 1) + t)] : 0.0;", "return 0.0;"),
+    "conv_history_reversed": ("x_prev[prow + (size_t)((W - 1) + t)]", "x_prev[prow + (size_t)(-1 - t)]"),
+    "conv_bias_dropped": ("                double acc = bias ? bias[d] : 0.0;\n                for (int k = 0; k < W; k++)",
+                          "                double acc = 0.0;\n                for (int k = 0; k < W; k++)"),
+    "conv_silu_dropped": ("out[row + (size_t)l] = silu_act ? silu(acc) : acc;", "out[row + (size_t)l] = acc;"),
+    "conv_state_shift_reversed": ("for (int k = 0; k + 1 < W - 1; k++) st[k] = st[k + 1];",
+                                  "for (int k = W - 2; k > 0; k--) st[k] = st[k - 1];"),
+    "conv_update_newest_tap_wrong": ("acc += w[(size_t)d * W + (W - 1)] * x[bd];", "acc += w[(size_t)d * W] * x[bd];"),
 }
 
 PIN_TESTS = [
@@ -43,6 +57,12 @@ PIN_TESTS = [
     lambda: pins.test_large_step_overwrites_state(),
     lambda: pins.test_decode_steps_equal_one_scan(),
     lambda: pins.test_decode_single_step_from_zero_state(),
+    lambda: conv_pins.test_conv_hand_worked_golden(),
+    lambda: conv_pins.test_conv_matches_numpy_convolve(4, True, True),
+    lambda: conv_pins.test_conv_impulse_response(),
+    lambda: conv_pins.test_conv_history_splits_sequence(9),
+    lambda: conv_pins.test_conv_decode_steps_equal_conv(),
+    lambda: conv_pins.test_conv_width_one_is_pointwise(),
 ]
 
 
