@@ -386,6 +386,79 @@ def bench_decode_device(ssm, I, torch, w, steps, warmup):
     return res
 
 
+def bench_graph(torch, launch, nsets, reps, warmup=3):
+    """Mean device time of one launch: CUDA events around `reps` replays of a
+    CUDA graph that calls launch(i) for i in range(nsets)."""
+    dev = torch.device("cuda")
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(stream):
+        for i in range(nsets):
+            launch(i)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(nsets):
+            launch(i)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / (reps * nsets)
+
+
+def bench_conv(ssm, I, torch, peaks, width=4):
+    """The short causal convolution (+ silu) in front of the scan, on the
+    three scan shapes (bf16), and its decode step on the decode shape: device
+    time per launch over rotating inputs (> 3x L2)."""
+    dev = torch.device("cuda")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    for name in ("scan_bf16_b2_d1536_l2048", "scan_bf16_b8_d2048_l4096", "scan_bf16_b1_d5120_l65536_final_state"):
+        w = I.WORKLOADS[name]
+        nbytes = I.compulsory_bytes_conv(w["batch"], w["dim"], w["seqlen"], w["io"])
+        nsets = n_rotating_sets(nbytes, l2)
+        ins = [I.make_conv_inputs(w["batch"], w["dim"], w["seqlen"], width, io=w["io"], seed=s, device=dev)
+               for s in range(nsets)]
+        outs = [torch.empty_like(c["x"]) for c in ins]
+
+        def launch(i, ins=ins, outs=outs):
+            c = ins[i]
+            ssm.causal_conv1d(c["x"], c["w"], c["bias"], out=outs[i])
+
+        ms = bench_graph(torch, launch, nsets, reps=max(3, 60 // nsets))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        key = "conv1d_w%d_%s" % (width, name.replace("scan_", "").replace("_final_state", ""))
+        res[key] = dict(GBps=round(gbs, 1), us_per_launch=round(ms * 1e3, 2),
+                        frac_of_hbm_measured=round(gbs / peaks["hbm_gbs"], 4))
+        del ins, outs
+    wd = I.WORKLOADS[DECODE]
+    b, d = wd["batch"], wd["dim"]
+    es = 2
+    per = b * d * es * (2 * (width - 1) + 2)  # state read + written, token read, out written
+    nsets = n_rotating_sets(per, l2)
+    ins = [I.make_conv_inputs(b, d, 1, width, io=wd["io"], seed=s, device=dev, with_prev=True) for s in range(nsets)]
+    toks = [c["x"][:, :, 0].contiguous() for c in ins]
+    outs = [torch.empty_like(t) for t in toks]
+
+    def launch_dec(i):
+        c = ins[i]
+        ssm.causal_conv1d_update(c["x_prev"], toks[i], c["w"], c["bias"], out=outs[i])
+
+    ms = bench_graph(torch, launch_dec, nsets, reps=max(3, 200 // nsets))
+    res["conv1d_update_w%d_b%d_d%d" % (width, b, d)] = dict(
+        us_per_step=round(ms * 1e3, 3), GBps=round(per / (ms * 1e-3) / 1e9, 1),
+        frac_of_hbm_measured=round(per / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4))
+    return res
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -456,6 +529,7 @@ def run_ours(args):
                                us_per_launch=round(rx["ms_per_launch"] * 1e3, 2),
                                frac_of_hbm_measured=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3)
                                                           / 1e9 / peaks["hbm_gbs"], 4))
+        extra.update(bench_conv(ssm, I, torch, peaks))
 
     base = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:

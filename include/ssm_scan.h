@@ -234,6 +234,54 @@ ssm_status_t ssm_state_update(float *state, const void *u, const void *delta, co
                               int batch, int dim, int dstate, int ngroups,
                               ssm_dtype_t io, void *stream);
 
+/*
+ * ssm_causal_conv1d_fwd -- the short causal convolution in front of the scan.
+ * The pages place a local convolution between the input projection and the
+ * selective SSM (eightmm.github.io "Mamba", Block Structure: it adds
+ * short-range local context; aipedia.org "Mamba: State Space Models", What a
+ * Mamba Block Contains: a short convolution for local mixing) without fixing
+ * its form.  This library reads it as one filter of `width` taps per channel
+ * (depthwise), causal, with a per-channel bias, followed by silu, so that its
+ * output is the scan's u:
+ *     out[b,d,l] = act(bias[d] + sum_{k<width} w[d,k] * x[b,d,l-(width-1)+k])
+ * Times before 0 read x_prev (the width-1 inputs that preceded the sequence,
+ * oldest first) or 0 when x_prev is NULL.
+ *   x       : [batch, dim, seqlen] io type
+ *   w       : [dim, width] fp32, width in 1..SSM_CONV_MAX_WIDTH
+ *   bias    : [dim] fp32, or NULL (0)
+ *   x_prev  : [batch, dim, width-1] io type, or NULL
+ *   out     : [batch, dim, seqlen] io type, written; must not overlap x
+ *   x_last  : [batch, dim, width-1] io type, or NULL; receives the last width-1
+ *             inputs of x_prev + x (the history of the next segment); must not
+ *             overlap x_prev
+ *   silu    : nonzero applies silu, 0 returns the convolution alone
+ * All pointers 16-byte aligned (SSM_ERR_MISALIGNED); x == out or
+ * x_prev == x_last is SSM_ERR_INVALID_ARG; width outside 1..4 or an unknown io
+ * type is SSM_ERR_UNSUPPORTED.  Checks run before anything is enqueued; the
+ * call is asynchronous on stream and allocates nothing.
+ */
+#define SSM_CONV_MAX_WIDTH 4
+ssm_status_t ssm_causal_conv1d_fwd(const void *x, const float *w, const float *bias, const void *x_prev,
+                                   void *out, void *x_last, int batch, int dim, int seqlen, int width,
+                                   int silu, ssm_dtype_t io, void *stream);
+
+/*
+ * ssm_causal_conv1d_update -- one decode token of the same convolution
+ * (cuishuaiwen.com "Mamba & State-Space Sequence Models", Core mechanics: a
+ * decode step works on a state of constant size).  The window is the width-1
+ * inputs held in conv_state followed by x; out = act(bias + sum_k w[d,k]
+ * window[k]), and conv_state drops its oldest input and appends x.
+ *   conv_state : [batch, dim, width-1] io type, read and overwritten in place
+ *                (may be NULL when width == 1)
+ *   x          : [batch, dim] io type
+ *   w, bias    : as in ssm_causal_conv1d_fwd
+ *   out        : [batch, dim] io type, written; must not be x
+ * Errors as in ssm_causal_conv1d_fwd.
+ */
+ssm_status_t ssm_causal_conv1d_update(void *conv_state, const void *x, const float *w, const float *bias,
+                                      void *out, int batch, int dim, int width, int silu, ssm_dtype_t io,
+                                      void *stream);
+
 #ifdef __cplusplus
 }
 #endif

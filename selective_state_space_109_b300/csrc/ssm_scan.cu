@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cmath>
 #include <mutex>
 #include <cstdint>
@@ -16,6 +17,7 @@
 #include <cstring>
 
 #include "../../include/ssm_scan.h"
+#include "conv1d.cuh"
 #include "scan_fwd.cuh"
 #include "decode_tma.cuh"
 #include "scan_tma.cuh"
@@ -631,6 +633,55 @@ ssm_status_t static_scratch_address(void** out) {
     return SSM_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Short causal convolution in front of the scan
+// ---------------------------------------------------------------------------
+
+template <typename T>
+cudaError_t launch_conv_t(const ssm::ConvParams& p, int width, cudaStream_t st) {
+    const int es = static_cast<int>(sizeof(T));
+    const bool vec = (static_cast<long long>(p.seqlen) * es) % 16 == 0;
+    // Vector path: 8 warps a block, each taking 4 x 32 chunks per iteration.
+    const long long work = vec ? (p.rows * (p.seqlen / (16 / es)) + 3) / 4 : p.rows * p.seqlen;
+    const long long want = (work + 255) / 256;
+    const unsigned grid = static_cast<unsigned>(std::max(1LL, std::min(want, static_cast<long long>(device_sm_count()) * 8)));
+    auto go = [&](auto wc) {
+        constexpr int W = decltype(wc)::value;
+        if (vec) {
+            if (p.rows * (p.seqlen / (16 / es)) < (1LL << 31))
+                ssm::conv1d_vec_kernel<T, W, unsigned><<<grid, 256, 0, st>>>(p);
+            else
+                ssm::conv1d_vec_kernel<T, W, unsigned long long><<<grid, 256, 0, st>>>(p);
+        } else {
+            ssm::conv1d_elem_kernel<T, W><<<grid, 256, 0, st>>>(p);
+            if (p.x_last && W > 1)
+                ssm::conv1d_last_kernel<T, W><<<static_cast<unsigned>((p.rows + 255) / 256), 256, 0, st>>>(p);
+        }
+    };
+    switch (width) {
+        case 1: go(std::integral_constant<int, 1>{}); break;
+        case 2: go(std::integral_constant<int, 2>{}); break;
+        case 3: go(std::integral_constant<int, 3>{}); break;
+        case 4: go(std::integral_constant<int, 4>{}); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_conv_update_t(void* state, const void* x, const float* w, const float* bias, void* out,
+                                 long long rows, int dim, int width, int silu_act, cudaStream_t st) {
+    const unsigned grid = static_cast<unsigned>((rows + 255) / 256);
+    switch (width) {
+        case 1: ssm::conv1d_update_kernel<T, 1><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
+        case 2: ssm::conv1d_update_kernel<T, 2><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
+        case 3: ssm::conv1d_update_kernel<T, 3><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
+        case 4: ssm::conv1d_update_kernel<T, 4><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 extern "C" {
@@ -811,6 +862,62 @@ ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, co
     }
 #undef SSM_DECODE_LAUNCH
     const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return SSM_OK;
+}
+
+
+ssm_status_t ssm_causal_conv1d_fwd(const void* x, const float* w, const float* bias, const void* x_prev,
+                                   void* out, void* x_last, int batch, int dim, int seqlen, int width,
+                                   int silu, ssm_dtype_t io, void* stream) {
+    if (batch < 0 || dim <= 0 || seqlen < 0) return SSM_ERR_INVALID_ARG;
+    if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+    if (width < 1 || width > SSM_CONV_MAX_WIDTH) return SSM_ERR_UNSUPPORTED;
+    if (batch == 0) return SSM_OK;
+    if (!w || (seqlen > 0 && (!x || !out))) return SSM_ERR_INVALID_ARG;
+    if ((x && x == out) || (x_prev && x_prev == x_last)) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, w, bias, x_prev, out, x_last};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SSM_ERR_MISALIGNED;
+    ssm::ConvParams p{};
+    p.x = x; p.w = w; p.bias = bias; p.x_prev = width > 1 ? x_prev : nullptr; p.out = out;
+    p.x_last = width > 1 ? x_last : nullptr;
+    p.rows = static_cast<long long>(batch) * dim;
+    p.dim = dim; p.seqlen = seqlen; p.silu = silu != 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (seqlen == 0) {
+        // Nothing to convolve; the next segment's history is this one's.
+        if (p.x_last) {
+            const size_t bytes = static_cast<size_t>(p.rows) * (width - 1) * (io == SSM_F32 ? 4 : 2);
+            e = p.x_prev ? cudaMemcpyAsync(p.x_last, p.x_prev, bytes, cudaMemcpyDeviceToDevice, st)
+                         : cudaMemsetAsync(p.x_last, 0, bytes, st);
+        }
+    } else {
+        e = io == SSM_F32 ? launch_conv_t<float>(p, width, st) : launch_conv_t<__nv_bfloat16>(p, width, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return SSM_OK;
+}
+
+ssm_status_t ssm_causal_conv1d_update(void* conv_state, const void* x, const float* w, const float* bias,
+                                      void* out, int batch, int dim, int width, int silu, ssm_dtype_t io,
+                                      void* stream) {
+    if (batch < 0 || dim <= 0) return SSM_ERR_INVALID_ARG;
+    if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+    if (width < 1 || width > SSM_CONV_MAX_WIDTH) return SSM_ERR_UNSUPPORTED;
+    if (batch == 0) return SSM_OK;
+    if (!x || !w || !out || (width > 1 && !conv_state)) return SSM_ERR_INVALID_ARG;
+    if (x == out) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {conv_state, x, w, bias, out};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SSM_ERR_MISALIGNED;
+    const long long rows = static_cast<long long>(batch) * dim;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        io == SSM_F32 ? launch_conv_update_t<float>(conv_state, x, w, bias, out, rows, dim, width, silu != 0, st)
+                      : launch_conv_update_t<__nv_bfloat16>(conv_state, x, w, bias, out, rows, dim, width, silu != 0,
+                                                            st);
     if (e != cudaSuccess) return cuda_fail(e);
     return SSM_OK;
 }

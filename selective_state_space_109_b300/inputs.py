@@ -30,7 +30,8 @@ import numpy as np
 import torch
 
 _TENSOR_IDS = {"u": 1, "delta": 2, "z": 3, "B": 4, "C": 5, "D": 6, "dt": 7,
-               "h0": 8, "state": 9, "A": 10}
+               "h0": 8, "state": 9, "A": 10, "conv_x": 11, "conv_w": 12, "conv_bias": 13,
+               "conv_prev": 14}
 
 
 def _subseed(seed: int, name: str, step: int = 0) -> int:
@@ -158,6 +159,25 @@ def decode_params(dim, dstate, recipe="scaled", seed=0, device="cpu"):
 
 # Named workloads: the sizes of the five synthetic workloads this library is
 # checked and measured on.
+def make_conv_inputs(batch, dim, seqlen, width=4, io="bf16", seed=0, device="cpu", with_prev=False):
+    """Inputs of the short causal convolution in front of the scan: x
+    [batch, dim, L] ~ N(0, 1) in the I/O type (the pre-convolution activation,
+    same scale as u); w [dim, W] ~ N(0, 1/W) fp32 (unit gain); bias [dim] ~
+    N(0, 0.1^2) fp32; optional history [batch, dim, W-1] ~ N(0, 1)."""
+    dt = io_torch_dtype(io)
+    x = _randn((batch, dim, seqlen), seed, "conv_x", "cpu").to(dt)
+    w = (_randn((dim, width), seed, "conv_w", "cpu") / width ** 0.5).float()
+    bias = (0.1 * _randn((dim,), seed, "conv_bias", "cpu")).float()
+    prev = _randn((batch, dim, width - 1), seed, "conv_prev", "cpu").to(dt) if with_prev else None
+    mv = lambda t: None if t is None else t.to(device)
+    return dict(x=mv(x), w=mv(w), bias=mv(bias), x_prev=mv(prev))
+
+
+def compulsory_bytes_conv(batch, dim, seqlen, io) -> int:
+    """x read and out written once ([batch, dim, L] each)."""
+    return 2 * batch * dim * seqlen * (4 if io == "f32" else 2)
+
+
 WORKLOADS = {
     "scan_f32_tiny": dict(kind="scan", batch=1, dim=64, dstate=16, seqlen=256, ngroups=1,
                           io="f32", recipe="unit"),

@@ -63,6 +63,10 @@ def _load() -> ctypes.CDLL:
     L.ssm_device_status.restype = I
     L.ssm_state_update.argtypes = [P] * 10 + [I] * 5 + [P]
     L.ssm_state_update.restype = I
+    L.ssm_causal_conv1d_fwd.argtypes = [P] * 6 + [I] * 6 + [P]
+    L.ssm_causal_conv1d_fwd.restype = I
+    L.ssm_causal_conv1d_update.argtypes = [P] * 5 + [I] * 5 + [P]
+    L.ssm_causal_conv1d_update.restype = I
     return L
 
 
@@ -227,3 +231,57 @@ def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=
     if st != 0:
         raise SsmError(st, "ssm_state_update")
     return y
+
+
+def causal_conv1d(x, w, bias=None, x_prev=None, *, silu=True, out=None, x_last=None) -> torch.Tensor:
+    """The short causal depthwise convolution in front of the scan:
+    out[b,d,l] = silu(bias[d] + sum_k w[d,k] x[b,d,l-(W-1)+k]), with x_prev
+    [batch, dim, W-1] as the inputs before the sequence (zeros if None).
+    x: [batch, dim, L] (float32 or bfloat16); w: [dim, W] float32, W <= 4.
+    ``x_last`` (optional, [batch, dim, W-1]) receives the next segment's history."""
+    if x.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    if x.dim() != 3 or w.dim() != 2:
+        raise ValueError("expected x [batch, dim, L], w [dim, W]")
+    batch, dim, L = x.shape
+    W = w.shape[1]
+    dev, io = x.device, x.dtype
+    _io_code(io)
+    _check(x, "x", (batch, dim, L), io, dev)
+    _check(w, "w", (dim, W), torch.float32, dev)
+    _check(bias, "bias", (dim,), torch.float32, dev)
+    _check(x_prev, "x_prev", (batch, dim, W - 1), io, dev)
+    _check(x_last, "x_last", (batch, dim, W - 1), io, dev)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", x.shape, io, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_causal_conv1d_fwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(x_prev), _ptr(y), _ptr(x_last),
+                                       batch, dim, L, W, int(bool(silu)), _io_code(io), _stream_handle(dev))
+    if st != 0:
+        raise SsmError(st, "ssm_causal_conv1d_fwd")
+    return y
+
+
+def causal_conv1d_update(conv_state, x, w, bias=None, *, silu=True, out=None) -> torch.Tensor:
+    """One decode token of the convolution: conv_state [batch, dim, W-1] (the
+    last W-1 inputs, oldest first) is advanced in place; returns out [batch, dim]."""
+    if x.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    if x.dim() != 2 or w.dim() != 2:
+        raise ValueError("expected x [batch, dim], w [dim, W]")
+    batch, dim = x.shape
+    W = w.shape[1]
+    dev, io = x.device, x.dtype
+    _io_code(io)
+    _check(conv_state, "conv_state", (batch, dim, W - 1), io, dev)
+    _check(w, "w", (dim, W), torch.float32, dev)
+    _check(bias, "bias", (dim,), torch.float32, dev)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", x.shape, io, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_causal_conv1d_update(_ptr(conv_state), _ptr(x), _ptr(w), _ptr(bias), _ptr(y), batch, dim,
+                                          W, int(bool(silu)), _io_code(io), _stream_handle(dev))
+    if st != 0:
+        raise SsmError(st, "ssm_causal_conv1d_update")
+    return y
+

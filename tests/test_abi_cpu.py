@@ -108,3 +108,30 @@ def test_workspace_status_argument_errors(lib):
     assert lib.ssm_workspace_status(None, 256, None) == 1
     assert lib.ssm_workspace_status(P, 8, None) == 1
     assert lib.ssm_workspace_status(MIS, 256, None) == 3
+
+
+def test_conv_argument_errors(lib):
+    """Argument checks of the short convolution (fake pointers; each call
+    returns before anything is enqueued)."""
+    Q = 0x20000
+
+    def fwd(x=P, w=P, bias=None, prev=None, out=Q, last=None, batch=2, dim=4, L=16, W=4, io=1):
+        return lib.ssm_causal_conv1d_fwd(x, w, bias, prev, out, last, batch, dim, L, W, 1, io, None)
+    assert fwd(w=None) == 1
+    assert fwd(out=None) == 1
+    assert fwd(out=P) == 1                    # out is x
+    assert fwd(prev=Q + 0x100, last=Q + 0x100) == 1   # history in and out share a buffer
+    assert fwd(dim=0) == 1
+    assert fwd(W=5) == 2
+    assert fwd(W=0) == 2
+    assert fwd(io=7) == 2
+    assert fwd(x=MIS) == 3
+    assert fwd(batch=0, x=None, out=None) == 0
+
+    def upd(state=P, x=Q, w=Q + 0x100, out=Q + 0x200, W=4, io=1):
+        return lib.ssm_causal_conv1d_update(state, x, w, None, out, 2, 4, W, 1, io, None)
+    assert upd(state=None) == 1
+    assert upd(x=None) == 1
+    assert upd(out=Q) == 1                    # out is x
+    assert upd(W=5) == 2
+    assert upd(state=MIS) == 3
