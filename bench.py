@@ -638,8 +638,28 @@ def run_profile_case(args):
     import torch
     from selective_state_space_109_b300 import inputs as I
     from selective_state_space_109_b300 import ssm
-    w = I.WORKLOADS[args.profile]
     dev = torch.device("cuda")
+    if args.profile.startswith("conv1d_"):
+        # conv1d_w4_<scan workload>: the short convolution on that scan shape;
+        # conv1d_update_w4_<decode workload>: its decode step on that shape.
+        upd = args.profile.startswith("conv1d_update_")
+        rest = args.profile[len("conv1d_update_w") if upd else len("conv1d_w"):]
+        width, name = int(rest.split("_", 1)[0]), rest.split("_", 1)[1]
+        w = I.WORKLOADS[name]
+        L = 1 if upd else w["seqlen"]
+        c = I.make_conv_inputs(w["batch"], w["dim"], L, width, io=w["io"], device=dev, with_prev=upd)
+        if upd:
+            tok = c["x"][:, :, 0].contiguous()
+            for _ in range(args.warmup + args.steps):
+                ssm.causal_conv1d_update(c["x_prev"], tok, c["w"], c["bias"])
+        else:
+            out = torch.empty_like(c["x"])
+            for _ in range(args.warmup + args.steps):
+                ssm.causal_conv1d(c["x"], c["w"], c["bias"], out=out)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
+        return
+    w = I.WORKLOADS[args.profile]
     if w["kind"] == "decode":
         prm = I.decode_params(w["dim"], w["dstate"], recipe=w["recipe"], device=dev)
         st = I.make_decode_state(w["batch"], w["dim"], w["dstate"], device=dev)
