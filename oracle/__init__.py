@@ -13,7 +13,10 @@ Pin status: every function here is pinned -- the scan and its decode step by
 ``tests/test_oracle_pins.py`` against closed forms, brute-force sums and limits
 that the pages fix, the short causal convolution and its decode step by
 ``tests/test_oracle_conv_pins.py`` against a hand-worked fixture, np.convolve,
-the impulse response and its split and decode identities -- and
+the impulse response and its split and decode identities, the packed
+variable-length scan and the pooled decode step by
+``tests/test_oracle_varlen_pins.py`` against the separately pinned scan and
+decode step -- and
 ``tests/test_oracle_mutants.py`` checks that the pins catch planted slips.
 """
 from __future__ import annotations
@@ -63,6 +66,10 @@ def _load():
 
 def _set_conv_types(lib):
     P, I = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_scan_varlen.argtypes = [P] * 12 + [I] * 5
+    lib.oracle_scan_varlen.restype = I
+    lib.oracle_state_update_indexed.argtypes = [P, P, I] + [P] * 9 + [I] * 4
+    lib.oracle_state_update_indexed.restype = I
     lib.oracle_causal_conv1d.argtypes = [P] * 6 + [I] * 5
     lib.oracle_causal_conv1d.restype = I
     lib.oracle_causal_conv1d_update.argtypes = [P] * 5 + [I] * 4
@@ -216,3 +223,67 @@ def causal_conv1d_update(conv_state, x, w, bias=None, *, silu=True):
     if rc != 0:
         raise ValueError(f"oracle_causal_conv1d_update rejected its arguments (code {rc})")
     return st, out
+
+
+def scan_varlen(u, delta, A, B, C, cu_seqlens, z=None, Dskip=None, dt_bias=None, h0=None, *,
+                return_final_state=False):
+    """Packed variable-length scan in fp64: sequence s occupies times
+    [cu_seqlens[s], cu_seqlens[s+1]) of one row and starts from h0[s] (or 0).
+    u, delta, z: [dim, T]; B, C: [G, N, T]; h0: [nseq, dim, N].  Returns y
+    [dim, T] (and h_final [nseq, dim, N] when ``return_final_state``)."""
+    u = _f64(u)
+    if u.ndim != 2:
+        raise ValueError("u must be [dim, T]")
+    dim, T = u.shape
+    delta = _f64(delta, u.shape)
+    z = _f64(z, u.shape)
+    A = _f64(A)
+    if A.ndim != 2 or A.shape[0] != dim:
+        raise ValueError("A must be [dim, N]")
+    N = A.shape[1]
+    B = _f64(B)
+    if B.ndim != 3 or B.shape[1:] != (N, T):
+        raise ValueError("B must be [G, N, T]")
+    G = B.shape[0]
+    C = _f64(C, B.shape)
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    nseq = cu.size - 1
+    Dskip = _f64(Dskip, (dim,))
+    dt_bias = _f64(dt_bias, (dim,))
+    h0 = _f64(h0, (nseq, dim, N))
+    y = np.empty((dim, T), dtype=np.float64)
+    hf = np.empty((nseq, dim, N), dtype=np.float64) if return_final_state else None
+    rc = _load().oracle_scan_varlen(_ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
+                                    _ptr(dt_bias), _ptr(h0), _ptr(cu), _ptr(y), _ptr(hf), dim, N, T, G, nseq)
+    if rc != 0:
+        raise ValueError(f"oracle_scan_varlen rejected its arguments (code {rc})")
+    return (y, hf) if return_final_state else y
+
+
+def state_update_indexed(state_pool, state_indices, u, delta, A, B, C, z=None, Dskip=None, dt_bias=None):
+    """One decode step on a pool of states in fp64: row b advances slot
+    state_indices[b] (negative: padding, untouched, y row left as NaN).
+    Returns (new_pool, y); the input pool is not modified."""
+    pool = np.array(state_pool, dtype=np.float64, copy=True, order="C")
+    nslots, dim, N = pool.shape
+    idx = np.ascontiguousarray(np.asarray(state_indices, dtype=np.int32))
+    batch = idx.size
+    u = _f64(u, (batch, dim))
+    delta = _f64(delta, (batch, dim))
+    z = _f64(z, (batch, dim))
+    A = _f64(A, (dim, N))
+    B = _f64(B)
+    if B.ndim != 3 or B.shape[0] != batch or B.shape[2] != N:
+        raise ValueError("B must be [batch, G, N]")
+    G = B.shape[1]
+    C = _f64(C, B.shape)
+    Dskip = _f64(Dskip, (dim,))
+    dt_bias = _f64(dt_bias, (dim,))
+    y = np.full((batch, dim), np.nan, dtype=np.float64)
+    rc = _load().oracle_state_update_indexed(_ptr(pool), _ptr(idx), nslots, _ptr(u), _ptr(delta), _ptr(z),
+                                             _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip), _ptr(dt_bias), _ptr(y),
+                                             batch, dim, N, G)
+    if rc != 0:
+        raise ValueError(f"oracle_state_update_indexed rejected its arguments (code {rc})")
+    return pool, y
+

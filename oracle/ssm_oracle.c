@@ -265,3 +265,98 @@ int oracle_causal_conv1d_update(double *conv_state, const double *x, const doubl
     }
     return ORACLE_OK;
 }
+
+/*
+ * Packed variable-length batch (serving: a batch of sequences of different
+ * lengths without padding).  The pages treat the layer as sequence in,
+ * sequence out with a recurrent state per sequence (eightmm.github.io
+ * "Mamba", Architecture Contract); packing several sequences end to end along
+ * time is the plainest layout for a batch of unequal lengths, and each
+ * sequence is then its own run of the recurrence:
+ *
+ *   sequence s occupies times [cu_seqlens[s], cu_seqlens[s+1]) of one row;
+ *   its state starts from h0[s] (or 0) at its first token, every token is the
+ *   step of oracle_scan, and its end state goes to h_final[s].
+ *
+ * Layouts: u, delta, z, y [dim, T]; B, C [ngroups, dstate, T];
+ * h0, h_final [nseq, dim, dstate]; cu_seqlens [nseq + 1], non-decreasing,
+ * cu_seqlens[0] = 0 and cu_seqlens[nseq] = T.
+ */
+int oracle_scan_varlen(const double *u, const double *delta, const double *z,
+                       const double *A, const double *B, const double *C,
+                       const double *Dskip, const double *dt_bias, const double *h0,
+                       const int *cu_seqlens, double *y, double *h_final,
+                       int dim, int dstate, int total, int ngroups, int nseq) {
+    if (dim <= 0 || dstate <= 0 || total < 0 || ngroups <= 0 || nseq < 1 || dim % ngroups != 0)
+        return ORACLE_BAD_ARG;
+    if (!cu_seqlens || !A || (total > 0 && (!u || !delta || !B || !C || !y))) return ORACLE_BAD_ARG;
+    if (cu_seqlens[0] != 0 || cu_seqlens[nseq] != total) return ORACLE_BAD_ARG;
+    for (int s = 0; s < nseq; s++)
+        if (cu_seqlens[s + 1] < cu_seqlens[s]) return ORACLE_BAD_ARG;
+    const int N = dstate, T = total;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!h) return ORACLE_BAD_ARG;
+    for (int d = 0; d < dim; d++) {
+        const int g = d / (dim / ngroups);
+        const size_t row = (size_t)d * (size_t)T;
+        const size_t bc = (size_t)g * (size_t)N * (size_t)T;
+        const double dskip = Dskip ? Dskip[d] : 0.0;
+        const double bias = dt_bias ? dt_bias[d] : 0.0;
+        for (int s = 0; s < nseq; s++) {
+            for (int n = 0; n < N; n++)
+                h[n] = h0 ? h0[((size_t)s * dim + d) * N + n] : 0.0;
+            for (int t = cu_seqlens[s]; t < cu_seqlens[s + 1]; t++) {
+                const double ut = u[row + t];
+                const double dt = softplus(delta[row + t] + bias);
+                double acc = 0.0;
+                for (int n = 0; n < N; n++) {
+                    h[n] = exp(dt * A[(size_t)d * N + n]) * h[n] + dt * B[bc + (size_t)n * T + t] * ut;
+                    acc += C[bc + (size_t)n * T + t] * h[n];
+                }
+                double yv = acc + dskip * ut;
+                if (z) yv *= silu(z[row + t]);
+                y[row + t] = yv;
+            }
+            if (h_final)
+                for (int n = 0; n < N; n++) h_final[((size_t)s * dim + d) * N + n] = h[n];
+        }
+    }
+    free(h);
+    return ORACLE_OK;
+}
+
+/* One decode step on a pool of states (continuous batching): batch row b
+ * advances state slot state_indices[b] of state_pool [nslots, dim, dstate]
+ * by its token; a negative index marks a padding row, which touches no state
+ * and leaves y[b, :] unwritten.  Otherwise the step of oracle_state_update. */
+int oracle_state_update_indexed(double *state_pool, const int *state_indices, int nslots,
+                                const double *u, const double *delta, const double *z,
+                                const double *A, const double *B, const double *C,
+                                const double *Dskip, const double *dt_bias, double *y,
+                                int batch, int dim, int dstate, int ngroups) {
+    if (!check_dims(batch, dim, dstate, 1, ngroups) || nslots < 1) return ORACLE_BAD_ARG;
+    if (!state_pool || !state_indices || !u || !delta || !A || !B || !C || !y) return ORACLE_BAD_ARG;
+    const int N = dstate;
+    for (int b = 0; b < batch; b++) {
+        const int slot = state_indices[b];
+        if (slot < 0) continue;
+        if (slot >= nslots) return ORACLE_BAD_ARG;
+        for (int d = 0; d < dim; d++) {
+            const int g = d / (dim / ngroups);
+            const size_t bd = (size_t)b * dim + d;
+            const size_t bc = ((size_t)b * ngroups + g) * (size_t)N;
+            double *h = &state_pool[((size_t)slot * dim + d) * N];
+            const double ut = u[bd];
+            const double dt = softplus(delta[bd] + (dt_bias ? dt_bias[d] : 0.0));
+            double acc = 0.0;
+            for (int n = 0; n < N; n++) {
+                h[n] = exp(dt * A[(size_t)d * N + n]) * h[n] + dt * B[bc + n] * ut;
+                acc += C[bc + n] * h[n];
+            }
+            double yv = acc + (Dskip ? Dskip[d] : 0.0) * ut;
+            if (z) yv *= silu(z[bd]);
+            y[bd] = yv;
+        }
+    }
+    return ORACLE_OK;
+}

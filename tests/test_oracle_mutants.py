@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 import test_oracle_conv_pins as conv_pins
+import test_oracle_varlen_pins as varlen_pins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
@@ -43,6 +44,16 @@ MUTANTS = {
     "conv_state_shift_reversed": ("for (int k = 0; k + 1 < W - 1; k++) st[k] = st[k + 1];",
                                   "for (int k = W - 2; k > 0; k--) st[k] = st[k - 1];"),
     "conv_update_newest_tap_wrong": ("acc += w[(size_t)d * W + (W - 1)] * x[bd];", "acc += w[(size_t)d * W] * x[bd];"),
+    # packed variable-length batches and the pooled decode step
+    "varlen_no_reset_between_sequences": (
+        "            for (int n = 0; n < N; n++)\n                h[n] = h0 ? h0[((size_t)s * dim + d) * N + n] : 0.0;",
+        "            for (int n = 0; n < N; n++)\n                if (s == 0) h[n] = h0 ? h0[((size_t)s * dim + d) * N + n] : 0.0;"),
+    "varlen_first_sequence_h0_for_all": ("h[n] = h0 ? h0[((size_t)s * dim + d) * N + n] : 0.0;",
+                                         "h[n] = h0 ? h0[((size_t)0 * dim + d) * N + n] : 0.0;"),
+    "varlen_group_interleaved": ("const size_t bc = (size_t)g * (size_t)N * (size_t)T;",
+                                 "const size_t bc = (size_t)(d % ngroups) * (size_t)N * (size_t)T;"),
+    "pooled_decode_reads_batch_row": ("double *h = &state_pool[((size_t)slot * dim + d) * N];",
+                                      "double *h = &state_pool[((size_t)b * dim + d) * N];"),
 }
 
 PIN_TESTS = [
@@ -63,6 +74,8 @@ PIN_TESTS = [
     lambda: conv_pins.test_conv_history_splits_sequence(9),
     lambda: conv_pins.test_conv_decode_steps_equal_conv(),
     lambda: conv_pins.test_conv_width_one_is_pointwise(),
+    lambda: varlen_pins.test_varlen_equals_each_sequence_alone(),
+    lambda: varlen_pins.test_pooled_decode_equals_gathered_decode(),
 ]
 
 
