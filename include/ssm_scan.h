@@ -235,6 +235,53 @@ ssm_status_t ssm_state_update(float *state, const void *u, const void *delta, co
                               ssm_dtype_t io, void *stream);
 
 /*
+ * ssm_state_update_pooled -- the decode step on a pool of states (continuous
+ * batching: sequences join and leave a serving batch between steps, each
+ * keeping its state in a slot of one pool).  Batch row b advances state slot
+ * state_indices[b]; an index outside [0, nslots) (a negative one, say) marks a
+ * padding row, which touches no state and leaves y[b, :] unwritten.
+ *   state_pool    : [nslots, dim, dstate] fp32, the rows' slots read and
+ *                   overwritten in place
+ *   state_indices : [batch] int32; the ones in [0, nslots) must be distinct
+ *   nslots        : slots in the pool (>= 1)
+ *   other arguments as in ssm_state_update.
+ * ssm_state_update is this call with state_indices = NULL (row b uses slot b,
+ * nslots = batch).  With state_indices, nslots must be >= 1; without, it must
+ * equal batch (SSM_ERR_INVALID_ARG otherwise).
+ */
+ssm_status_t ssm_state_update_pooled(float *state_pool, const int *state_indices, int nslots, const void *u,
+                                     const void *delta, const void *z, const float *A, const void *B,
+                                     const void *C, const float *Dskip, const float *dt_bias, void *y,
+                                     int batch, int dim, int dstate, int ngroups, ssm_dtype_t io, void *stream);
+
+/*
+ * ssm_scan_fwd_varlen -- the scan over a packed batch of sequences of
+ * different lengths (serving: no padding).  The sequences lie end to end
+ * along time in one row; sequence s occupies times
+ * [cu_seqlens[s], cu_seqlens[s+1]) and is its own run of the recurrence
+ * (eightmm.github.io "Mamba", Architecture Contract: sequence in, sequence
+ * out, a recurrent state per sequence): its state starts from h0[s] (or 0) and
+ * its end state goes to h_final[s].
+ *   u, delta, z, y : [dim, total] io type (z nullable)
+ *   A              : [dim, dstate] fp32
+ *   B, C           : [ngroups, dstate, total] io type
+ *   Dskip, dt_bias : [dim] fp32, or NULL
+ *   h0, h_final    : [nseq, dim, dstate] fp32, or NULL
+ *   cu_seqlens     : [nseq + 1] int32 on the device, cu_seqlens[0] = 0,
+ *                    non-decreasing, cu_seqlens[nseq] = total
+ * The offsets are not read on the host; offsets outside [0, total] are
+ * clamped into it on the device (the result is then meaningless, but every
+ * access stays in bounds).  One CTA scans one channel block of one sequence,
+ * so the parallelism is channel blocks x sequences: a long sequence is not
+ * split in time.  Errors as for ssm_scan_fwd (batch is 1); nseq < 1 or a NULL
+ * cu_seqlens is SSM_ERR_INVALID_ARG.
+ */
+ssm_status_t ssm_scan_fwd_varlen(const void *u, const void *delta, const void *z, const float *A,
+                                 const void *B, const void *C, const float *Dskip, const float *dt_bias,
+                                 const float *h0, const int *cu_seqlens, void *y, float *h_final, int dim,
+                                 int dstate, int total, int ngroups, int nseq, ssm_dtype_t io, void *stream);
+
+/*
  * ssm_causal_conv1d_fwd -- the short causal convolution in front of the scan.
  * The pages place a local convolution between the input projection and the
  * selective SSM (eightmm.github.io "Mamba", Block Structure: it adds

@@ -54,6 +54,8 @@ struct DecodeTmaParams {
     int nblk;              // channel blocks per sequence
     long long ntiles;      // batch * nblk
     int has_z;
+    const int* slots;      // nullable: row b uses state slot slots[b] (outside [0, nslots): padding)
+    int nslots;
 };
 
 template <typename T, int CH_, int STAGES_, bool ACCURATE>
@@ -98,6 +100,13 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_con
         cb = static_cast<int>(t / p.batch);
         b = static_cast<int>(t % p.batch);
     };
+    // State slot of batch row b: b itself, or the caller's slot; -1 for a
+    // padding row (an index outside [0, nslots)), which loads slot 0, computes
+    // on it and stores nothing.
+    auto slot_of = [&](int b) {
+        const int sl = p.slots ? __ldg(p.slots + b) : b;
+        return sl >= 0 && sl < p.nslots ? sl : -1;
+    };
     auto issue = [&](int k) {  // thread 0 only
         int b, cb;
         tile_of(k, b, cb);
@@ -106,7 +115,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_con
         const int d0 = cb * CH;
         const int g = d0 / p.dim_per_group;
         mbar_arrive_expect_tx(&full_bar[s], tx);
-        tma_load_3d(st, &tm_state, 0, d0, b, &full_bar[s]);
+        tma_load_3d(st, &tm_state, 0, d0, max(slot_of(b), 0), &full_bar[s]);
         tma_load_2d(st + Lay::OFF_U, &tm_u, d0, b, &full_bar[s]);
         tma_load_2d(st + Lay::OFF_D, &tm_d, d0, b, &full_bar[s]);
         if (has_z) tma_load_2d(st + Lay::OFF_Z, &tm_z, d0, b, &full_bar[s]);
@@ -201,7 +210,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_con
             }
             *hp = make_float4(h0.x, h0.y, h1.x, h1.y);
         }
-        if (active) {
+        const int slot = slot_of(b);
+        if (active && slot >= 0) {
             float yv = fmaf(dsk, uv, y2.x + y2.y);
             if (has_z) yv *= silu<ACCURATE>(lds_elem<T>(st + Lay::OFF_Z + c * sizeof(T)));
             Elem<T>::store(yp + static_cast<long long>(b) * p.dim + d, yv);
@@ -210,7 +220,9 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_con
         fence_proxy_async_smem();
         __syncthreads();
         if (threadIdx.x == 0) {
-            tma_store_3d(&tm_state, 0, cb * CH, b, st);
+            // One bulk group per tile (empty for a padding row), so that
+            // waiting for all but the newest covers the previous tile's store.
+            if (slot >= 0) tma_store_3d(&tm_state, 0, cb * CH, slot, st);
             bulk_commit();
             if (k >= 1 && k - 1 + STAGES < nt) {
                 bulk_wait_read<1>();

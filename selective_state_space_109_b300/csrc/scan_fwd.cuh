@@ -46,6 +46,11 @@ struct ScanParams {
     int blocks_per_group; // CTAs along the channels of one group
     int vec_ok;           // seqlen is a multiple of the activation packet width
     int bc_vec_ok;        // seqlen is a multiple of the 16-byte B/C packet width
+    // Packed variable-length batch (batch == 1): sequence s occupies times
+    // [cu_seqlens[s], cu_seqlens[s+1]) of the row and starts from h0[s];
+    // h_final[s] is its end state.  NULL: one sequence per batch row.
+    const int* cu_seqlens;
+    int nseq;
 };
 
 template <typename T, int LANES>
@@ -86,22 +91,35 @@ scan_fwd_kernel(const ScanParams p) {
     const int cb = blockIdx.x % p.blocks_per_group;
     const int bg = blockIdx.x / p.blocks_per_group;
     const int g = bg % p.ngroups;
-    const int b = bg / p.ngroups;
+    const int b = bg / p.ngroups;  // sequence: a batch row, or one of the packed sequences
     const int dloc = cb * CH + warp * CPW + cw;
     const bool active = dloc < p.dim_per_group;
     const int d = g * p.dim_per_group + (active ? dloc : 0);
-    const int L = p.seqlen;
-
-    const long long row = (static_cast<long long>(b) * p.dim + d) * L;
+    // This CTA's run of time: a whole row, or one packed sequence of the
+    // single row (its offsets clamped into the row, so that any offsets stay
+    // in bounds).  Lst is the row stride of every [.., L] tensor.
+    const long long Lst = p.seqlen;
+    long long seg0 = 0;
+    int L = p.seqlen;
+    const bool packed = p.cu_seqlens != nullptr;
+    if (packed) {
+        const int s0 = min(max(__ldg(p.cu_seqlens + b), 0), p.seqlen);
+        const int s1 = min(max(__ldg(p.cu_seqlens + b + 1), s0), p.seqlen);
+        seg0 = s0;
+        L = s1 - s0;
+    }
+    const long long rowb = packed ? 0 : b;  // the tensors' batch row
+    const long long row = (rowb * p.dim + d) * Lst + seg0;
     const T* __restrict__ u_row = static_cast<const T*>(p.u) + row;
     const T* __restrict__ dl_row = static_cast<const T*>(p.delta) + row;
     const T* __restrict__ z_row = p.z ? static_cast<const T*>(p.z) + row : nullptr;
     T* __restrict__ y_row = static_cast<T*>(p.y) + row;
-    const long long bc_off = (static_cast<long long>(b) * p.ngroups + g) * N * static_cast<long long>(L);
+    const long long bc_off = (rowb * p.ngroups + g) * N * Lst + seg0;
     const T* __restrict__ Bg = static_cast<const T*>(p.B) + bc_off;
     const T* __restrict__ Cg = static_cast<const T*>(p.C) + bc_off;
-    const bool vec_ok = p.vec_ok != 0;
-    const bool bc_vec_ok = p.bc_vec_ok != 0;
+    // Vector packets need the run to start on a packet boundary.
+    const bool vec_ok = p.vec_ok != 0 && seg0 % V == 0;
+    const bool bc_vec_ok = p.bc_vec_ok != 0 && seg0 % VE == 0;
     const bool has_z = z_row != nullptr;
 
     // Per-lane constants: A (scaled for the exp form in use) for this lane's
@@ -130,7 +148,7 @@ scan_fwd_kernel(const ScanParams p) {
                 const int r = item % (2 * N);  // (n, B|C) row, fastest across threads
                 const int tv = item / (2 * N);
                 const int n = r >> 1;
-                const T* src = ((r & 1) ? Cg : Bg) + static_cast<long long>(n) * L + t0 + tv * VE;
+                const T* src = ((r & 1) ? Cg : Bg) + static_cast<long long>(n) * Lst + t0 + tv * VE;
                 const int valid = L - (t0 + tv * VE);
                 if (bc_vec_ok && valid >= VE) bc_reg[i].load_cached(src);
                 else if (valid > 0) bc_reg[i].load_partial(src, valid);

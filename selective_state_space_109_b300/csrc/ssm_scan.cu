@@ -458,9 +458,9 @@ bool decode_tma_eligible(int batch, int dim, int dstate, int ngroups, ssm_dtype_
 }
 
 template <typename T, int CH, int STAGES>
-cudaError_t launch_decode_tma_v(float* state, const void* u, const void* delta, const void* z, const float* A,
-                                const void* B, const void* C, const float* Dskip, const float* dt_bias, void* y,
-                                int batch, int dim, int ngroups, cudaStream_t st) {
+cudaError_t launch_decode_tma_v(float* state, const int* slots, int nslots, const void* u, const void* delta,
+                                const void* z, const float* A, const void* B, const void* C, const float* Dskip,
+                                const float* dt_bias, void* y, int batch, int dim, int ngroups, cudaStream_t st) {
     using Lay = ssm::DecodeTmaLayout<T, CH, STAGES>;
     constexpr int N = Lay::N;
     if (!encode_tiled()) return cudaErrorNotSupported;
@@ -469,8 +469,8 @@ cudaError_t launch_decode_tma_v(float* state, const void* u, const void* delta, 
     const cuuint64_t es = sizeof(T);
     const cuuint32_t e1[3] = {1, 1, 1};
     CUtensorMap ms, mu, md, mz, mB, mC;
-    {  // state [batch, dim, N] fp32, box [N, CH, 1], 64-byte swizzle
-        const cuuint64_t dims[3] = {N, static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(batch)};
+    {  // state [nslots, dim, N] fp32, box [N, CH, 1], 64-byte swizzle
+        const cuuint64_t dims[3] = {N, static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(nslots)};
         const cuuint64_t str[2] = {N * 4, static_cast<cuuint64_t>(dim) * N * 4};
         const cuuint32_t box[3] = {N, Lay::CH, 1};
         if (encode_tiled()(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, state, dims, str, box, e1,
@@ -504,6 +504,8 @@ cudaError_t launch_decode_tma_v(float* state, const void* u, const void* delta, 
     p.nblk = (dim + Lay::CH - 1) / Lay::CH;
     p.ntiles = static_cast<long long>(p.nblk) * batch;
     p.has_z = z != nullptr;
+    p.slots = slots;
+    p.nslots = nslots;
 
     auto kern = ssm::decode_tma_kernel<T, CH, STAGES, sizeof(T) == 4>;
     static unsigned long long done = 0;
@@ -521,22 +523,24 @@ cudaError_t launch_decode_tma_v(float* state, const void* u, const void* delta, 
 // pipeline stages.  SSM_DECODE_TILE=<channels>x<stages> overrides the default
 // for tuning.
 template <typename T>
-cudaError_t launch_decode_tma(float* state, const void* u, const void* delta, const void* z, const float* A,
-                              const void* B, const void* C, const float* Dskip, const float* dt_bias, void* y,
-                              int batch, int dim, int ngroups, cudaStream_t st) {
+cudaError_t launch_decode_tma(float* state, const int* slots, int nslots, const void* u, const void* delta,
+                              const void* z, const float* A, const void* B, const void* C, const float* Dskip,
+                              const float* dt_bias, void* y, int batch, int dim, int ngroups, cudaStream_t st) {
     // 128 channels x 3 stages measured fastest on B300 (32 us for batch 256 x
     // 5120 channels; 128x4, 64x4, 64x6 within 4%, 32x8 30% slower).
     int ch = 128, stages = 3;
     if (const char* v = std::getenv("SSM_DECODE_TILE")) std::sscanf(v, "%dx%d", &ch, &stages);
 #define SSM_DECODE_V(C_, S_) \
     if (ch == C_ && stages == S_) \
-        return launch_decode_tma_v<T, C_, S_>(state, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, dim, ngroups, st);
+        return launch_decode_tma_v<T, C_, S_>(state, slots, nslots, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, \
+                                              dim, ngroups, st);
     SSM_DECODE_V(128, 4)
     SSM_DECODE_V(64, 4)
     SSM_DECODE_V(64, 6)
     SSM_DECODE_V(32, 8)
 #undef SSM_DECODE_V
-    return launch_decode_tma_v<T, 128, 3>(state, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, dim, ngroups, st);
+    return launch_decode_tma_v<T, 128, 3>(state, slots, nslots, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, dim,
+                                          ngroups, st);
 }
 
 bool force_generic() {
@@ -816,30 +820,33 @@ ssm_status_t ssm_device_status(int clear, void* stream) {
     return word == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
 }
 
-ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, const void* z,
-                              const float* A, const void* B, const void* C, const float* Dskip,
-                              const float* dt_bias, void* y, int batch, int dim, int dstate,
-                              int ngroups, ssm_dtype_t io, void* stream) {
+ssm_status_t ssm_state_update_pooled(float* state_pool, const int* state_indices, int nslots, const void* u,
+                                     const void* delta, const void* z, const float* A, const void* B, const void* C,
+                                     const float* Dskip, const float* dt_bias, void* y, int batch, int dim,
+                                     int dstate, int ngroups, ssm_dtype_t io, void* stream) {
+    float* state = state_pool;
     if (batch < 0 || dim <= 0 || dstate <= 0 || ngroups <= 0 || dim % ngroups != 0)
         return SSM_ERR_INVALID_ARG;
     if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
     if (!supported_dstate(dstate)) return SSM_ERR_UNSUPPORTED;
     if (batch == 0) return SSM_OK;
     if (!state || !u || !delta || !A || !B || !C || !y) return SSM_ERR_INVALID_ARG;
-    const void* ptrs[] = {state, u, delta, z, A, B, C, Dskip, dt_bias, y};
+    if (state_indices ? nslots < 1 : nslots != batch) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {state, state_indices, u, delta, z, A, B, C, Dskip, dt_bias, y};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return SSM_ERR_MISALIGNED;
 
     ssm::DecodeParams p{};
     p.state = state; p.u = u; p.delta = delta; p.z = z; p.A = A; p.B = B; p.C = C;
-    p.D = Dskip; p.dt_bias = dt_bias; p.y = y;
+    p.D = Dskip; p.dt_bias = dt_bias; p.y = y; p.slots = state_indices; p.nslots = nslots;
     p.batch = batch; p.dim = dim; p.ngroups = ngroups; p.dim_per_group = dim / ngroups;
     cudaStream_t st0 = static_cast<cudaStream_t>(stream);
     if (decode_tma_eligible(batch, dim, dstate, ngroups, io) && !force_generic()) {
         const cudaError_t e = io == SSM_F32
-            ? launch_decode_tma<float>(state, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, dim, ngroups, st0)
-            : launch_decode_tma<__nv_bfloat16>(state, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, dim, ngroups,
-                                               st0);
+            ? launch_decode_tma<float>(state, state_indices, nslots, u, delta, z, A, B, C, Dskip, dt_bias, y, batch,
+                                       dim, ngroups, st0)
+            : launch_decode_tma<__nv_bfloat16>(state, state_indices, nslots, u, delta, z, A, B, C, Dskip, dt_bias, y,
+                                               batch, dim, ngroups, st0);
         if (e != cudaSuccess) return cuda_fail(e);
         return SSM_OK;
     }
@@ -866,6 +873,50 @@ ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, co
     return SSM_OK;
 }
 
+ssm_status_t ssm_state_update(float* state, const void* u, const void* delta, const void* z,
+                              const float* A, const void* B, const void* C, const float* Dskip,
+                              const float* dt_bias, void* y, int batch, int dim, int dstate,
+                              int ngroups, ssm_dtype_t io, void* stream) {
+    return ssm_state_update_pooled(state, nullptr, batch, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, dim,
+                                   dstate, ngroups, io, stream);
+}
+
+
+ssm_status_t ssm_scan_fwd_varlen(const void* u, const void* delta, const void* z, const float* A, const void* B,
+                                 const void* C, const float* Dskip, const float* dt_bias, const float* h0,
+                                 const int* cu_seqlens, void* y, float* h_final, int dim, int dstate, int total,
+                                 int ngroups, int nseq, ssm_dtype_t io, void* stream) {
+    const ssm_status_t s = check_scan_args(u, delta, z, A, B, C, Dskip, dt_bias, y, h0, h_final, 1, dim, dstate,
+                                           total, ngroups, io);
+    if (s != SSM_OK) return s;
+    if (nseq < 1 || !cu_seqlens) return SSM_ERR_INVALID_ARG;
+    if (!aligned16(cu_seqlens)) return SSM_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (total == 0) {
+        if (h_final) {
+            const long long n = static_cast<long long>(nseq) * dim * dstate;
+            copy_or_zero_state_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(h0, h_final, n);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        return SSM_OK;
+    }
+    ssm::ScanParams p{};
+    p.u = u; p.delta = delta; p.z = z; p.A = A; p.B = B; p.C = C; p.D = Dskip;
+    p.dt_bias = dt_bias; p.y = y; p.h0 = h0; p.h_final = h_final;
+    p.batch = nseq;  // one CTA row per packed sequence
+    p.dim = dim; p.seqlen = total; p.ngroups = ngroups;
+    p.dim_per_group = dim / ngroups;
+    p.cu_seqlens = cu_seqlens; p.nseq = nseq;
+    int lanes = choose_lanes(nseq * dim, dstate, device_sm_count());
+    const int forced = env_int("SSM_FORCE_LANES", 0);
+    if (forced == 1 || forced == 2 || forced == 4 || forced == 8) lanes = forced;
+    if (lanes > dstate / 2) lanes = dstate / 2;
+    const cudaError_t e = (io == SSM_F32) ? launch_scan_t<float>(p, dstate, lanes, st)
+                                          : launch_scan_t<__nv_bfloat16>(p, dstate, lanes, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return SSM_OK;
+}
 
 ssm_status_t ssm_causal_conv1d_fwd(const void* x, const float* w, const float* bias, const void* x_prev,
                                    void* out, void* x_last, int batch, int dim, int seqlen, int width,

@@ -28,6 +28,8 @@ struct DecodeParams {
     const float* D;       // nullable
     const float* dt_bias; // nullable
     void* y;
+    const int* slots;     // nullable: row b uses state slot slots[b] (outside [0, nslots): padding)
+    int nslots;
     int batch, dim, ngroups, dim_per_group;
 };
 
@@ -63,8 +65,10 @@ state_update_kernel(const DecodeParams p) {
     for (int i = 0; i < BPT; ++i) {
         const int b = blockIdx.y * BPT + i;
         if (b >= p.batch) break;  // uniform over the CTA
+        const int slot = p.slots ? __ldg(p.slots + b) : b;
+        if (slot < 0 || slot >= p.nslots) continue;  // a padding row (uniform over the CTA)
         const long long bd = static_cast<long long>(b) * p.dim + dc;
-        float4* sp = reinterpret_cast<float4*>(p.state + bd * N) + q;
+        float4* sp = reinterpret_cast<float4*>(p.state + (static_cast<long long>(slot) * p.dim + dc) * N) + q;
         const float4 s = active ? *sp : make_float4(0.f, 0.f, 0.f, 0.f);
         const float uv = Elem<T>::load(up + bd);
         const float dt = softplus<ACCURATE>(Elem<T>::load(dp + bd) + bias);

@@ -173,6 +173,30 @@ def make_conv_inputs(batch, dim, seqlen, width=4, io="bf16", seed=0, device="cpu
     return dict(x=mv(x), w=mv(w), bias=mv(bias), x_prev=mv(prev))
 
 
+def make_varlen_inputs(dim, dstate, lengths, ngroups=1, io="bf16", recipe="scaled", seed=0, device="cpu",
+                       with_h0=False):
+    """A packed batch of sequences of the given lengths laid end to end along
+    time: the tensors of make_scan_inputs for one row of T = sum(lengths)
+    steps with the batch axis dropped (u, delta, z [dim, T]; B, C [G, N, T]),
+    h0 [nseq, dim, N] when asked, and cu_seqlens [nseq + 1] int32."""
+    T = int(sum(lengths))
+    x = make_scan_inputs(1, dim, dstate, T, ngroups, io=io, recipe=recipe, seed=seed, device="cpu")
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    out = dict(u=x.u[0], delta=x.delta[0], z=x.z[0], A=x.A, B=x.B[0], C=x.C[0], D=x.D, dt_bias=x.dt_bias,
+               cu_seqlens=cu)
+    if with_h0:
+        out["h0"] = _randn((len(lengths), dim, dstate), seed, "h0", "cpu")
+    return {k: (v.contiguous().to(device) if v is not None else None) for k, v in out.items()}
+
+
+def varlen_lengths(n, mean, seed=0):
+    """n sequence lengths drawn uniformly from [1, 2 * mean - 1] (a serving
+    batch: mixed lengths, no padding), from the seeded stream of tensor "dt"."""
+    g = _gen(seed, "dt", "cpu", step=7)
+    return [int(v) for v in torch.randint(1, 2 * mean, (n,), generator=g)]
+
+
 def compulsory_bytes_conv(batch, dim, seqlen, io) -> int:
     """x read and out written once ([batch, dim, L] each)."""
     return 2 * batch * dim * seqlen * (4 if io == "f32" else 2)

@@ -63,6 +63,10 @@ def _load() -> ctypes.CDLL:
     L.ssm_device_status.restype = I
     L.ssm_state_update.argtypes = [P] * 10 + [I] * 5 + [P]
     L.ssm_state_update.restype = I
+    L.ssm_scan_fwd_varlen.argtypes = [P] * 12 + [I] * 6 + [P]
+    L.ssm_scan_fwd_varlen.restype = I
+    L.ssm_state_update_pooled.argtypes = [P, P, I] + [P] * 9 + [I] * 5 + [P]
+    L.ssm_state_update_pooled.restype = I
     L.ssm_causal_conv1d_fwd.argtypes = [P] * 6 + [I] * 6 + [P]
     L.ssm_causal_conv1d_fwd.restype = I
     L.ssm_causal_conv1d_update.argtypes = [P] * 5 + [I] * 5 + [P]
@@ -203,17 +207,25 @@ def device_status(clear: bool = False, device=None) -> int:
         return int(lib.ssm_device_status(int(bool(clear)), _stream_handle(dev)))
 
 
-def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None) -> torch.Tensor:
-    """One decode step: updates ``state`` [batch, dim, N] in place, returns y [batch, dim]."""
+def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None,
+                 state_indices=None) -> torch.Tensor:
+    """One decode step: updates ``state`` [batch, dim, N] in place, returns y
+    [batch, dim].  With ``state_indices`` ([batch] int32), ``state`` is a pool
+    [nslots, dim, N] and row b advances slot state_indices[b] (outside
+    [0, nslots): a padding row, whose y is left unwritten)."""
     if state.device.type != "cuda":
         raise ValueError("tensors must be on a CUDA device")
     if state.dim() != 3 or B.dim() != 3:
         raise ValueError("expected state [batch, dim, N], B [batch, G, N]")
-    batch, dim, N = state.shape
+    nslots, dim, N = state.shape
+    batch = u.shape[0]
     G = B.shape[1]
     dev, io = state.device, u.dtype
     _io_code(io)
-    _check(state, "state", (batch, dim, N), torch.float32, dev)
+    if state_indices is None and nslots != batch:
+        raise ValueError("state must be [batch, dim, N] without state_indices")
+    _check(state, "state", (nslots, dim, N), torch.float32, dev)
+    _check(state_indices, "state_indices", (batch,), torch.int32, dev)
     _check(u, "u", (batch, dim), io, dev)
     _check(delta, "delta", (batch, dim), io, dev)
     _check(z, "z", (batch, dim), io, dev)
@@ -225,11 +237,11 @@ def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=
     y = torch.empty((batch, dim), dtype=io, device=dev) if out is None else out
     _check(y, "out", (batch, dim), io, dev)
     with torch.cuda.device(dev):
-        st = lib.ssm_state_update(_ptr(state), _ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B),
-                                  _ptr(C), _ptr(D), _ptr(dt_bias), _ptr(y), batch, dim, N, G,
-                                  _io_code(io), _stream_handle(dev))
+        st = lib.ssm_state_update_pooled(_ptr(state), _ptr(state_indices), nslots, _ptr(u), _ptr(delta), _ptr(z),
+                                         _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias), _ptr(y), batch, dim, N,
+                                         G, _io_code(io), _stream_handle(dev))
     if st != 0:
-        raise SsmError(st, "ssm_state_update")
+        raise SsmError(st, "ssm_state_update_pooled")
     return y
 
 
@@ -284,4 +296,41 @@ def causal_conv1d_update(conv_state, x, w, bias=None, *, silu=True, out=None) ->
     if st != 0:
         raise SsmError(st, "ssm_causal_conv1d_update")
     return y
+
+
+def scan_fwd_varlen(u, delta, A, B, C, cu_seqlens, z=None, D=None, dt_bias=None, h0=None, *,
+                    out=None, h_final=None, return_final_state=False):
+    """Scan of a packed batch: u, delta, z [dim, T]; B, C [G, N, T];
+    cu_seqlens [nseq + 1] int32 (device); h0, h_final [nseq, dim, N].
+    Sequence s occupies times [cu_seqlens[s], cu_seqlens[s+1]) and starts
+    from h0[s] (or 0).  Returns y (and h_final when ``return_final_state``)."""
+    if u.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    if u.dim() != 2 or A.dim() != 2 or B.dim() != 3 or cu_seqlens.dim() != 1:
+        raise ValueError("expected u [dim, T], A [dim, N], B [G, N, T], cu_seqlens [nseq + 1]")
+    dim, T = u.shape
+    N = A.shape[1]
+    G = B.shape[0]
+    nseq = cu_seqlens.shape[0] - 1
+    dev, io = u.device, u.dtype
+    _io_code(io)
+    for t, name, shape, dt in ((u, "u", (dim, T), io), (delta, "delta", (dim, T), io), (z, "z", (dim, T), io),
+                               (A, "A", (dim, N), torch.float32), (B, "B", (G, N, T), io),
+                               (C, "C", (G, N, T), io), (D, "D", (dim,), torch.float32),
+                               (dt_bias, "dt_bias", (dim,), torch.float32), (h0, "h0", (nseq, dim, N), torch.float32),
+                               (cu_seqlens, "cu_seqlens", (nseq + 1,), torch.int32)):
+        _check(t, name, shape, dt, dev)
+    y = torch.empty_like(u) if out is None else out
+    _check(y, "out", u.shape, io, dev)
+    hf = h_final
+    if hf is None and return_final_state:
+        hf = torch.empty((nseq, dim, N), dtype=torch.float32, device=dev)
+    _check(hf, "h_final", (nseq, dim, N), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_fwd_varlen(_ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens), _ptr(y), _ptr(hf), dim, N, T, G,
+                                     nseq, _io_code(io), _stream_handle(dev))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_fwd_varlen")
+    return (y, hf) if return_final_state else y
 

@@ -135,3 +135,23 @@ def test_conv_argument_errors(lib):
     assert upd(out=Q) == 1                    # out is x
     assert upd(W=5) == 2
     assert upd(state=MIS) == 3
+
+
+def test_varlen_and_pooled_argument_errors(lib):
+    """Argument checks of the packed scan and the pooled decode step (fake
+    pointers; each call returns before anything is enqueued)."""
+    def varlen(u=P, cu=P, dim=8, N=16, T=64, G=1, nseq=3, io=1):
+        return lib.ssm_scan_fwd_varlen(u, P, None, P, P, P, None, None, None, cu, P, None, dim, N, T, G, nseq, io,
+                                       None)
+    assert varlen(nseq=0) == 1
+    assert varlen(cu=None) == 1
+    assert varlen(cu=MIS) == 3
+    assert varlen(N=12) == 2
+    assert varlen(dim=6, G=4) == 1
+
+    def pooled(idx=None, nslots=2, batch=2):
+        return lib.ssm_state_update_pooled(P, idx, nslots, P, P, None, P, P, P, None, None, P, batch, 4, 16, 1, 1,
+                                           None)
+    assert pooled(idx=None, nslots=3) == 1      # without indices the pool is the batch
+    assert pooled(idx=P, nslots=0) == 1
+    assert pooled(idx=MIS, nslots=4) == 3
