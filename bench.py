@@ -459,6 +459,63 @@ def bench_conv(ssm, I, torch, peaks, width=4):
     return res
 
 
+VARLEN_SHAPE = dict(dim=1536, dstate=16, nseq=64, mean=64)   # serving prefill: 64 sequences, mean 64 tokens
+
+
+def bench_varlen(ssm, I, torch, peaks):
+    """Packed variable-length scan (64 bf16 sequences of mixed lengths, 1536
+    channels) and the decode step on a pool of state slots (the decode shape,
+    rows mapped to a permutation of the slots): device time per launch over
+    rotating inputs (> 3x L2)."""
+    dev = torch.device("cuda")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    vs = VARLEN_SHAPE
+    lengths = I.varlen_lengths(vs["nseq"], vs["mean"], seed=0)
+    T = sum(lengths)
+    nbytes = I.compulsory_bytes_scan(1, vs["dim"], vs["dstate"], T, 1, "bf16")
+    nsets = n_rotating_sets(nbytes, l2)
+    # Rows padded to a multiple of 8 steps (the 16-byte packet) after the last sequence.
+    ins = [I.make_varlen_inputs(vs["dim"], vs["dstate"], lengths, io="bf16", seed=s, device=dev, with_h0=True,
+                                row_multiple=8) for s in range(nsets)]
+    outs = [torch.empty_like(x["u"]) for x in ins]
+    hfs = [torch.empty((vs["nseq"], vs["dim"], vs["dstate"]), device=dev) for _ in ins]
+
+    def launch(i):
+        x = ins[i]
+        ssm.scan_fwd_varlen(x["u"], x["delta"], x["A"], x["B"], x["C"], x["cu_seqlens"], z=x["z"], D=x["D"],
+                            dt_bias=x["dt_bias"], h0=x["h0"], out=outs[i], h_final=hfs[i])
+
+    ms = bench_graph(torch, launch, nsets, reps=max(3, 60 // nsets))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["scan_varlen_bf16_d%d_n%d_mean%d" % (vs["dim"], vs["nseq"], vs["mean"])] = dict(
+        tokens=T, GBps=round(gbs, 1), us_per_launch=round(ms * 1e3, 2),
+        frac_of_hbm_measured=round(gbs / peaks["hbm_gbs"], 4))
+    del ins, outs, hfs
+    wd = I.WORKLOADS[DECODE]
+    b, d, n = wd["batch"], wd["dim"], wd["dstate"]
+    per = I.compulsory_bytes_decode(b, d, n)
+    nsets = n_rotating_sets(per, l2)
+    prm = I.decode_params(d, n, recipe=wd["recipe"], seed=0, device=dev)
+    pools = [I.make_decode_state(b, d, n, seed=s, device=dev) for s in range(nsets)]
+    g = torch.Generator().manual_seed(0)
+    perm = torch.randperm(b, generator=g).to(torch.int32).to(dev)
+    toks = [I.make_decode_token(b, d, n, s, io=wd["io"], recipe=wd["recipe"], seed=0, device=dev)
+            for s in range(nsets)]
+    ys = [torch.empty((b, d), dtype=toks[0]["u"].dtype, device=dev) for _ in range(nsets)]
+
+    def launch_dec(i):
+        t = toks[i]
+        ssm.state_update(pools[i], t["u"], t["delta"], prm["A"], t["B"], t["C"], z=t["z"], D=prm["D"],
+                         dt_bias=prm["dt_bias"], out=ys[i], state_indices=perm)
+
+    ms = bench_graph(torch, launch_dec, nsets, reps=max(3, 200 // nsets))
+    res["decode_pooled_b%d_d%d" % (b, d)] = dict(
+        us_per_step=round(ms * 1e3, 3), state_GBps=round(per / (ms * 1e-3) / 1e9, 1),
+        frac_of_hbm_measured=round(per / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4))
+    return res
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -530,6 +587,7 @@ def run_ours(args):
                                frac_of_hbm_measured=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3)
                                                           / 1e9 / peaks["hbm_gbs"], 4))
         extra.update(bench_conv(ssm, I, torch, peaks))
+        extra.update(bench_varlen(ssm, I, torch, peaks))
 
     base = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -656,6 +714,16 @@ def run_profile_case(args):
             out = torch.empty_like(c["x"])
             for _ in range(args.warmup + args.steps):
                 ssm.causal_conv1d(c["x"], c["w"], c["bias"], out=out)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
+        return
+    if args.profile == "scan_varlen":
+        vs = VARLEN_SHAPE
+        x = I.make_varlen_inputs(vs["dim"], vs["dstate"], I.varlen_lengths(vs["nseq"], vs["mean"], seed=0),
+                                 io="bf16", device=dev, with_h0=True, row_multiple=8)
+        for _ in range(args.warmup + args.steps):
+            ssm.scan_fwd_varlen(x["u"], x["delta"], x["A"], x["B"], x["C"], x["cu_seqlens"], z=x["z"], D=x["D"],
+                                dt_bias=x["dt_bias"], h0=x["h0"], return_final_state=True)
         torch.cuda.synchronize(dev)
         print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
         return

@@ -208,9 +208,11 @@ ssm_status_t ssm_scan_fwd_chunked_static(const void *u, const void *delta, const
 
 /*
  * Synchronises stream, then returns the library's device-wide error word for
- * the current device: SSM_OK, or SSM_ERR_TIMEOUT if any kernel of this library
- * gave up on a bounded device-side wait since the word was last cleared (its
- * outputs are then unreliable).  clear != 0 resets the word afterwards.
+ * the current device: SSM_OK, SSM_ERR_TIMEOUT if any kernel of this library
+ * gave up on a bounded device-side wait since the word was last cleared, or
+ * SSM_ERR_INVALID_ARG if a kernel found an access outside its tensor (packed
+ * sequence offsets that do not describe the row, say) and skipped it; the
+ * outputs are then unreliable.  clear != 0 resets the word afterwards.
  * SSM_ERR_CUDA if the read itself failed.
  */
 ssm_status_t ssm_device_status(int clear, void *stream);
@@ -268,7 +270,11 @@ ssm_status_t ssm_state_update_pooled(float *state_pool, const int *state_indices
  *   Dskip, dt_bias : [dim] fp32, or NULL
  *   h0, h_final    : [nseq, dim, dstate] fp32, or NULL
  *   cu_seqlens     : [nseq + 1] int32 on the device, cu_seqlens[0] = 0,
- *                    non-decreasing, cu_seqlens[nseq] = total
+ *                    non-decreasing, cu_seqlens[nseq] <= total
+ * total is the row length (the stride of every [.., total] tensor); times past
+ * the last sequence are padding, read by nothing, and y there is left
+ * unwritten.  A total that is a multiple of 8 (bf16) or 4 (fp32) keeps every
+ * row on the 16-byte packet grid: the kernel then loads whole packets.
  * The offsets are not read on the host; offsets outside [0, total] are
  * clamped into it on the device (the result is then meaningless, but every
  * access stays in bounds).  One CTA scans one channel block of one sequence,

@@ -280,7 +280,8 @@ int oracle_causal_conv1d_update(double *conv_state, const double *x, const doubl
  *
  * Layouts: u, delta, z, y [dim, T]; B, C [ngroups, dstate, T];
  * h0, h_final [nseq, dim, dstate]; cu_seqlens [nseq + 1], non-decreasing,
- * cu_seqlens[0] = 0 and cu_seqlens[nseq] = T.
+ * cu_seqlens[0] = 0 and cu_seqlens[nseq] <= T (T is the row length; times
+ * past the last sequence are padding, read by nothing and left unwritten).
  */
 int oracle_scan_varlen(const double *u, const double *delta, const double *z,
                        const double *A, const double *B, const double *C,
@@ -290,7 +291,7 @@ int oracle_scan_varlen(const double *u, const double *delta, const double *z,
     if (dim <= 0 || dstate <= 0 || total < 0 || ngroups <= 0 || nseq < 1 || dim % ngroups != 0)
         return ORACLE_BAD_ARG;
     if (!cu_seqlens || !A || (total > 0 && (!u || !delta || !B || !C || !y))) return ORACLE_BAD_ARG;
-    if (cu_seqlens[0] != 0 || cu_seqlens[nseq] != total) return ORACLE_BAD_ARG;
+    if (cu_seqlens[0] != 0 || cu_seqlens[nseq] > total) return ORACLE_BAD_ARG;
     for (int s = 0; s < nseq; s++)
         if (cu_seqlens[s + 1] < cu_seqlens[s]) return ORACLE_BAD_ARG;
     const int N = dstate, T = total;

@@ -26,8 +26,20 @@
 #pragma once
 
 #include "ssm_device.cuh"
+#include "tma.cuh"  // the library's device error word
 
 namespace ssm {
+
+// Range guard of every global access of the kernel below: an access whose
+// elements [lo, hi) are not inside its tensor [0, size) is skipped and
+// reported in the library's device error word (ssm_device_status).  Valid
+// arguments never trip it; it keeps packed offsets that do not describe the
+// row, or any slip in the index arithmetic, from touching other memory.
+__device__ __forceinline__ bool in_range(long long lo, long long hi, long long size) {
+    if (lo >= 0 && lo <= hi && hi <= size) return true;
+    atomicOr(&g_ssm_device_error, kDeviceErrRange);
+    return false;
+}
 
 struct ScanParams {
     const void* u;
@@ -101,14 +113,24 @@ scan_fwd_kernel(const ScanParams p) {
     const long long Lst = p.seqlen;
     long long seg0 = 0;
     int L = p.seqlen;
+    int lead = 0;  // masked steps before a packed sequence's first one
     const bool packed = p.cu_seqlens != nullptr;
     if (packed) {
         const int s0 = min(max(__ldg(p.cu_seqlens + b), 0), p.seqlen);
         const int s1 = min(max(__ldg(p.cu_seqlens + b + 1), s0), p.seqlen);
-        seg0 = s0;
-        L = s1 - s0;
+        // Start the run on the 16-byte boundary at or before the sequence's
+        // first step, so that every load and store stays a whole packet; the
+        // `lead` steps before it belong to the previous sequence: they get
+        // Delta = 0 (the state passes through) and their y is not written.
+        lead = s0 % VE;
+        seg0 = s0 - lead;
+        L = s1 - s0 + lead;
     }
     const long long rowb = packed ? 0 : b;  // the tensors' batch row
+    const long long nrows = packed ? 1 : p.batch;
+    const long long act_size = nrows * p.dim * Lst;                  // u, delta, z, y
+    const long long bc_size = nrows * p.ngroups * N * Lst;           // B, C
+    const long long st_size = (packed ? p.nseq : p.batch) * static_cast<long long>(p.dim) * N;  // h0, h_final
     const long long row = (rowb * p.dim + d) * Lst + seg0;
     const T* __restrict__ u_row = static_cast<const T*>(p.u) + row;
     const T* __restrict__ dl_row = static_cast<const T*>(p.delta) + row;
@@ -132,7 +154,9 @@ scan_fwd_kernel(const ScanParams p) {
         for (int k = 0; k < P; ++k) {
             const float2 av = __ldg(reinterpret_cast<const float2*>(Ad) + k);
             a2[k] = make_float2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
-            h[k] = (h0 && active) ? __ldg(reinterpret_cast<const float2*>(h0) + k) : make_float2(0.f, 0.f);
+            const long long hoff = (static_cast<long long>(b) * p.dim + d) * N + j * S + 2 * k;
+            h[k] = (h0 && active && in_range(hoff, hoff + 2, st_size))
+                       ? __ldg(reinterpret_cast<const float2*>(h0) + k) : make_float2(0.f, 0.f);
         }
     }
     const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
@@ -150,7 +174,10 @@ scan_fwd_kernel(const ScanParams p) {
                 const int n = r >> 1;
                 const T* src = ((r & 1) ? Cg : Bg) + static_cast<long long>(n) * Lst + t0 + tv * VE;
                 const int valid = L - (t0 + tv * VE);
-                if (bc_vec_ok && valid >= VE) bc_reg[i].load_cached(src);
+                const long long boff = bc_off + static_cast<long long>(n) * Lst + t0 + tv * VE;
+                const long long bhi = boff + ((bc_vec_ok && valid >= VE) ? VE : min(max(valid, 0), VE));
+                if (valid > 0 && !in_range(boff, bhi, bc_size)) bc_reg[i].zero();
+                else if (bc_vec_ok && valid >= VE) bc_reg[i].load_cached(src);
                 else if (valid > 0) bc_reg[i].load_partial(src, valid);
                 else bc_reg[i].zero();
             }
@@ -179,7 +206,11 @@ scan_fwd_kernel(const ScanParams p) {
     Packet<T, V> pd_cur, pu_cur, pz_cur, pd_nxt, pu_nxt, pz_nxt;
     auto load_act = [&](int tb0, Packet<T, V>& pd, Packet<T, V>& pu, Packet<T, V>& pz) {
         const int t = tb0 + j * V;
-        const int valid = active ? (L - t) : 0;
+        int valid = active ? (L - t) : 0;
+        {
+            const long long lo = row + t, hi = lo + ((vec_ok && valid >= V) ? V : min(max(valid, 0), V));
+            if (valid > 0 && !in_range(lo, hi, act_size)) valid = 0;
+        }
         load_row<T, V>(pd, dl_row + t, valid, vec_ok);
         load_row<T, V>(pu, u_row + t, valid, vec_ok);
         if (has_z) load_row<T, V>(pz, z_row + t, valid, vec_ok);
@@ -214,7 +245,8 @@ scan_fwd_kernel(const ScanParams p) {
                 pz_cur.to_float(zz);
 #pragma unroll
                 for (int k = 0; k < V; ++k) {
-                    const bool in = active && (tb0 + j * V + k < L);
+                    const int tk = tb0 + j * V + k;
+                    const bool in = active && tk < L && tk >= lead;
                     const float dt = in ? softplus<ACCURATE>(dv[k] + bias) : 0.f;
                     dd_s[warp][cw][j * V + k] = make_float2(dt, dt * uu[k]);
                 }
@@ -253,7 +285,16 @@ scan_fwd_kernel(const ScanParams p) {
                     out[k] = yv;
                 }
                 const int t = tb0 + j * V;
-                store_row<T, V>(y_row + t, out, L - t, vec_ok);
+                if (t >= lead) {
+                    const int valid = L - t;
+                    const long long lo = row + t, hi = lo + ((vec_ok && valid >= V) ? V : min(max(valid, 0), V));
+                    if (valid <= 0 || in_range(lo, hi, act_size)) store_row<T, V>(y_row + t, out, valid, vec_ok);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < V; ++k)
+                        if (t + k >= lead && t + k < L && in_range(row + t + k, row + t + k + 1, act_size))
+                            Elem<T>::store(y_row + t + k, out[k]);
+                }
             }
             pd_cur = pd_nxt;
             pu_cur = pu_nxt;
@@ -268,7 +309,10 @@ scan_fwd_kernel(const ScanParams p) {
     if (p.h_final && active) {
         float* hf = p.h_final + (static_cast<long long>(b) * p.dim + d) * N + j * S;
 #pragma unroll
-        for (int k = 0; k < P; ++k) reinterpret_cast<float2*>(hf)[k] = h[k];
+        for (int k = 0; k < P; ++k) {
+            const long long hoff = (static_cast<long long>(b) * p.dim + d) * N + j * S + 2 * k;
+            if (in_range(hoff, hoff + 2, st_size)) reinterpret_cast<float2*>(hf)[k] = h[k];
+        }
     }
 }
 

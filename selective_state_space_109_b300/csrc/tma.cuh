@@ -14,7 +14,8 @@
 namespace ssm {
 
 // Device-side error bits (OR-ed together).
-constexpr unsigned kDeviceErrTimeout = 1u;
+constexpr unsigned kDeviceErrTimeout = 1u;  // a bounded wait gave up
+constexpr unsigned kDeviceErrRange = 2u;    // an access fell outside its tensor and was skipped
 
 // Library-wide device error word (the library is a single translation unit,
 // so this is its only definition); read and cleared by ssm_device_status.

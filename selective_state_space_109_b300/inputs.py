@@ -174,12 +174,13 @@ def make_conv_inputs(batch, dim, seqlen, width=4, io="bf16", seed=0, device="cpu
 
 
 def make_varlen_inputs(dim, dstate, lengths, ngroups=1, io="bf16", recipe="scaled", seed=0, device="cpu",
-                       with_h0=False):
+                       with_h0=False, row_multiple=1):
     """A packed batch of sequences of the given lengths laid end to end along
     time: the tensors of make_scan_inputs for one row of T = sum(lengths)
-    steps with the batch axis dropped (u, delta, z [dim, T]; B, C [G, N, T]),
-    h0 [nseq, dim, N] when asked, and cu_seqlens [nseq + 1] int32."""
-    T = int(sum(lengths))
+    steps (rounded up to a multiple of row_multiple; the rest is padding) with
+    the batch axis dropped (u, delta, z [dim, T]; B, C [G, N, T]), h0
+    [nseq, dim, N] when asked, and cu_seqlens [nseq + 1] int32."""
+    T = -(-int(sum(lengths)) // row_multiple) * row_multiple
     x = make_scan_inputs(1, dim, dstate, T, ngroups, io=io, recipe=recipe, seed=seed, device="cpu")
     cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)

@@ -76,9 +76,21 @@ def test_varlen_empty_sequence_returns_its_h0():
     np.testing.assert_array_equal(hf[1], c["h0"][1])   # sequence 1 is [7, 7)
 
 
+def test_varlen_padding_after_the_last_sequence_is_not_read():
+    """A row longer than the packed sequences: the trailing times are padding."""
+    c = varlen_case(np.random.default_rng(6))
+    y, hf = oracle.scan_varlen(**c, return_final_state=True)
+    T = c["u"].shape[1]
+    pad = {k: (np.concatenate([v, 100.0 + np.zeros(v.shape[:-1] + (5,))], axis=-1)
+               if k in ("u", "delta", "z", "B", "C") else v) for k, v in c.items()}
+    y2, hf2 = oracle.scan_varlen(**pad, return_final_state=True)
+    np.testing.assert_array_equal(y2[:, :T], y)
+    np.testing.assert_array_equal(hf2, hf)
+
+
 def test_varlen_rejects_bad_offsets():
     c = varlen_case(np.random.default_rng(4))
-    for bad in ([0, 7, 5, 19, 20, 33], [1, 7, 7, 19, 20, 33], [0, 7, 7, 19, 20, 32]):
+    for bad in ([0, 7, 5, 19, 20, 33], [1, 7, 7, 19, 20, 33], [0, 7, 7, 19, 20, 34]):
         with pytest.raises(ValueError):
             oracle.scan_varlen(**dict(c, cu_seqlens=np.array(bad, dtype=np.int32)))
 

@@ -50,6 +50,22 @@ def test_varlen_mixed_lengths(ssm, monkeypatch, io, lanes):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_varlen_padded_row(ssm, io):
+    """Mixed lengths in a row padded to a multiple of 8 steps (whole-packet
+    loads for every channel row); the padding's y is not compared."""
+    lengths = [37, 0, 1, 200, 64, 5, 130]
+    x = I.make_varlen_inputs(96, 16, lengths, ngroups=2, io=io, seed=58, device="cuda", with_h0=True,
+                             row_multiple=8)
+    y, hf = run_varlen(ssm, x)
+    torch.cuda.synchronize()
+    ry, rh = oracle_varlen(x)
+    n = int(x["cu_seqlens"][-1])
+    assert x["u"].shape[1] % 8 == 0 and x["u"].shape[1] > n
+    assert_close(to_np(y)[:, :n], ry[:, :n], io, f"varlen padded row io={io}")
+    assert rel_l2(to_np(hf), rh) <= STATE_REL_L2
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_varlen_aligned_lengths_without_h0(ssm, io):
     """Lengths that keep every start on the packet boundary (vector loads)."""
     lengths = [64, 128, 8, 256]
