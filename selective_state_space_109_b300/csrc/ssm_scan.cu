@@ -34,7 +34,11 @@ ssm_status_t cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool supported_dstate(int n) { return n == 4 || n == 8 || n == 16; }
+bool supported_dstate(int n) { return n == 4 || n == 8 || n == 16 || n == 32 || n == 64; }
+
+// Lanes that may share one channel's N states: each lane keeps an even number
+// of them, at most 16 (the register budget of the update loop).
+constexpr int min_lanes_for(int n) { return n > 16 ? n / 16 : 1; }
 
 int env_int(const char* name, int fallback) {
     const char* s = std::getenv(name);
@@ -87,7 +91,10 @@ int device_sm_count() {
 }
 
 constexpr int kScanWarps = 4;
-constexpr int kScanTile = 64;
+// Steps per staged B/C tile of the generic kernel: 64, or 32 for N = 64 (its
+// fp32 B/C quads of 64 steps would not fit the 48 KB of static shared memory).
+template <int N>
+constexpr int scan_tile() { return N >= 64 ? 32 : 64; }
 
 template <typename T, int N, int LANES>
 cudaError_t launch_scan_variant(ssm::ScanParams p, cudaStream_t st) {
@@ -100,7 +107,7 @@ cudaError_t launch_scan_variant(ssm::ScanParams p, cudaStream_t st) {
     const long long blocks = static_cast<long long>(p.blocks_per_group) * p.ngroups * p.batch;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     constexpr bool kAccurate = sizeof(T) == 4;
-    ssm::scan_fwd_kernel<T, N, LANES, kScanWarps, kScanTile, kAccurate>
+    ssm::scan_fwd_kernel<T, N, LANES, kScanWarps, scan_tile<N>(), kAccurate>
         <<<static_cast<unsigned>(blocks), kScanWarps * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
@@ -108,8 +115,8 @@ cudaError_t launch_scan_variant(ssm::ScanParams p, cudaStream_t st) {
 template <typename T, int N>
 cudaError_t launch_scan_n(const ssm::ScanParams& p, int lanes, cudaStream_t st) {
     switch (lanes) {
-        case 1: return launch_scan_variant<T, N, 1>(p, st);
-        case 2: return launch_scan_variant<T, N, 2>(p, st);
+        case 1: if constexpr (N <= 16) return launch_scan_variant<T, N, 1>(p, st); break;
+        case 2: if constexpr (N <= 32) return launch_scan_variant<T, N, 2>(p, st); break;
         case 4: if constexpr (N >= 8) return launch_scan_variant<T, N, 4>(p, st); break;
         case 8: if constexpr (N >= 16) return launch_scan_variant<T, N, 8>(p, st); break;
         default: break;
@@ -123,6 +130,8 @@ cudaError_t launch_scan_t(const ssm::ScanParams& p, int dstate, int lanes, cudaS
         case 4: return launch_scan_n<T, 4>(p, lanes, st);
         case 8: return launch_scan_n<T, 8>(p, lanes, st);
         case 16: return launch_scan_n<T, 16>(p, lanes, st);
+        case 32: return launch_scan_n<T, 32>(p, lanes, st);
+        case 64: return launch_scan_n<T, 64>(p, lanes, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -161,18 +170,24 @@ struct ScanPlan {
 
 template <typename T, int N, ssm::ScanMode MODE>
 int tma_smem_bytes(int lanes) {
+    constexpr int L1 = N <= 16 ? 1 : N / 16;  // lanes the TMA kernel is built with for this N
     switch (lanes) {
-        case 1: return ssm::TmaScanLayout<T, N, 1, kTmaWarps, MODE>::SMEM_BYTES;
-        case 2: return ssm::TmaScanLayout<T, N, 2, kTmaWarps, MODE>::SMEM_BYTES;
+        case 1: return ssm::TmaScanLayout<T, N, L1, kTmaWarps, MODE>::SMEM_BYTES;
+        case 2: return ssm::TmaScanLayout<T, N, (N <= 32 ? 2 : L1), kTmaWarps, MODE>::SMEM_BYTES;
         default: return ssm::TmaScanLayout<T, N, (N >= 8 ? 4 : 2), kTmaWarps, MODE>::SMEM_BYTES;
     }
 }
 
 template <ssm::ScanMode MODE>
 int tma_smem_for(ssm_dtype_t io, int dstate, int lanes) {
-    if (io == SSM_F32)
+    if (io == SSM_F32) {
+        if (dstate == 32) return tma_smem_bytes<float, 32, MODE>(lanes);
+        if (dstate == 64) return tma_smem_bytes<float, 64, MODE>(lanes);
         return dstate == 4 ? tma_smem_bytes<float, 4, MODE>(lanes)
                            : dstate == 8 ? tma_smem_bytes<float, 8, MODE>(lanes) : tma_smem_bytes<float, 16, MODE>(lanes);
+    }
+    if (dstate == 32) return tma_smem_bytes<__nv_bfloat16, 32, MODE>(lanes);
+    if (dstate == 64) return tma_smem_bytes<__nv_bfloat16, 64, MODE>(lanes);
     return dstate == 4 ? tma_smem_bytes<__nv_bfloat16, 4, MODE>(lanes)
                        : dstate == 8 ? tma_smem_bytes<__nv_bfloat16, 8, MODE>(lanes)
                                      : tma_smem_bytes<__nv_bfloat16, 16, MODE>(lanes);
@@ -216,13 +231,14 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
     const int dpg = dim / ngroups;
     const int kmax = std::max(1, std::min(chunk_cap, max_chunks_for(seqlen, io)));
     const int lmax = dstate >= 8 ? 4 : 2;
+    const int lmin = min_lanes_for(dstate);
     // Time units: one unit ~ one channel-step of a 16-state lane at full rate;
     // ~0.54 ns per unit on B300 at N = 16.
     const double launch_units = 2000.0 / 0.54 * (16.0 / dstate);
     const double chunk_units = 650.0 / 0.54 * (16.0 / dstate);
-    ScanPlan best{1, 1, 1};
+    ScanPlan best{lmin, 1, lmin};
     double best_cost = 1e300;
-    for (int lanes = 1; lanes <= lmax; lanes *= 2) {
+    for (int lanes = lmin; lanes <= lmax; lanes *= 2) {
         const double lane_cost = lanes == 1 ? 1.0 : (lanes == 2 ? 1.2 : 2.0);
         const int ch = kTmaWarps * 32 / lanes;
         const long long blocks = static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
@@ -235,7 +251,7 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
                 // The summary pass picks its own lanes (no readout to reduce:
                 // cheaper lane sharing).
                 double agg_cost = 1e300;
-                for (int la = 1; la <= lmax; la *= 2) {
+                for (int la = lmin; la <= lmax; la *= 2) {
                     const double la_cost = la == 1 ? 1.0 : (la == 2 ? 1.1 : 1.7);
                     const int cha = kTmaWarps * 32 / la;
                     const long long blocks_a = static_cast<long long>((dpg + cha - 1) / cha) * ngroups * batch;
@@ -255,12 +271,12 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
         }
     }
     const int fl = env_int("SSM_FORCE_LANES", 0);
-    if ((fl == 1 || fl == 2 || fl == 4) && fl <= lmax) best.lanes = fl;
+    if ((fl == 1 || fl == 2 || fl == 4) && fl <= lmax && fl >= lmin) best.lanes = fl;
     const int fk = env_int("SSM_FORCE_CHUNKS", 0);
     if (fk >= 1) best.chunks = std::min(fk, kmax);
     if (fl || fk) best.agg_lanes = best.lanes;
     const int fa = env_int("SSM_FORCE_AGG_LANES", 0);
-    if ((fa == 1 || fa == 2 || fa == 4) && fa <= lmax) best.agg_lanes = fa;
+    if ((fa == 1 || fa == 2 || fa == 4) && fa <= lmax && fa >= lmin) best.agg_lanes = fa;
     return best;
 }
 
@@ -358,8 +374,8 @@ template <typename T, int N, ssm::ScanMode MODE>
 cudaError_t launch_tma_lanes(const ScanMaps& m, const ssm::TmaScanParams& p, int lanes, int grid_y,
                              cudaStream_t st) {
     switch (lanes) {
-        case 1: return launch_tma<T, N, 1, MODE>(m, p, grid_y, st);
-        case 2: return launch_tma<T, N, 2, MODE>(m, p, grid_y, st);
+        case 1: if constexpr (N <= 16) return launch_tma<T, N, 1, MODE>(m, p, grid_y, st); break;
+        case 2: if constexpr (N <= 32) return launch_tma<T, N, 2, MODE>(m, p, grid_y, st); break;
         case 4: if constexpr (N >= 8) return launch_tma<T, N, 4, MODE>(m, p, grid_y, st); break;
         default: break;
     }
@@ -373,6 +389,8 @@ cudaError_t launch_tma_n(const ScanMaps& m, const ssm::TmaScanParams& p, int dst
         case 4: return launch_tma_lanes<T, 4, MODE>(m, p, lanes, grid_y, st);
         case 8: return launch_tma_lanes<T, 8, MODE>(m, p, lanes, grid_y, st);
         case 16: return launch_tma_lanes<T, 16, MODE>(m, p, lanes, grid_y, st);
+        case 32: return launch_tma_lanes<T, 32, MODE>(m, p, lanes, grid_y, st);
+        case 64: return launch_tma_lanes<T, 64, MODE>(m, p, lanes, grid_y, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -439,6 +457,8 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
         cfg.numAttrs = 1;
         if (dstate == 4) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<4, kMaxChunks>, agg, h0, BD, plan.chunks);
         else if (dstate == 8) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<8, kMaxChunks>, agg, h0, BD, plan.chunks);
+        else if (dstate == 32) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<32, kMaxChunks>, agg, h0, BD, plan.chunks);
+        else if (dstate == 64) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<64, kMaxChunks>, agg, h0, BD, plan.chunks);
         else e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<16, kMaxChunks>, agg, h0, BD, plan.chunks);
         if (e != cudaSuccess) return cuda_fail(e);
     }
@@ -597,7 +617,7 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
     int lanes = choose_lanes(batch * dim, dstate, device_sm_count());
     const int forced = env_int("SSM_FORCE_LANES", 0);
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8) lanes = forced;
-    if (lanes > dstate / 2) lanes = dstate / 2;
+    lanes = std::max(std::min({lanes, dstate / 2, 8}), min_lanes_for(dstate));
     const cudaError_t e = (io == SSM_F32) ? launch_scan_t<float>(p, dstate, lanes, st)
                                           : launch_scan_t<__nv_bfloat16>(p, dstate, lanes, st);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -862,10 +882,14 @@ ssm_status_t ssm_state_update_pooled(float* state_pool, const int* state_indices
     if (io == SSM_F32) {
         if (dstate == 4) SSM_DECODE_LAUNCH(float, 4, true);
         else if (dstate == 8) SSM_DECODE_LAUNCH(float, 8, true);
+        else if (dstate == 32) SSM_DECODE_LAUNCH(float, 32, true);
+        else if (dstate == 64) SSM_DECODE_LAUNCH(float, 64, true);
         else SSM_DECODE_LAUNCH(float, 16, true);
     } else {
         if (dstate == 4) SSM_DECODE_LAUNCH(__nv_bfloat16, 4, false);
         else if (dstate == 8) SSM_DECODE_LAUNCH(__nv_bfloat16, 8, false);
+        else if (dstate == 32) SSM_DECODE_LAUNCH(__nv_bfloat16, 32, false);
+        else if (dstate == 64) SSM_DECODE_LAUNCH(__nv_bfloat16, 64, false);
         else SSM_DECODE_LAUNCH(__nv_bfloat16, 16, false);
     }
 #undef SSM_DECODE_LAUNCH
@@ -915,7 +939,7 @@ ssm_status_t ssm_scan_fwd_varlen(const void* u, const void* delta, const void* z
     int lanes = std::max(choose_lanes(nseq * dim, dstate, device_sm_count()), std::min(2, dstate / 2));
     const int forced = env_int("SSM_FORCE_LANES", 0);
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8) lanes = forced;
-    if (lanes > dstate / 2) lanes = dstate / 2;
+    lanes = std::max(std::min({lanes, dstate / 2, 8}), min_lanes_for(dstate));
     const cudaError_t e = (io == SSM_F32) ? launch_scan_t<float>(p, dstate, lanes, st)
                                           : launch_scan_t<__nv_bfloat16>(p, dstate, lanes, st);
     if (e != cudaSuccess) return cuda_fail(e);

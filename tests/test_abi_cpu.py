@@ -69,7 +69,7 @@ def test_scan_argument_errors(lib):
     assert scan(lib, L=-5) == 1
     assert scan(lib, dim=6, G=4) == 1          # dim % ngroups
     assert scan(lib, N=12) == 2                # unsupported state size
-    assert scan(lib, N=32) == 2
+    assert scan(lib, N=128) == 2               # N up to 64
     assert scan(lib, io=7) == 2
     assert scan(lib, B=MIS) == 3               # misaligned
     assert scan(lib, z=MIS) == 3

@@ -167,6 +167,16 @@ def test_matches_causal_matrix_mixer(with_h0, gated):
     assert rel_err(y, want) < 1e-12
 
 
+def test_matches_causal_matrix_mixer_large_state():
+    """N = 64 states (the large-state case of the library): the same
+    brute-force causal matrix-mixer expansion."""
+    rng = np.random.default_rng(12)
+    c = rand_case(rng, 1, 3, 64, 13, 1)
+    y = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], z=c["z"], Dskip=c["Dskip"],
+                    dt_bias=c["dt_bias"], h0=c["h0"])
+    assert rel_err(y, brute_force_mixer(c, with_h0=True, gated=True)) < 1e-12
+
+
 def test_groups_read_their_own_B_C():
     """With G = 4 groups of 2 channels, each channel must use its group's B/C:
     the brute force indexes g = d // (dim / G) independently."""
