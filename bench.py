@@ -579,13 +579,16 @@ def run_ours(args):
 
     extra = {}
     if not args.skip_extra and world == 1:
-        for name in ("scan_bf16_b8_d2048_l4096", "scan_bf16_b1_d5120_l65536_final_state"):
+        for name in ("scan_bf16_b8_d2048_l4096", "scan_bf16_b1_d5120_l65536_final_state",
+                     "scan_bf16_b2_d1536_l2048_n64"):
             wx = I.WORKLOADS[name]
             rx = bench_scan_device(ssm, I, torch, wx, max(4, min(args.steps, 40)), 3, preroll_s=0.0)
             extra[name] = dict(GBps=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3) / 1e9, 1),
                                us_per_launch=round(rx["ms_per_launch"] * 1e3, 2),
                                frac_of_hbm_measured=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3)
-                                                          / 1e9 / peaks["hbm_gbs"], 4))
+                                                          / 1e9 / peaks["hbm_gbs"], 4),
+                               Gupd_per_s=round(rx["upd_per_step"] / (rx["ms_per_launch"] * 1e-3) / 1e9, 1),
+                               plan=rx["plan"])
         extra.update(bench_conv(ssm, I, torch, peaks))
         extra.update(bench_varlen(ssm, I, torch, peaks))
 

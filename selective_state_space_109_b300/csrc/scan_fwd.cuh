@@ -193,7 +193,10 @@ scan_fwd_kernel(const ScanParams p) {
                 const int tv = item / (2 * N);
                 const int n = r >> 1;
                 const int isC = r & 1;
-                const int off = (n >> 1) * 4 + isC * 2 + (n & 1);
+                // Pair k of sub-lane j sits at k * LANES + j: the lanes of a
+                // channel read adjacent quads (no bank conflicts).
+                const int q = n >> 1;
+                const int off = ((q % P) * LANES + q / P) * 4 + isC * 2 + (n & 1);
                 float f[VE];
                 bc_reg[i].to_float(f);
 #pragma unroll
@@ -255,7 +258,7 @@ scan_fwd_kernel(const ScanParams p) {
 
             // Scan: every lane advances its S states through all TB steps.
             float acc[TB];
-            const float4* bcq = &bc_s[buf][blk * TB][j * P];
+            const float4* bcq = &bc_s[buf][blk * TB][j];
 #pragma unroll
             for (int st = 0; st < TB; ++st) {
                 const float2 dd = dd_s[warp][cw][st];
@@ -264,7 +267,7 @@ scan_fwd_kernel(const ScanParams p) {
                 float2 y2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < P; ++k) {
-                    const float4 q = bcq[st * NQ + k];
+                    const float4 q = bcq[st * NQ + k * LANES];
                     const float2 x = __fmul2_rn(dt2, a2[k]);
                     const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
                     const float2 bx = __fmul2_rn(du2, make_float2(q.x, q.y));

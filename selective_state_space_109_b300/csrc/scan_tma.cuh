@@ -97,7 +97,11 @@ struct TmaScanLayout {
     // runs STAGES - 2 tiles ahead; the summary pass runs STAGES - 1 ahead.
     static constexpr int STAGES = FULL ? 4 : 3;
     static constexpr int STAGE_BYTES = ((NACT * ACT_BYTES + NBC * BC_BYTES) + 1023) / 1024 * 1024;
-    static constexpr int BCF_BYTES = TileShape<T>::TS * N * 4 * NBC;  // widened B (, C)
+    // Widened B (, C): one row of N/2 state pairs per step plus one pad pair,
+    // so that the widening loop's stores (consecutive steps of one pair) fall
+    // in different banks.
+    static constexpr int BCF_ROW = N / 2 + 1;
+    static constexpr int BCF_BYTES = TileShape<T>::TS * BCF_ROW * 8 * NBC;
     // Per-warp scratch through which the lanes of a channel share (Delta,
     // Delta u) for one 16-byte chunk: two buffers (alternating chunks) of one
     // padded row of VPC float4 per channel.
@@ -198,6 +202,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     constexpr int S = N / LANES;       // states per lane
     constexpr int P = S / 2;           // fp32x2 state pairs per lane
     constexpr int NQ = N / 2;          // state pairs per step
+    constexpr int NQP = Lay::BCF_ROW;  // widened row stride (pairs)
     constexpr int H = VPC / LANES;     // steps per lane per 16-byte chunk
     // Per-step scalar work (softplus, Delta u, gate) in fp32x2 pairs of steps.
     constexpr bool PACKED = !ACCURATE && (H % 2 == 0);
@@ -319,20 +324,24 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         mbar_wait(&full_bar[s], static_cast<uint32_t>((i / STAGES) & 1), p.status);
 
         // Widen this tile's B (and C) rows into per-step fp32 pairs/quads.
+        // Steps run fastest over the threads (a warp reads whole 32-byte rows:
+        // no bank conflicts).  Within a step row, pair k of sub-lane j sits at
+        // k * LANES + j, so that the lanes of a channel read adjacent entries.
         {
             const unsigned char* bsrc = st + Lay::NACT * Lay::ACT_BYTES;
             for (int item = threadIdx.x; item < TS * NQ; item += THREADS) {
-                const int t = item / NQ;
-                const int q = item % NQ;
+                const int t = item % TS;
+                const int q = item / TS;
+                const int slot = t * NQP + (q % P) * LANES + q / P;
                 const unsigned char* b0 = bsrc + (2 * q) * Sh::kRowBytes + t * static_cast<int>(sizeof(T));
                 const float B0 = lds_elem<T>(b0);
                 const float B1 = lds_elem<T>(b0 + Sh::kRowBytes);
                 if constexpr (FULL) {
                     const unsigned char* c0 = b0 + Lay::BC_BYTES;
-                    reinterpret_cast<float4*>(bcf)[item] =
+                    reinterpret_cast<float4*>(bcf)[slot] =
                         make_float4(B0, B1, lds_elem<T>(c0), lds_elem<T>(c0 + Sh::kRowBytes));
                 } else {
-                    reinterpret_cast<float2*>(bcf)[item] = make_float2(B0, B1);
+                    reinterpret_cast<float2*>(bcf)[slot] = make_float2(B0, B1);
                 }
             }
         }
@@ -415,11 +424,11 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                     }
                 }
                 if constexpr (FULL) {
-                    const float4* q4 = reinterpret_cast<const float4*>(bcf) + row * NQ + j * P;
+                    const float4* q4 = reinterpret_cast<const float4*>(bcf) + row * NQP + j;
                     float2 y2 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int k = 0; k < P; ++k) {
-                        const float4 q = q4[k];
+                        const float4 q = q4[k * LANES];
                         const float2 x = __fmul2_rn(dt2, a2[k]);
                         const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
                         const float2 bx = __fmul2_rn(du2, make_float2(q.x, q.y));
@@ -428,10 +437,10 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                     }
                     acc[kk] = y2.x + y2.y;
                 } else {
-                    const float2* q2 = reinterpret_cast<const float2*>(bcf) + row * NQ + j * P;
+                    const float2* q2 = reinterpret_cast<const float2*>(bcf) + row * NQP + j;
 #pragma unroll
                     for (int k = 0; k < P; ++k) {
-                        const float2 bq = q2[k];
+                        const float2 bq = q2[k * LANES];
                         const float2 x = __fmul2_rn(dt2, a2[k]);
                         const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
                         h[k] = __ffma2_rn(abar, h[k], __fmul2_rn(du2, bq));

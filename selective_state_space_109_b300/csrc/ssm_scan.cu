@@ -219,44 +219,50 @@ double pass_time(long long ctas, int cap, double work) {
     return t;
 }
 
+// Time of one step of a CTA whose lanes hold S states each (units below): a
+// fixed part per step (softplus, the Delta exchange, the readout and gate)
+// plus a part per state, plus the cross-lane reduction at 4 lanes.  Fitted to
+// B300 timings at N = 16, 32 and 64 over 1, 2 and 4 lanes; the summary pass
+// has no readout and a smaller fixed part.
+double step_time(int S, int lanes, bool summary) {
+    const double shared = lanes >= 4 ? 12.8 : 0.0;
+    return summary ? 12.8 + 7.2 * S + shared : 25.6 + 6.4 * S + shared;
+}
+
 // Picks lanes per channel and time chunks by a wave model of the two passes,
-// fitted to B300 timings of the three bf16 scan workloads over plans of 1 to 32
-// chunks and 1, 2 or 4 lanes.  Per-update cost of sharing a channel's states
-// over 2 or 4 lanes: 1.2 and 2.0 in the full pass, 1.1 and 1.7 in the summary
-// pass (no readout to reduce); the summary pass costs 0.9 of a full pass; the
-// two extra kernels cost about 2 us, and each chunk about 0.65 us more (every
-// chunk's CTAs fetch their first tiles at once when the kernel starts).
+// fitted to B300 timings of the bf16 scan workloads over plans of 1 to 32
+// chunks and 1, 2 or 4 lanes.  The summary pass costs 0.9 of its step time;
+// the two extra kernels cost about 2 us, and each chunk about 0.65 us more
+// (every chunk's CTAs fetch their first tiles at once when the kernel starts).
 ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io,
                    int chunk_cap) {
     const int dpg = dim / ngroups;
     const int kmax = std::max(1, std::min(chunk_cap, max_chunks_for(seqlen, io)));
     const int lmax = dstate >= 8 ? 4 : 2;
     const int lmin = min_lanes_for(dstate);
-    // Time units: one unit ~ one channel-step of a 16-state lane at full rate;
-    // ~0.54 ns per unit on B300 at N = 16.
-    const double launch_units = 2000.0 / 0.54 * (16.0 / dstate);
-    const double chunk_units = 650.0 / 0.54 * (16.0 / dstate);
+    // Time units: ~0.54 ns of an SM each on B300 (one step of a CTA of
+    // 16-state lanes is 128 units).
+    const double launch_units = 2000.0 / 0.54;
+    const double chunk_units = 650.0 / 0.54;
     ScanPlan best{lmin, 1, lmin};
     double best_cost = 1e300;
     for (int lanes = lmin; lanes <= lmax; lanes *= 2) {
-        const double lane_cost = lanes == 1 ? 1.0 : (lanes == 2 ? 1.2 : 2.0);
         const int ch = kTmaWarps * 32 / lanes;
         const long long blocks = static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
         const int cap_full = ctas_per_sm(tma_smem_for<ssm::ScanMode::Full>(io, dstate, lanes));
         for (int k = 1; k <= kmax; ++k) {
-            const double steps = (static_cast<double>(seqlen) / k) * (dstate / 16.0);
-            double cost = pass_time(blocks * k, cap_full, lane_cost * ch * steps);
+            const double steps = static_cast<double>(seqlen) / k;
+            double cost = pass_time(blocks * k, cap_full, step_time(dstate / lanes, lanes, false) * steps);
             int best_agg = lanes;
             if (k > 1) {
                 // The summary pass picks its own lanes (no readout to reduce:
                 // cheaper lane sharing).
                 double agg_cost = 1e300;
                 for (int la = lmin; la <= lmax; la *= 2) {
-                    const double la_cost = la == 1 ? 1.0 : (la == 2 ? 1.1 : 1.7);
                     const int cha = kTmaWarps * 32 / la;
                     const long long blocks_a = static_cast<long long>((dpg + cha - 1) / cha) * ngroups * batch;
                     const int cap_agg = ctas_per_sm(tma_smem_for<ssm::ScanMode::Aggregate>(io, dstate, la));
-                    const double c = pass_time(blocks_a * (k - 1), cap_agg, 0.9 * la_cost * cha * steps);
+                    const double c = pass_time(blocks_a * (k - 1), cap_agg, 0.9 * step_time(dstate / la, la, true) * steps);
                     if (c < agg_cost * 0.999) {
                         agg_cost = c;
                         best_agg = la;
