@@ -16,7 +16,9 @@ that the pages fix, the short causal convolution and its decode step by
 the impulse response and its split and decode identities, the packed
 variable-length scan and the pooled decode step by
 ``tests/test_oracle_varlen_pins.py`` against the separately pinned scan and
-decode step -- and
+decode step, the backward pass by ``tests/test_oracle_bwd_pins.py`` against
+central finite differences of the pinned forward scan and a closed form at
+L = 1 -- and
 ``tests/test_oracle_mutants.py`` checks that the pins catch planted slips.
 """
 from __future__ import annotations
@@ -74,6 +76,8 @@ def _set_conv_types(lib):
     lib.oracle_causal_conv1d.restype = I
     lib.oracle_causal_conv1d_update.argtypes = [P] * 5 + [I] * 4
     lib.oracle_causal_conv1d_update.restype = I
+    lib.oracle_scan_bwd.argtypes = [P] * 20 + [I] * 6
+    lib.oracle_scan_bwd.restype = I
 
 
 class _use_library:
@@ -287,3 +291,44 @@ def state_update_indexed(state_pool, state_indices, u, delta, A, B, C, z=None, D
         raise ValueError(f"oracle_state_update_indexed rejected its arguments (code {rc})")
     return pool, y
 
+
+
+def scan_bwd(u, delta, A, B, C, dy, z=None, Dskip=None, dt_bias=None, h0=None, dh_final=None, *,
+             nthreads=None):
+    """Gradients of the selective scan in fp64, given dy = dLoss/dy [batch,
+    dim, L] and optionally dh_final = dLoss/dh_final [batch, dim, N].
+
+    Returns a dict with du, ddelta, dz (None without z) [batch, dim, L]; dA
+    [dim, N]; dB, dC [batch, G, N, L]; dD, ddt_bias [dim]; dh0 [batch, dim, N]
+    (the gradient with respect to the initial state, zero or not)."""
+    u = _f64(u)
+    if u.ndim != 3:
+        raise ValueError("u must be [batch, dim, L]")
+    batch, dim, L = u.shape
+    delta = _f64(delta, u.shape)
+    z = _f64(z, u.shape)
+    dy = _f64(dy, u.shape)
+    A = _f64(A)
+    if A.ndim != 2 or A.shape[0] != dim:
+        raise ValueError("A must be [dim, N]")
+    N = A.shape[1]
+    B = _f64(B)
+    if B.ndim != 4 or B.shape[0] != batch or B.shape[2:] != (N, L):
+        raise ValueError("B must be [batch, G, N, L]")
+    G = B.shape[1]
+    C = _f64(C, B.shape)
+    Dskip = _f64(Dskip, (dim,))
+    dt_bias = _f64(dt_bias, (dim,))
+    h0 = _f64(h0, (batch, dim, N))
+    dh_final = _f64(dh_final, (batch, dim, N))
+    out = dict(du=np.empty(u.shape), ddelta=np.empty(u.shape), dz=np.empty(u.shape) if z is not None else None,
+               dA=np.empty((dim, N)), dB=np.empty(B.shape), dC=np.empty(B.shape), dD=np.empty(dim),
+               ddt_bias=np.empty(dim), dh0=np.empty((batch, dim, N)))
+    rc = _load().oracle_scan_bwd(_ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
+                                 _ptr(dt_bias), _ptr(h0), _ptr(dy), _ptr(dh_final),
+                                 _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dz"]), _ptr(out["dA"]),
+                                 _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["ddt_bias"]),
+                                 _ptr(out["dh0"]), batch, dim, N, L, G, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_scan_bwd rejected its arguments (code {rc})")
+    return out

@@ -361,3 +361,167 @@ int oracle_state_update_indexed(double *state_pool, const int *state_indices, in
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward pass of the scan: the gradients of a scalar loss with respect to
+ * every input, given its gradient dy with respect to y (and, optionally, dhf
+ * with respect to the final state).
+ *
+ * The pages say that training keeps the states on chip and recomputes them in
+ * the backward pass (intvml.com "DL0170 Mamba Selective SSM vs Attention",
+ * the paragraphs after the list of key points); they print no gradient
+ * formulas.  The reading taken is the plain chain rule through the forward
+ * definition above, written out per channel.  With s_t the ungated output
+ * (sum_n C_t[n] h_t[n] + Dskip u_t), g_t = dy_t * silu(z_t) its gradient,
+ * and lam_t[n] the gradient of the loss with respect to h_t[n]:
+ *
+ *   lam_t[n]   = g_t C_t[n] + Abar_{t+1}[n] lam_{t+1}[n]   (lam_{L-1} gets + dhf[n])
+ *   dz_t       = dy_t * s_t * silu'(z_t),  silu'(z) = sig(z) (1 + z (1 - sig(z)))
+ *   dC_t[n]    = g_t h_t[n]
+ *   dB_t[n]    = lam_t[n] Delta_t u_t
+ *   du_t       = g_t Dskip + Delta_t sum_n lam_t[n] B_t[n]
+ *   dDelta_t   = sum_n lam_t[n] (B_t[n] u_t + A[n] Abar_t[n] h_{t-1}[n])
+ *   ddelta_t   = dDelta_t * sig(delta_t + dt_bias)        (softplus' = sigmoid)
+ *   dA[n]     += lam_t[n] Delta_t Abar_t[n] h_{t-1}[n]
+ *   dDskip    += g_t u_t,   ddt_bias += ddelta_t,   dh0[n] = Abar_0[n] lam_0[n]
+ *
+ * dB, dC sum over the channels of a group, dA, dDskip, ddt_bias over the
+ * batch (and time).  Each channel first runs the forward recurrence keeping
+ * every state, then walks time backwards.
+ * ---------------------------------------------------------------------- */
+
+static double sigmoid(double x) {
+    return x >= 0.0 ? 1.0 / (1.0 + exp(-x)) : exp(x) / (1.0 + exp(x));
+}
+
+typedef struct {
+    const double *u, *delta, *z, *A, *B, *C, *Dskip, *dt_bias, *h0, *dy, *dhf;
+    double *du, *ddelta, *dz, *dh0;
+    double *dA, *dB, *dC, *dDskip, *ddt_bias; /* this worker's private sums */
+    int batch, dim, dstate, seqlen, ngroups;
+    long first, last;
+    int ok;
+} bwd_job;
+
+static void *bwd_worker(void *arg) {
+    bwd_job *J = (bwd_job *)arg;
+    const int N = J->dstate, L = J->seqlen;
+    /* hs[t * N + n] = h_t[n] for t = -1 .. L-1 (row 0 holds h_{-1} = h0) */
+    double *hs = (double *)malloc(sizeof(double) * (size_t)(L + 1) * (size_t)N);
+    double *dts = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double *lam = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!hs || !dts || !lam) { free(hs); free(dts); free(lam); J->ok = 0; return NULL; }
+    for (long i = J->first; i < J->last; i++) {
+        const int b = (int)(i / J->dim), d = (int)(i % J->dim);
+        const int g = d / (J->dim / J->ngroups);
+        const size_t row = ((size_t)b * J->dim + d) * (size_t)L;
+        const size_t bc = ((size_t)b * J->ngroups + g) * (size_t)N * (size_t)L;
+        const size_t st = ((size_t)b * J->dim + d) * (size_t)N;
+        const double *Ad = J->A + (size_t)d * N;
+        const double dskip = J->Dskip ? J->Dskip[d] : 0.0;
+        const double bias = J->dt_bias ? J->dt_bias[d] : 0.0;
+
+        /* forward, keeping every state */
+        for (int n = 0; n < N; n++) hs[n] = J->h0 ? J->h0[st + n] : 0.0;
+        for (int t = 0; t < L; t++) {
+            const double dt = softplus(J->delta[row + t] + bias);
+            dts[t] = dt;
+            for (int n = 0; n < N; n++)
+                hs[(size_t)(t + 1) * N + n] = exp(dt * Ad[n]) * hs[(size_t)t * N + n]
+                                              + dt * J->B[bc + (size_t)n * L + t] * J->u[row + t];
+        }
+
+        /* backward over time */
+        for (int n = 0; n < N; n++) lam[n] = J->dhf ? J->dhf[st + n] : 0.0;  /* carried from t+1 */
+        for (int t = L - 1; t >= 0; t--) {
+            const double ut = J->u[row + t], dt = dts[t];
+            const double *hprev = hs + (size_t)t * N, *hcur = hs + (size_t)(t + 1) * N;
+            double s = dskip * ut;
+            for (int n = 0; n < N; n++) s += J->C[bc + (size_t)n * L + t] * hcur[n];
+            double gt = J->dy[row + t];
+            if (J->z) {
+                const double zt = J->z[row + t], sg = sigmoid(zt);
+                J->dz[row + t] = J->dy[row + t] * s * sg * (1.0 + zt * (1.0 - sg));
+                gt *= silu(zt);
+            }
+            double dsum_b = 0.0, ddelta_t = 0.0;
+            for (int n = 0; n < N; n++) {
+                const size_t k = bc + (size_t)n * L + t;
+                const double abar = exp(dt * Ad[n]);
+                const double l = gt * J->C[k] + lam[n];     /* lam_t[n] */
+                J->dC[k] += gt * hcur[n];
+                J->dB[k] += l * dt * ut;
+                dsum_b += l * J->B[k];
+                ddelta_t += l * (J->B[k] * ut + Ad[n] * abar * hprev[n]);
+                J->dA[(size_t)d * N + n] += l * dt * abar * hprev[n];
+                lam[n] = abar * l;                           /* passes to t-1 */
+            }
+            J->du[row + t] = gt * dskip + dt * dsum_b;
+            const double dd = ddelta_t * sigmoid(J->delta[row + t] + bias);
+            J->ddelta[row + t] = dd;
+            J->dDskip[d] += gt * ut;
+            J->ddt_bias[d] += dd;
+        }
+        if (J->dh0)
+            for (int n = 0; n < N; n++) J->dh0[st + n] = lam[n];
+    }
+    free(hs); free(dts); free(lam);
+    J->ok = 1;
+    return NULL;
+}
+
+/* Gradients of the scan.  Inputs as oracle_scan plus dy [batch, dim, L] and
+ * dhf [batch, dim, N] (may be NULL: zero).  Outputs (all overwritten): du,
+ * ddelta [batch, dim, L]; dz [batch, dim, L] (ignored when z is NULL); dA
+ * [dim, N]; dB, dC [batch, G, N, L]; dDskip, ddt_bias [dim]; dh0 [batch, dim,
+ * N] (may be NULL). */
+int oracle_scan_bwd(const double *u, const double *delta, const double *z,
+                    const double *A, const double *B, const double *C,
+                    const double *Dskip, const double *dt_bias, const double *h0,
+                    const double *dy, const double *dhf,
+                    double *du, double *ddelta, double *dz, double *dA, double *dB, double *dC,
+                    double *dDskip, double *ddt_bias, double *dh0,
+                    int batch, int dim, int dstate, int seqlen, int ngroups, int nthreads) {
+    if (!check_dims(batch, dim, dstate, seqlen, ngroups)) return ORACLE_BAD_ARG;
+    if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC || !dDskip || !ddt_bias)
+        return ORACLE_BAD_ARG;
+    if (z && !dz) return ORACLE_BAD_ARG;
+    const long total = (long)batch * dim;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > total) nthreads = (int)total;
+    const size_t nA = (size_t)dim * dstate, nBC = (size_t)batch * ngroups * dstate * (size_t)seqlen;
+    const size_t per = nA + 2 * nBC + 2 * (size_t)dim; /* private sums of one worker */
+    bwd_job *jobs = (bwd_job *)malloc(sizeof(bwd_job) * (size_t)nthreads);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    double *sums = (double *)calloc((size_t)nthreads * per, sizeof(double));
+    if (!jobs || !tid || !sums) { free(jobs); free(tid); free(sums); return ORACLE_BAD_ARG; }
+    for (int k = 0; k < nthreads; k++) {
+        double *p = sums + (size_t)k * per;
+        bwd_job J = {u, delta, z, A, B, C, Dskip, dt_bias, h0, dy, dhf,
+                     du, ddelta, dz, dh0,
+                     p, p + nA, p + nA + nBC, p + nA + 2 * nBC, p + nA + 2 * nBC + dim,
+                     batch, dim, dstate, seqlen, ngroups,
+                     total * k / nthreads, total * (k + 1) / nthreads, 0};
+        jobs[k] = J;
+    }
+    if (nthreads == 1) {
+        bwd_worker(&jobs[0]);
+    } else {
+        for (int k = 0; k < nthreads; k++) pthread_create(&tid[k], NULL, bwd_worker, &jobs[k]);
+        for (int k = 0; k < nthreads; k++) pthread_join(tid[k], NULL);
+    }
+    int ok = 1;
+    for (int k = 0; k < nthreads; k++) ok &= jobs[k].ok;
+    /* add up the workers' sums */
+    for (size_t i = 0; i < nA; i++) dA[i] = 0.0;
+    for (size_t i = 0; i < nBC; i++) { dB[i] = 0.0; dC[i] = 0.0; }
+    for (int i = 0; i < dim; i++) { dDskip[i] = 0.0; ddt_bias[i] = 0.0; }
+    for (int k = 0; k < nthreads; k++) {
+        const bwd_job *J = &jobs[k];
+        for (size_t i = 0; i < nA; i++) dA[i] += J->dA[i];
+        for (size_t i = 0; i < nBC; i++) { dB[i] += J->dB[i]; dC[i] += J->dC[i]; }
+        for (int i = 0; i < dim; i++) { dDskip[i] += J->dDskip[i]; ddt_bias[i] += J->ddt_bias[i]; }
+    }
+    free(jobs); free(tid); free(sums);
+    return ok ? ORACLE_OK : ORACLE_BAD_ARG;
+}

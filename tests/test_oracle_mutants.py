@@ -7,6 +7,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_bwd_pins as bwd_pins
 import test_oracle_conv_pins as conv_pins
 import test_oracle_varlen_pins as varlen_pins
 import test_oracle_pins as pins
@@ -54,6 +55,20 @@ MUTANTS = {
                                  "const size_t bc = (size_t)(d % ngroups) * (size_t)N * (size_t)T;"),
     "pooled_decode_reads_batch_row": ("double *h = &state_pool[((size_t)slot * dim + d) * N];",
                                       "double *h = &state_pool[((size_t)b * dim + d) * N];"),
+    # the backward pass
+    "bwd_dB_without_step": ("J->dB[k] += l * dt * ut;", "J->dB[k] += l * ut;"),
+    "bwd_adjoint_not_decayed": ("lam[n] = abar * l;", "lam[n] = l;"),
+    "bwd_dDelta_drops_decay_term": ("ddelta_t += l * (J->B[k] * ut + Ad[n] * abar * hprev[n]);",
+                                    "ddelta_t += l * J->B[k] * ut;"),
+    "bwd_dC_uses_previous_state": ("J->dC[k] += gt * hcur[n];", "J->dC[k] += gt * hprev[n];"),
+    "bwd_dz_drops_silu_derivative_term": ("sg * (1.0 + zt * (1.0 - sg))", "sg"),
+    "bwd_softplus_derivative_without_bias": ("ddelta_t * sigmoid(J->delta[row + t] + bias)",
+                                             "ddelta_t * sigmoid(J->delta[row + t])"),
+    "bwd_du_skip_dropped": ("J->du[row + t] = gt * dskip + dt * dsum_b;", "J->du[row + t] = dt * dsum_b;"),
+    "bwd_dA_uses_current_state": ("J->dA[(size_t)d * N + n] += l * dt * abar * hprev[n];",
+                                  "J->dA[(size_t)d * N + n] += l * dt * abar * hcur[n];"),
+    "bwd_dh_final_ignored": ("lam[n] = J->dhf ? J->dhf[st + n] : 0.0;", "lam[n] = 0.0;"),
+    "bwd_worker_sums_overwritten": ("dA[i] += J->dA[i];", "dA[i] = J->dA[i];"),
 }
 
 PIN_TESTS = [
@@ -76,6 +91,10 @@ PIN_TESTS = [
     lambda: conv_pins.test_conv_width_one_is_pointwise(),
     lambda: varlen_pins.test_varlen_equals_each_sequence_alone(),
     lambda: varlen_pins.test_pooled_decode_equals_gathered_decode(),
+    lambda: bwd_pins.test_gradients_match_finite_differences(True, True, 2),
+    lambda: bwd_pins.test_single_step_closed_form(True),
+    lambda: bwd_pins.test_empty_sequence_passes_dh_final_to_h0(),
+    lambda: bwd_pins.test_threads_do_not_change_sums(),
 ]
 
 
