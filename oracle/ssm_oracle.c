@@ -424,7 +424,8 @@ static void *bwd_worker(void *arg) {
         /* forward, keeping every state */
         for (int n = 0; n < N; n++) hs[n] = J->h0 ? J->h0[st + n] : 0.0;
         for (int t = 0; t < L; t++) {
-            const double dt = softplus(J->delta[row + t] + bias);
+            const double x = J->delta[row + t] + bias;
+            const double dt = softplus(x);
             dts[t] = dt;
             for (int n = 0; n < N; n++)
                 hs[(size_t)(t + 1) * N + n] = exp(dt * Ad[n]) * hs[(size_t)t * N + n]
