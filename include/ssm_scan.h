@@ -44,7 +44,7 @@
  * - stream is a cudaStream_t (NULL = legacy default stream).  Every call is
  *   asynchronous on that stream; argument errors are returned before anything
  *   is enqueued.
- * - Supported dstate: 4, 8, 16 (others return SSM_ERR_UNSUPPORTED).
+ * - Supported dstate: 4, 8, 16, 32, 64 (others return SSM_ERR_UNSUPPORTED).
  * - batch == 0 is an empty problem: the call returns SSM_OK without touching
  *   any pointer.  seqlen == 0 is accepted: nothing is read or written except
  *   h_final (which then equals h0, or zeros).
@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = 1,        /* null required pointer, bad size, dim % ngroups != 0 */
-    SSM_ERR_UNSUPPORTED = 2,        /* dstate not in {4, 8, 16}, unknown io type */
+    SSM_ERR_UNSUPPORTED = 2,        /* dstate not in {4, 8, 16, 32, 64}, unknown io type */
     SSM_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
     SSM_ERR_WORKSPACE_TOO_SMALL = 4,/* workspace_bytes below the size query's answer */
     SSM_ERR_TIMEOUT = 5,            /* a bounded device-side wait gave up (see ssm_workspace_status) */
@@ -334,6 +334,50 @@ ssm_status_t ssm_causal_conv1d_fwd(const void *x, const float *w, const float *b
 ssm_status_t ssm_causal_conv1d_update(void *conv_state, const void *x, const float *w, const float *bias,
                                       void *out, int batch, int dim, int width, int silu, ssm_dtype_t io,
                                       void *stream);
+
+/*
+ * ssm_scan_bwd -- gradients of the selective scan (training).  The pages keep
+ * the states on chip and recompute them in the backward pass rather than
+ * storing them (intvml.com "DL0170 Mamba Selective SSM vs Attention", the
+ * paragraphs after the key points); the gradients are the chain rule through
+ * the forward definition of ssm_scan_fwd_chunked.  With s_t the ungated
+ * output, g_t = dy_t silu(z_t) and lam_t[n] = dLoss/dh_t[n]
+ * (= g_t C_t[n] + Abar_{t+1}[n] lam_{t+1}[n], plus dh_final at the last step):
+ *   du_t = g_t D + Delta_t sum_n lam_t[n] B_t[n]
+ *   ddelta_t = sigmoid(delta_t + dt_bias) sum_n lam_t[n] (B_t[n] u_t + A[n] Abar_t[n] h_{t-1}[n])
+ *   dz_t = dy_t s_t silu'(z_t);  dB_t[n] = sum over the group's channels of lam_t[n] Delta_t u_t;
+ *   dC_t[n] = sum over the group's channels of g_t h_t[n];
+ *   dA[n] = sum over batch and time of lam_t[n] Delta_t Abar_t[n] h_{t-1}[n];
+ *   dDskip = sum g_t u_t;  ddt_bias = sum ddelta_t;  dh0[n] = Abar_0[n] lam_0[n].
+ * Inputs: the forward call's inputs (u, delta, z, A, B, C, Dskip, dt_bias, h0
+ *   as in ssm_scan_fwd_chunked; z, Dskip, dt_bias, h0 may be NULL), plus
+ *   dy         : [batch, dim, seqlen] io type, dLoss/dy
+ *   dh_final   : [batch, dim, dstate] fp32, dLoss/dh_final, or NULL (zero)
+ * Outputs (all overwritten, none may alias an input):
+ *   du, ddelta : [batch, dim, seqlen] io type
+ *   dz         : [batch, dim, seqlen] io type; required when z is given, else ignored
+ *   dA         : [dim, dstate] fp32
+ *   dB, dC     : [batch, ngroups, dstate, seqlen] fp32 (sums over channels)
+ *   dDskip     : [dim] fp32; required when Dskip is given, may be NULL otherwise
+ *   ddt_bias   : [dim] fp32; required when dt_bias is given, may be NULL otherwise
+ *   dh0        : [batch, dim, dstate] fp32, or NULL (not wanted)
+ * workspace: device memory of at least ssm_scan_bwd_workspace_size() bytes
+ *   (the chunk summaries; 12 * dstate bytes per channel and chunk of 128 steps,
+ *   64 at dstate 64); may be NULL when that size is 0.
+ * The sums over channels and time are accumulated with fp32 atomic adds, so
+ * dA, dB, dC, dDskip and ddt_bias may differ in the last bits between runs.
+ * Errors: SSM_ERR_INVALID_ARG (bad size, missing required pointer, an output
+ * aliasing an input), SSM_ERR_UNSUPPORTED, SSM_ERR_MISALIGNED,
+ * SSM_ERR_WORKSPACE_TOO_SMALL, SSM_ERR_CUDA.
+ */
+size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io);
+
+ssm_status_t ssm_scan_bwd(const void *u, const void *delta, const void *z, const float *A, const void *B,
+                          const void *C, const float *Dskip, const float *dt_bias, const float *h0,
+                          const void *dy, const float *dh_final, void *du, void *ddelta, void *dz, float *dA,
+                          float *dB, float *dC, float *dDskip, float *ddt_bias, float *dh0, int batch, int dim,
+                          int dstate, int seqlen, int ngroups, ssm_dtype_t io, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

@@ -18,6 +18,7 @@
 
 #include "../../include/ssm_scan.h"
 #include "conv1d.cuh"
+#include "scan_bwd.cuh"
 #include "scan_fwd.cuh"
 #include "decode_tma.cuh"
 #include "scan_tma.cuh"
@@ -712,9 +713,143 @@ cudaError_t launch_conv_update_t(void* state, const void* x, const float* w, con
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Backward pass
+// ---------------------------------------------------------------------------
+
+int bwd_chunk_steps_for(int dstate) { return ssm::bwd_chunk_steps(dstate); }
+
+int bwd_nchunks(int seqlen, int dstate) {
+    const int cs = bwd_chunk_steps_for(dstate);
+    return std::max(1, (seqlen + cs - 1) / cs);
+}
+
+size_t bwd_workspace_bytes(int batch, int dim, int dstate, int seqlen) {
+    const int k = bwd_nchunks(seqlen, dstate);
+    if (k <= 1 || batch <= 0) return 0;
+    // fagg [k][BD][2][N] and bagg [k][BD][N], fp32
+    return static_cast<size_t>(k) * static_cast<size_t>(batch) * static_cast<size_t>(dim) *
+           static_cast<size_t>(dstate) * 3u * sizeof(float);
+}
+
+template <typename T, int N>
+cudaError_t launch_bwd_n(const ssm::BwdParams& p, cudaStream_t st) {
+    constexpr bool kAcc = sizeof(T) == 4;
+    const dim3 grid(static_cast<unsigned>(static_cast<long long>(p.blocks_per_group) * p.batch * p.ngroups),
+                    static_cast<unsigned>(p.nchunks), 1);
+    const dim3 block(ssm::kBwdWarps * 32);
+    if (p.nchunks > 1) {
+        ssm::scan_bwd_summary_kernel<T, N, kAcc><<<dim3(grid.x, grid.y, 2), block, 0, st>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const long long BD = static_cast<long long>(p.batch) * p.dim;
+        const long long n = BD * N;
+        ssm::scan_bwd_carry_kernel<N><<<dim3(static_cast<unsigned>((n + 255) / 256), 2), 256, 0, st>>>(
+            p.fagg, p.bagg, p.h0, p.dhf, BD, p.nchunks);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    ssm::scan_bwd_kernel<T, N, kAcc><<<grid, block, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_t(const ssm::BwdParams& p, int dstate, cudaStream_t st) {
+    switch (dstate) {
+        case 4: return launch_bwd_n<T, 4>(p, st);
+        case 8: return launch_bwd_n<T, 8>(p, st);
+        case 32: return launch_bwd_n<T, 32>(p, st);
+        case 64: return launch_bwd_n<T, 64>(p, st);
+        default: return launch_bwd_n<T, 16>(p, st);
+    }
+}
+
+// Copies dh_final (or zeros) into dh0: the gradient of an empty sequence.
+__global__ void copy_or_zero_kernel(const float* __restrict__ src, float* __restrict__ dst, long long n) {
+    const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (i < n) dst[i] = src ? src[i] : 0.f;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io) {
+    (void)ngroups;
+    (void)io;
+    if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return 0;
+    return bwd_workspace_bytes(batch, dim, dstate, seqlen);
+}
+
+ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const void* z, const float* A, const void* B,
+                          const void* C, const float* Dskip, const float* dt_bias, const float* h0,
+                          const void* dy, const float* dh_final, void* du, void* ddelta, void* dz, float* dA,
+                          float* dB, float* dC, float* dDskip, float* ddt_bias, float* dh0, int batch, int dim,
+                          int dstate, int seqlen, int ngroups, ssm_dtype_t io, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || ngroups <= 0) return SSM_ERR_INVALID_ARG;
+    if (dim % ngroups != 0) return SSM_ERR_INVALID_ARG;
+    if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+    if (!supported_dstate(dstate)) return SSM_ERR_UNSUPPORTED;
+    if (batch == 0) return SSM_OK;
+    if (!A || !dA) return SSM_ERR_INVALID_ARG;
+    if (seqlen > 0 && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)) return SSM_ERR_INVALID_ARG;
+    if (z && seqlen > 0 && !dz) return SSM_ERR_INVALID_ARG;
+    if ((Dskip && !dDskip) || (dt_bias && !ddt_bias)) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {u, delta, z, A, B, C, Dskip, dt_bias, h0, dy, dh_final, du, ddelta, dz, dA, dB, dC,
+                          dDskip, ddt_bias, dh0, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SSM_ERR_MISALIGNED;
+    const void* outs[] = {du, ddelta, dz, dB, dC};
+    const void* ins[] = {u, delta, z, B, C, dy};
+    for (const void* o : outs)
+        for (const void* i : ins)
+            if (o && o == i) return SSM_ERR_INVALID_ARG;
+    const size_t need = ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen, ngroups, io);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return SSM_ERR_WORKSPACE_TOO_SMALL;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int es = io == SSM_F32 ? 4 : 2;
+    const size_t nBC = static_cast<size_t>(batch) * ngroups * dstate * static_cast<size_t>(seqlen);
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * static_cast<size_t>(dim) * dstate, st);
+    if (e == cudaSuccess && dDskip) e = cudaMemsetAsync(dDskip, 0, sizeof(float) * static_cast<size_t>(dim), st);
+    if (e == cudaSuccess && ddt_bias) e = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * static_cast<size_t>(dim), st);
+    if (e == cudaSuccess && nBC > 0) e = cudaMemsetAsync(dB, 0, sizeof(float) * nBC, st);
+    if (e == cudaSuccess && nBC > 0) e = cudaMemsetAsync(dC, 0, sizeof(float) * nBC, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (seqlen == 0) {
+        if (dh0) {
+            const long long n = static_cast<long long>(batch) * dim * dstate;
+            copy_or_zero_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(dh_final, dh0, n);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        return SSM_OK;
+    }
+
+    ssm::BwdParams p{};
+    p.u = u; p.delta = delta; p.z = z; p.dy = dy; p.B = B; p.C = C;
+    p.A = A; p.D = Dskip; p.dt_bias = dt_bias; p.h0 = h0; p.dhf = dh_final;
+    p.du = du; p.ddelta = ddelta; p.dz = dz;
+    p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dDskip; p.ddt_bias = ddt_bias; p.dh0 = dh0;
+    p.batch = batch; p.dim = dim; p.seqlen = seqlen; p.ngroups = ngroups;
+    p.dim_per_group = dim / ngroups;
+    const int ch = ssm::kBwdWarps * 32 / (dstate / ssm::kBwdStates);
+    p.blocks_per_group = (p.dim_per_group + ch - 1) / ch;
+    p.nchunks = bwd_nchunks(seqlen, dstate);
+    p.vec_ok = (static_cast<long long>(seqlen) * es) % 16 == 0;
+    if (p.nchunks > 1) {
+        const size_t BDN = static_cast<size_t>(batch) * dim * dstate;
+        p.fagg = static_cast<float*>(workspace);
+        p.bagg = p.fagg + static_cast<size_t>(p.nchunks) * BDN * 2u;
+    }
+    const long long grid_x = static_cast<long long>(p.blocks_per_group) * batch * ngroups;
+    if (grid_x > 0x7fffffffLL || p.nchunks > 65535) return SSM_ERR_INVALID_ARG;
+    e = io == SSM_F32 ? launch_bwd_t<float>(p, dstate, st) : launch_bwd_t<__nv_bfloat16>(p, dstate, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return SSM_OK;
+}
+
 
 ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io, int chunked,
                            int* lanes, int* chunks, int* kernels, int* staged) {

@@ -71,6 +71,10 @@ def _load() -> ctypes.CDLL:
     L.ssm_causal_conv1d_fwd.restype = I
     L.ssm_causal_conv1d_update.argtypes = [P] * 5 + [I] * 5 + [P]
     L.ssm_causal_conv1d_update.restype = I
+    L.ssm_scan_bwd_workspace_size.argtypes = [I] * 6
+    L.ssm_scan_bwd_workspace_size.restype = Z
+    L.ssm_scan_bwd.argtypes = [P] * 20 + [I] * 6 + [P, Z, P]
+    L.ssm_scan_bwd.restype = I
     return L
 
 
@@ -334,3 +338,50 @@ def scan_fwd_varlen(u, delta, A, B, C, cu_seqlens, z=None, D=None, dt_bias=None,
         raise SsmError(st, "ssm_scan_fwd_varlen")
     return (y, hf) if return_final_state else y
 
+
+
+def bwd_workspace_size(batch, dim, dstate, seqlen, ngroups, dtype) -> int:
+    return int(lib.ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen, ngroups, _io_code(dtype)))
+
+
+def scan_bwd(u, delta, A, B, C, dy, z=None, D=None, dt_bias=None, h0=None, dh_final=None, *,
+             want_dh0=True, out=None, workspace=None) -> dict:
+    """Gradients of the selective scan given dy = dLoss/dy [batch, dim, L]
+    (and dh_final = dLoss/dh_final [batch, dim, N], or None).
+
+    Returns a dict: du, ddelta, dz (None without z) [batch, dim, L] in the
+    I/O type; dA [dim, N], dB and dC [batch, G, N, L], dD and ddt_bias [dim]
+    (None when D / dt_bias is None), dh0 [batch, dim, N] (None unless
+    want_dh0) in fp32.  ``out`` may hold preallocated tensors under the same
+    keys."""
+    batch, dim, N, L, G = _validate_scan(u, delta, z, A, B, C, D, dt_bias)
+    dev, io = u.device, u.dtype
+    _check(dy, "dy", (batch, dim, L), io, dev)
+    _check(h0, "h0", (batch, dim, N), torch.float32, dev)
+    _check(dh_final, "dh_final", (batch, dim, N), torch.float32, dev)
+    o = dict(out or {})
+    f32 = torch.float32
+    specs = dict(du=((batch, dim, L), io, True), ddelta=((batch, dim, L), io, True),
+                 dz=((batch, dim, L), io, z is not None), dA=((dim, N), f32, True),
+                 dB=((batch, G, N, L), f32, True), dC=((batch, G, N, L), f32, True),
+                 dD=((dim,), f32, D is not None), ddt_bias=((dim,), f32, dt_bias is not None),
+                 dh0=((batch, dim, N), f32, bool(want_dh0)))
+    for k, (shape, dt, wanted) in specs.items():
+        if not wanted:
+            o[k] = None
+            continue
+        if o.get(k) is None:
+            o[k] = torch.empty(shape, dtype=dt, device=dev)
+        _check(o[k], k, shape, dt, dev)
+    need = bwd_workspace_size(batch, dim, N, L, G, io)
+    ws = alloc_workspace(need, dev) if workspace is None else workspace
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_bwd(_ptr(u), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                              _ptr(h0), _ptr(dy), _ptr(dh_final), _ptr(o["du"]), _ptr(o["ddelta"]), _ptr(o["dz"]),
+                              _ptr(o["dA"]), _ptr(o["dB"]), _ptr(o["dC"]), _ptr(o["dD"]), _ptr(o["ddt_bias"]),
+                              _ptr(o["dh0"]), batch, dim, N, L, G, _io_code(io), _ptr(ws), ws_bytes,
+                              _stream_handle(dev))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_bwd")
+    return o

@@ -155,3 +155,36 @@ def test_varlen_and_pooled_argument_errors(lib):
     assert pooled(idx=None, nslots=3) == 1      # without indices the pool is the batch
     assert pooled(idx=P, nslots=0) == 1
     assert pooled(idx=MIS, nslots=4) == 3
+
+
+def test_bwd_argument_errors(lib):
+    """Argument checks of the backward pass (fake pointers; every call below
+    fails its checks and returns before anything is enqueued)."""
+    Q = 0x40000
+
+    def bwd(u=P, z=None, D=None, bias=None, dy=Q, du=Q + 0x100, dd=Q + 0x200, dz=None, dA=Q + 0x300, dB=Q + 0x400,
+            dC=Q + 0x500, dD=None, db=None, dh0=None, ws=None, ws_bytes=0, batch=1, dim=4, N=16, L=8, G=1, io=1):
+        return lib.ssm_scan_bwd(u, P, z, P, P, P, D, bias, None, dy, None, du, dd, dz, dA, dB, dC, dD, db, dh0,
+                                batch, dim, N, L, G, io, ws, ws_bytes, None)
+    assert bwd(dy=None) == 1
+    assert bwd(du=None) == 1
+    assert bwd(dB=None) == 1
+    assert bwd(dA=None) == 1
+    assert bwd(z=P + 0x600, dz=None) == 1          # a gated forward needs dz
+    assert bwd(D=P + 0x700, dD=None) == 1          # D given: dD required
+    assert bwd(bias=P + 0x800, db=None) == 1       # dt_bias given: ddt_bias required
+    assert bwd(du=P) == 1                          # du aliases u
+    assert bwd(dim=6, G=4) == 1
+    assert bwd(N=12) == 2
+    assert bwd(N=128) == 2
+    assert bwd(io=9) == 2
+    assert bwd(dy=MIS) == 3
+    assert bwd(dh0=MIS) == 3
+    # 300 steps are three chunks: summaries need a workspace
+    need = lib.ssm_scan_bwd_workspace_size(1, 4, 16, 300, 1, 1)
+    assert need == 3 * 4 * 16 * 3 * 4
+    assert bwd(L=300) == 4
+    assert bwd(L=300, ws=Q + 0x900, ws_bytes=need - 16) == 4
+    assert lib.ssm_scan_bwd_workspace_size(1, 4, 16, 128, 1, 1) == 0   # one chunk: no workspace
+    assert lib.ssm_scan_bwd_workspace_size(2, 4, 64, 129, 1, 1) == 3 * 2 * 4 * 64 * 3 * 4
+    assert bwd(batch=0, u=None, dy=None, du=None, dd=None, dA=None, dB=None, dC=None) == 0  # empty problem
