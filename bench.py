@@ -516,6 +516,40 @@ def bench_varlen(ssm, I, torch, peaks):
     return res
 
 
+def bench_bwd(ssm, I, torch, peaks, names=("scan_bf16_b2_d1536_l2048", "scan_bf16_b8_d2048_l4096")):
+    """Backward pass (every gradient, no final-state gradient) on the scan
+    shapes: device time per call over rotating inputs (> 3x L2)."""
+    dev = torch.device("cuda")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    for name in names:
+        w = I.WORKLOADS[name]
+        b, d, n, L, G = w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"]
+        nbytes = I.compulsory_bytes_bwd(b, d, n, L, G, w["io"])
+        nsets = n_rotating_sets(nbytes, l2)
+        xs = [I.make_scan_inputs(b, d, n, L, G, io=w["io"], recipe=w["recipe"], seed=s, device=dev)
+              for s in range(nsets)]
+        dys = [I.make_scan_inputs(b, d, n, L, G, io=w["io"], recipe=w["recipe"], seed=100 + s, device=dev).u
+               for s in range(nsets)]
+        outs = [None] * nsets
+        ws = ssm.alloc_workspace(ssm.bwd_workspace_size(b, d, n, L, G, xs[0].u.dtype), dev)
+
+        def launch(i):
+            x = xs[i]
+            outs[i] = ssm.scan_bwd(x.u, x.delta, x.A, x.B, x.C, dys[i], z=x.z, D=x.D, dt_bias=x.dt_bias,
+                                   out=outs[i], workspace=ws, want_dh0=False)
+
+        for i in range(nsets):
+            launch(i)  # allocates the outputs outside the captured graph
+        ms = bench_graph(torch, launch, nsets, reps=max(3, 40 // nsets))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res["scan_bwd_" + name[len("scan_"):]] = dict(
+            GBps=round(gbs, 1), us_per_launch=round(ms * 1e3, 2), frac_of_hbm_measured=round(gbs / peaks["hbm_gbs"], 4),
+            Gupd_per_s=round(b * d * n * L / (ms * 1e-3) / 1e9, 1))
+        del xs, dys, outs, ws
+    return res
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -591,6 +625,7 @@ def run_ours(args):
                                plan=rx["plan"])
         extra.update(bench_conv(ssm, I, torch, peaks))
         extra.update(bench_varlen(ssm, I, torch, peaks))
+        extra.update(bench_bwd(ssm, I, torch, peaks))
 
     base = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -727,6 +762,19 @@ def run_profile_case(args):
         for _ in range(args.warmup + args.steps):
             ssm.scan_fwd_varlen(x["u"], x["delta"], x["A"], x["B"], x["C"], x["cu_seqlens"], z=x["z"], D=x["D"],
                                 dt_bias=x["dt_bias"], h0=x["h0"], return_final_state=True)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
+        return
+    if args.profile.startswith("scan_bwd_"):
+        # scan_bwd_<scan workload>: the backward pass on that shape.
+        w = I.WORKLOADS["scan_" + args.profile[len("scan_bwd_"):]]
+        x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                               recipe=w["recipe"], device=dev)
+        dy = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                                recipe=w["recipe"], seed=1, device=dev).u
+        out = None
+        for _ in range(args.warmup + args.steps):
+            out = ssm.scan_bwd(x.u, x.delta, x.A, x.B, x.C, dy, z=x.z, D=x.D, dt_bias=x.dt_bias, out=out)
         torch.cuda.synchronize(dev)
         print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
         return

@@ -227,6 +227,15 @@ def compulsory_bytes_scan(batch, dim, dstate, seqlen, ngroups, io) -> int:
     return 4 * batch * dim * seqlen * s + 2 * batch * ngroups * dstate * seqlen * s
 
 
+def compulsory_bytes_bwd(batch, dim, dstate, seqlen, ngroups, io) -> int:
+    """Backward pass: reads u, delta, z, dy ([batch, dim, L] each) and B, C
+    ([batch, G, N, L] each); writes du, ddelta, dz in the I/O type and dB, dC
+    in fp32."""
+    s = 4 if io == "f32" else 2
+    act, bc = batch * dim * seqlen, batch * ngroups * dstate * seqlen
+    return 7 * act * s + 2 * bc * s + 2 * bc * 4
+
+
 def compulsory_bytes_decode(batch, dim, dstate) -> int:
     """The fp32 state read plus written once per token."""
     return 2 * batch * dim * dstate * 4
