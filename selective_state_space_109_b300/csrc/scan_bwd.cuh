@@ -41,6 +41,7 @@
 #pragma once
 
 #include "ssm_device.cuh"
+#include "tma.cuh"
 
 namespace ssm {
 
@@ -77,29 +78,64 @@ __device__ __forceinline__ float sigmoid_f(float v) {
     }
 }
 
-// kBwdTT consecutive elements of a row starting at p (valid = elements in
-// range; the rest read as zero); cached loads (the rows are read twice).
+// Asynchronous 16-byte global -> shared copies (L1 bypassed).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int K>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory"); }
+
 template <typename T>
-__device__ __forceinline__ void bwd_load_steps(const T* p, int valid, bool vec_ok, float (&f)[kBwdTT]) {
+__device__ __forceinline__ float bwd_to_f(T v) {
+    if constexpr (sizeof(T) == 4) return v;
+    else return __bfloat162float(v);
+}
+template <typename T>
+__device__ __forceinline__ T bwd_zero() {
+    if constexpr (sizeof(T) == 4) return 0.f;
+    else return __float2bfloat16_rn(0.f);
+}
+
+// Stages kBwdTT elements of a row (from src, `valid` of them in range) into
+// shared memory: cp.async when the whole segment is in range and aligned,
+// element copies (zero past the end) otherwise.
+template <typename T>
+__device__ __forceinline__ void bwd_stage_row(T* dst, const T* src, int valid, bool vec) {
     constexpr int VP = 16 / static_cast<int>(sizeof(T));
+    if (vec && valid >= kBwdTT) {
 #pragma unroll
-    for (int q = 0; q < kBwdTT / VP; ++q) {
-        Packet<T, VP> pk;
-        const int v = valid - q * VP;
-        if (vec_ok && v >= VP) {
-            pk.load_cached(p + q * VP);
-        } else {
-            float g[VP];
+        for (int q = 0; q < kBwdTT / VP; ++q) cp_async16(dst + q * VP, src + q * VP);
+    } else {
 #pragma unroll
-            for (int k = 0; k < VP; ++k) g[k] = k < v ? Elem<T>::load(p + q * VP + k) : 0.f;
-            pk.from_float(g);
-        }
-        float g[VP];
-        pk.to_float(g);
-#pragma unroll
-        for (int k = 0; k < VP; ++k) f[q * VP + k] = g[k];
+        for (int k = 0; k < kBwdTT; ++k) dst[k] = k < valid ? src[k] : bwd_zero<T>();
     }
 }
+
+// softplus(v) and sigmoid(v) from one exp(-|v|).
+template <bool ACCURATE>
+__device__ __forceinline__ void softplus_sigmoid(float v, float& sp, float& sg) {
+    if (ACCURATE) {
+        const float w = expf(-fabsf(v));
+        sp = fmaxf(v, 0.f) + log1pf(w);
+        const float r = 1.f / (1.f + w);
+        sg = v >= 0.f ? r : w * r;
+    } else {
+        sp = softplus<false>(v);
+        sg = sigmoid_f<false>(v);
+    }
+}
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+template <bool ACCURATE>
+__device__ __forceinline__ float2 decay2(float2 x) {
+    return make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+}
+
+// Tensors of the activation rows staged per tile, in this order.
+enum BwdAct { kU = 0, kDelta = 1, kZ = 2, kDy = 3 };
 
 // Butterfly all-reduce over the LN lanes of a channel.
 template <int LN>
@@ -191,126 +227,174 @@ __device__ __forceinline__ BwdLane bwd_lane(const BwdParams& p) {
     return l;
 }
 
-// Loads the B (and/or C) rows of the tile at t0 and widens them into
-// bcf[t][pair slot] = (B_2q, B_2q+1, C_2q, C_2q+1); pair q of sub-lane j sits
-// at slot (q % P2) * LN + q / P2 so that a channel's lanes read adjacent
-// entries.  Called by every thread; synchronises before and after.
-template <typename T, int N>
-__device__ __forceinline__ void bwd_stage_bc(const BwdParams& p, int bg, int t0, bool withB, bool withC,
-                                             float4 (*bcf)[BwdShape<N>::NQP]) {
-    using Sh = BwdShape<N>;
-    __syncthreads();
-    const long long base = static_cast<long long>(bg) * N * p.seqlen + t0;
-    for (int item = threadIdx.x; item < 2 * N; item += kBwdWarps * 32) {
-        const int isC = item / N;
-        const int n = item % N;
-        if ((isC && !withC) || (!isC && !withB)) continue;
-        const T* src = static_cast<const T*>(isC ? p.C : p.B) + base + static_cast<long long>(n) * p.seqlen;
-        float f[kBwdTT];
-        bwd_load_steps<T>(src, p.seqlen - t0, p.vec_ok != 0, f);
-        const int q = n >> 1;
-        const int slot = (q % Sh::P2) * Sh::LN + q / Sh::P2;
-        float* dst = reinterpret_cast<float*>(&bcf[0][slot]) + isC * 2 + (n & 1);
-#pragma unroll
-        for (int t = 0; t < kBwdTT; ++t) dst[t * Sh::NQP * 4] = f[t];
-    }
-    __syncthreads();
-}
-
 // ---------------------------------------------------------------------------
 // 1. Chunk summaries.  blockIdx.z = 0: forward (P_c, E_c); 1: backward M_c.
+// Needs no exchange between lanes, so a lane holds up to 16 states (one lane
+// per channel up to N = 16).  The per-step scalars (Delta, Delta u or the
+// gate gradient g) are computed once per (channel, step) into shared memory.
 // ---------------------------------------------------------------------------
+template <int N>
+struct BwdSumShape {
+    static constexpr int S = N < 16 ? N : 16;   // states per lane
+    static constexpr int LN = N / S;            // lanes per channel
+    static constexpr int CH = kBwdWarps * 32 / LN;
+    static constexpr int P = S / 2;             // state pairs per lane
+    static constexpr int NQP = N / 2 + 1;
+};
+
 template <typename T, int N, bool ACCURATE>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 scan_bwd_summary_kernel(const BwdParams p) {
-    using Sh = BwdShape<N>;
-    constexpr int S = Sh::S;
-    constexpr int TT = kBwdTT;
-    __shared__ __align__(16) float4 bcf[TT][Sh::NQP];
-    const BwdLane l = bwd_lane<N>(p);
+    using Sh = BwdSumShape<N>;
+    constexpr int S = Sh::S, LN = Sh::LN, CH = Sh::CH, TT = kBwdTT;
+    constexpr int THREADS = kBwdWarps * 32;
+    __shared__ __align__(16) T act_s[2][3][CH][TT];
+    __shared__ __align__(16) T bc_s[2][N][TT];
+    __shared__ __align__(16) float2 sc[TT][CH];
+    __shared__ __align__(16) float2 bcf[TT][Sh::NQP];
+
     const int c = blockIdx.y;
     const bool fwd = blockIdx.z == 0;
     if (!fwd && c == 0) return;  // M_0 is not needed (uniform over the CTA)
+    const int lane = threadIdx.x & 31;
+    const int j = lane % LN;
+    const int r = (threadIdx.x) / LN;  // channel row within the CTA
+    const int cb = blockIdx.x % p.blocks_per_group;
+    const int bg = blockIdx.x / p.blocks_per_group;
+    const int g = bg % p.ngroups;
+    const int b = bg / p.ngroups;
+    const int dloc0 = cb * CH;
+    const bool active = dloc0 + r < p.dim_per_group;
+    const int d = g * p.dim_per_group + (active ? dloc0 + r : 0);
+    const long long bd = static_cast<long long>(b) * p.dim + d;
     const int L = p.seqlen;
     const int s0 = c * bwd_chunk_steps(N);
     const int s1 = min(L, s0 + bwd_chunk_steps(N));
     const int ntile = (s1 - s0 + TT - 1) / TT;
     const long long BD = static_cast<long long>(p.batch) * p.dim;
-
-    float a2[S];
-#pragma unroll
-    for (int s = 0; s < S; ++s) a2[s] = __ldg(p.A + static_cast<long long>(l.d) * N + l.j * S + s) * decay_scale<ACCURATE>();
-    const float bias = p.dt_bias ? __ldg(p.dt_bias + l.d) : 0.f;
     const bool vec = p.vec_ok != 0;
-    const T* drow = static_cast<const T*>(p.delta) + l.row;
+    const bool gated = p.z != nullptr;
 
-    if (fwd) {
-        const T* urow = static_cast<const T*>(p.u) + l.row;
-        float h[S], pr[S];
+    // Activation tensors staged: forward u, delta; backward delta, z, dy.
+    const int nact = fwd ? 2 : (gated ? 3 : 2);
+    auto act_ptr = [&](int x) -> const T* {
+        if (fwd) return static_cast<const T*>(x == 0 ? p.u : p.delta);
+        if (x == 0) return static_cast<const T*>(p.delta);
+        return static_cast<const T*>((x == 1 && gated) ? p.z : p.dy);
+    };
+    auto fetch = [&](int tile, int buf) {
+        const int t0 = s0 + tile * TT;
+        const int valid = L - t0;
+        const int na = nact * CH;
+        for (int item = threadIdx.x; item < na + N; item += THREADS) {
+            if (item < na) {
+                const int x = item / CH, rr = item % CH;
+                const int dl = min(dloc0 + rr, p.dim_per_group - 1);
+                const long long row = (static_cast<long long>(b) * p.dim + g * p.dim_per_group + dl) * L + t0;
+                bwd_stage_row<T>(&act_s[buf][x][rr][0], act_ptr(x) + row, valid, vec);
+            } else {
+                const int n = item - na;
+                const T* src = static_cast<const T*>(fwd ? p.B : p.C) + (static_cast<long long>(bg) * N + n) * L + t0;
+                bwd_stage_row<T>(&bc_s[buf][n][0], src, valid, vec);
+            }
+        }
+        cp_async_commit();
+    };
+
+    float2 a2[Sh::P], st[Sh::P];
 #pragma unroll
-        for (int s = 0; s < S; ++s) { h[s] = 0.f; pr[s] = 1.f; }
-        for (int i = 0; i < ntile; ++i) {
-            const int t0 = s0 + i * TT;
-            bwd_stage_bc<T, N>(p, l.bg, t0, true, false, bcf);
-            float uu[TT], dv[TT];
-            bwd_load_steps<T>(urow + t0, L - t0, vec, uu);
-            bwd_load_steps<T>(drow + t0, L - t0, vec, dv);
+    for (int k = 0; k < Sh::P; ++k) {
+        const float2 av = __ldg(reinterpret_cast<const float2*>(p.A + static_cast<long long>(d) * N + j * S) + k);
+        a2[k] = f2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
+        st[k] = f2(0.f);
+    }
+    float dsum = 0.f, dcomp = 0.f;
+
+    const int first = fwd ? 0 : ntile - 1;
+    fetch(first, 0);
+    for (int ii = 0; ii < ntile; ++ii) {
+        const int i = fwd ? ii : ntile - 1 - ii;
+        const int buf = ii & 1;
+        if (ii + 1 < ntile) {
+            fetch(fwd ? i + 1 : i - 1, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const int t0 = s0 + i * TT;
+        // Per-(channel, step) scalars and the widened B or C rows.
+        for (int item = threadIdx.x; item < TT * CH; item += THREADS) {
+            const int t = item / CH, rr = item % CH;
+            const int dl = min(dloc0 + rr, p.dim_per_group - 1);
+            const float bias = p.dt_bias ? __ldg(p.dt_bias + g * p.dim_per_group + dl) : 0.f;
+            const bool in = t0 + t < L;
+            if (fwd) {
+                const float dt = in ? softplus<ACCURATE>(bwd_to_f(act_s[buf][1][rr][t]) + bias) : 0.f;
+                sc[t][rr] = f2(dt, dt * bwd_to_f(act_s[buf][0][rr][t]));
+            } else {
+                const float dt = in ? softplus<ACCURATE>(bwd_to_f(act_s[buf][0][rr][t]) + bias) : 0.f;
+                float gg;
+                if (gated) {
+                    const float zv = bwd_to_f(act_s[buf][1][rr][t]);
+                    gg = bwd_to_f(act_s[buf][2][rr][t]) * zv * sigmoid_f<ACCURATE>(zv);
+                } else {
+                    gg = bwd_to_f(act_s[buf][1][rr][t]);
+                }
+                sc[t][rr] = f2(dt, gg);
+            }
+        }
+        for (int item = threadIdx.x; item < TT * N; item += THREADS) {
+            const int t = item % TT, n = item / TT;
+            const int q = n >> 1;
+            const int slot = (q % Sh::P) * LN + q / Sh::P;
+            reinterpret_cast<float*>(&bcf[t][slot])[n & 1] = bwd_to_f(bc_s[buf][n][t]);
+        }
+        __syncthreads();
+        if (fwd) {
 #pragma unroll
             for (int t = 0; t < TT; ++t) {
-                const float dt = (t0 + t < L) ? softplus<ACCURATE>(dv[t] + bias) : 0.f;
-                const float dtu = dt * uu[t];
+                const float2 q = sc[t][r];
+                if (ACCURATE) {
+                    const float yk = q.x - dcomp;
+                    const float tk = dsum + yk;
+                    dcomp = (tk - dsum) - yk;
+                    dsum = tk;
+                } else {
+                    dsum += q.x;
+                }
 #pragma unroll
-                for (int k = 0; k < Sh::P2; ++k) {
-                    const float4 q = bcf[t][k * Sh::LN + l.j];
-                    const float e0 = decay<ACCURATE>(dt * a2[2 * k]);
-                    const float e1 = decay<ACCURATE>(dt * a2[2 * k + 1]);
-                    pr[2 * k] *= e0;
-                    pr[2 * k + 1] *= e1;
-                    h[2 * k] = fmaf(e0, h[2 * k], dtu * q.x);
-                    h[2 * k + 1] = fmaf(e1, h[2 * k + 1], dtu * q.y);
+                for (int k = 0; k < Sh::P; ++k) {
+                    const float2 bq = bcf[t][k * LN + j];
+                    st[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), st[k], __fmul2_rn(f2(q.y), bq));
                 }
             }
-        }
-        if (l.active) {
-            float* out = p.fagg + (static_cast<long long>(c) * BD + l.bd) * (2 * N) + l.j * S;
-#pragma unroll
-            for (int s = 0; s < S; ++s) {
-                out[s] = pr[s];
-                out[N + s] = h[s];
-            }
-        }
-    } else {
-        const T* zrow = p.z ? static_cast<const T*>(p.z) + l.row : nullptr;
-        const T* yrow = static_cast<const T*>(p.dy) + l.row;
-        float mu[S];
-#pragma unroll
-        for (int s = 0; s < S; ++s) mu[s] = 0.f;
-        for (int i = ntile - 1; i >= 0; --i) {
-            const int t0 = s0 + i * TT;
-            bwd_stage_bc<T, N>(p, l.bg, t0, false, true, bcf);
-            float dv[TT], zz[TT], gy[TT];
-            bwd_load_steps<T>(drow + t0, L - t0, vec, dv);
-            bwd_load_steps<T>(yrow + t0, L - t0, vec, gy);
-            if (zrow) bwd_load_steps<T>(zrow + t0, L - t0, vec, zz);
+        } else {
 #pragma unroll
             for (int t = TT - 1; t >= 0; --t) {
-                const bool in = t0 + t < L;
-                const float dt = in ? softplus<ACCURATE>(dv[t] + bias) : 0.f;
-                const float g = zrow ? gy[t] * silu<ACCURATE>(zz[t]) : gy[t];
+                const float2 q = sc[t][r];
 #pragma unroll
-                for (int k = 0; k < Sh::P2; ++k) {
-                    const float4 q = bcf[t][k * Sh::LN + l.j];
-                    const float l0 = fmaf(g, q.z, mu[2 * k]);
-                    const float l1 = fmaf(g, q.w, mu[2 * k + 1]);
-                    mu[2 * k] = decay<ACCURATE>(dt * a2[2 * k]) * l0;
-                    mu[2 * k + 1] = decay<ACCURATE>(dt * a2[2 * k + 1]) * l1;
+                for (int k = 0; k < Sh::P; ++k) {
+                    const float2 cq = bcf[t][k * LN + j];
+                    const float2 lam = __ffma2_rn(f2(q.y), cq, st[k]);
+                    st[k] = __fmul2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), lam);
                 }
             }
         }
-        if (l.active) {
-            float* out = p.bagg + (static_cast<long long>(c) * BD + l.bd) * N + l.j * S;
+    }
+    if (active) {
+        if (fwd) {
+            float* out = p.fagg + (static_cast<long long>(c) * BD + bd) * (2 * N) + j * S;
 #pragma unroll
-            for (int s = 0; s < S; ++s) out[s] = mu[s];
+            for (int k = 0; k < Sh::P; ++k) {
+                const float2 pr = decay2<ACCURATE>(__fmul2_rn(a2[k], f2(dsum)));
+                reinterpret_cast<float2*>(out)[k] = pr;
+                reinterpret_cast<float2*>(out + N)[k] = st[k];
+            }
+        } else {
+            float* out = p.bagg + (static_cast<long long>(c) * BD + bd) * N + j * S;
+#pragma unroll
+            for (int k = 0; k < Sh::P; ++k) reinterpret_cast<float2*>(out)[k] = st[k];
         }
     }
 }
@@ -376,21 +460,50 @@ scan_bwd_carry_kernel(float* __restrict__ fagg, float* __restrict__ bagg, const 
 }
 
 // ---------------------------------------------------------------------------
-// 3. Main pass: checkpoints, then the tiles backwards.
+// 3. Main pass: checkpoints, then the tiles backwards.  Each tile's rows are
+// staged by cp.async one tile ahead; the per-(channel, step) scalars are
+// computed once into shared memory; the lanes run the state loops on packed
+// fp32 pairs.
 // ---------------------------------------------------------------------------
+template <typename T, int N>
+struct BwdLayout {
+    using Sh = BwdShape<N>;
+    static constexpr int TT = kBwdTT;
+    static constexpr int THREADS = kBwdWarps * 32;
+    static constexpr int CKPT = 0;                                                  // float4 [tiles][THREADS]
+    static constexpr int ACT = CKPT + bwd_chunk_tiles(N) * THREADS * 16;           // T [2][4][CH][TT]
+    static constexpr int BC = ACT + 2 * 4 * Sh::CH * TT * static_cast<int>(sizeof(T));  // T [2][2][N][TT]
+    static constexpr int SC = BC + 2 * 2 * N * TT * static_cast<int>(sizeof(T));   // float4 [TT][CH]
+    static constexpr int SC2 = SC + TT * Sh::CH * 16;                               // float2 [TT][CH]
+    static constexpr int BCF = SC2 + TT * Sh::CH * 8;                               // float4 [TT][NQP]
+    static constexpr int RED = BCF + TT * Sh::NQP * 16;                             // float [WARPS][TT][2N]
+    static constexpr int OUTS = RED + kBwdWarps * TT * 2 * N * 4;                   // float [3][CH][TT + 1]
+    static constexpr int BYTES = OUTS + 3 * Sh::CH * (TT + 1) * 4;
+};
+
+#ifndef SSM_BWD_MIN_BLOCKS
+#define SSM_BWD_MIN_BLOCKS 3
+#endif
 template <typename T, int N, bool ACCURATE>
-__global__ void __launch_bounds__(kBwdWarps * 32, 3)
+__global__ void __launch_bounds__(kBwdWarps * 32, SSM_BWD_MIN_BLOCKS)
 scan_bwd_kernel(const BwdParams p) {
     using Sh = BwdShape<N>;
+    using Lay = BwdLayout<T, N>;
     constexpr int S = Sh::S;
     constexpr int LN = Sh::LN;
     constexpr int CH = Sh::CH;
     constexpr int TT = kBwdTT;
+    constexpr int P2 = Sh::P2;
     constexpr int THREADS = kBwdWarps * 32;
-    __shared__ __align__(16) float4 ckpt[bwd_chunk_tiles(N)][THREADS];
-    __shared__ __align__(16) float4 bcf[TT][Sh::NQP];
-    __shared__ float red[kBwdWarps][TT][2 * N];
-    __shared__ float outs[3][CH][TT + 1];
+    extern __shared__ __align__(16) unsigned char smem[];
+    float4 (*ckpt)[THREADS] = reinterpret_cast<float4 (*)[THREADS]>(smem + Lay::CKPT);
+    T (*act_s)[4][CH][TT] = reinterpret_cast<T (*)[4][CH][TT]>(smem + Lay::ACT);
+    T (*bc_s)[2][N][TT] = reinterpret_cast<T (*)[2][N][TT]>(smem + Lay::BC);
+    float4 (*sc)[CH] = reinterpret_cast<float4 (*)[CH]>(smem + Lay::SC);
+    float2 (*sc2)[CH] = reinterpret_cast<float2 (*)[CH]>(smem + Lay::SC2);
+    float4 (*bcf)[Sh::NQP] = reinterpret_cast<float4 (*)[Sh::NQP]>(smem + Lay::BCF);
+    float (*red)[TT][2 * N] = reinterpret_cast<float (*)[TT][2 * N]>(smem + Lay::RED);
+    float (*outs)[CH][TT + 1] = reinterpret_cast<float (*)[CH][TT + 1]>(smem + Lay::OUTS);
 
     const BwdLane l = bwd_lane<N>(p);
     const int c = blockIdx.y;
@@ -401,153 +514,198 @@ scan_bwd_kernel(const BwdParams p) {
     const long long BD = static_cast<long long>(p.batch) * p.dim;
     const bool vec = p.vec_ok != 0;
     const bool gated = p.z != nullptr;
+    const int dloc0 = (blockIdx.x % p.blocks_per_group) * CH;
 
-    float a2[S], Ar[S], h[S], mu[S];
+    float2 a2[P2], Ar[P2], h[P2], mu[P2];
 #pragma unroll
-    for (int s = 0; s < S; ++s) {
-        Ar[s] = __ldg(p.A + static_cast<long long>(l.d) * N + l.j * S + s);
-        a2[s] = Ar[s] * decay_scale<ACCURATE>();
-        const long long st = l.bd * N + l.j * S + s;
-        if (c == 0) h[s] = p.h0 ? __ldg(p.h0 + st) : 0.f;
-        else h[s] = __ldcg(p.fagg + (static_cast<long long>(c - 1) * BD + l.bd) * (2 * N) + N + l.j * S + s);
-        if (c == p.nchunks - 1) mu[s] = p.dhf ? __ldg(p.dhf + st) : 0.f;
-        else mu[s] = __ldcg(p.bagg + (static_cast<long long>(c + 1) * BD + l.bd) * N + l.j * S + s);
-        if (!l.active) mu[s] = 0.f;
+    for (int k = 0; k < P2; ++k) {
+        const long long sidx = l.j * S + 2 * k;
+        Ar[k] = __ldg(reinterpret_cast<const float2*>(p.A + static_cast<long long>(l.d) * N + sidx));
+        a2[k] = __fmul2_rn(Ar[k], f2(decay_scale<ACCURATE>()));
+        const long long st = l.bd * N + sidx;
+        if (c == 0) h[k] = p.h0 ? __ldg(reinterpret_cast<const float2*>(p.h0 + st)) : f2(0.f);
+        else h[k] = __ldcg(reinterpret_cast<const float2*>(p.fagg + (static_cast<long long>(c - 1) * BD + l.bd) * (2 * N) + N + sidx));
+        if (c == p.nchunks - 1) mu[k] = p.dhf ? __ldg(reinterpret_cast<const float2*>(p.dhf + st)) : f2(0.f);
+        else mu[k] = __ldcg(reinterpret_cast<const float2*>(p.bagg + (static_cast<long long>(c + 1) * BD + l.bd) * N + sidx));
+        if (!l.active) mu[k] = f2(0.f);
     }
-    const float bias = p.dt_bias ? __ldg(p.dt_bias + l.d) : 0.f;
     const float dsk = p.D ? __ldg(p.D + l.d) : 0.f;
-    const T* urow = static_cast<const T*>(p.u) + l.row;
-    const T* drow = static_cast<const T*>(p.delta) + l.row;
-    const T* zrow = gated ? static_cast<const T*>(p.z) + l.row : nullptr;
-    const T* yrow = static_cast<const T*>(p.dy) + l.row;
+
+    auto act_ptr = [&](int x) -> const T* {
+        return static_cast<const T*>(x == kU ? p.u : (x == kDelta ? p.delta : (x == kZ ? p.z : p.dy)));
+    };
+    // Stage tile `tile` into buffer `buf`: the activation rows (u, delta, and
+    // for the backward walk z, dy) and the B (and C) rows.
+    auto fetch = [&](int tile, int buf, bool main) {
+        const int t0 = s0 + tile * TT;
+        const int valid = L - t0;
+        const int na = (main ? 4 : 2) * CH;
+        const int nb = (main ? 2 : 1) * N;
+        for (int item = threadIdx.x; item < na + nb; item += THREADS) {
+            if (item < na) {
+                const int x = item / CH, rr = item % CH;
+                if (x == kZ && !gated) continue;
+                const int dl = min(dloc0 + rr, p.dim_per_group - 1);
+                const long long row = (static_cast<long long>(l.b) * p.dim + l.g * p.dim_per_group + dl) * L + t0;
+                bwd_stage_row<T>(&act_s[buf][x][rr][0], act_ptr(x) + row, valid, vec);
+            } else {
+                const int k = item - na;
+                const int isC = k / N, n = k % N;
+                const T* src = static_cast<const T*>(isC ? p.C : p.B) + (static_cast<long long>(l.bg) * N + n) * L + t0;
+                bwd_stage_row<T>(&bc_s[buf][isC][n][0], src, valid, vec);
+            }
+        }
+        cp_async_commit();
+    };
+    // Per-(channel, step) scalars of the staged tile and the widened B/C rows.
+    auto prepare = [&](int t0, int buf, bool main) {
+        for (int item = threadIdx.x; item < TT * CH; item += THREADS) {
+            const int t = item / CH, rr = item % CH;
+            const bool live = dloc0 + rr < p.dim_per_group;
+            const int dl = live ? dloc0 + rr : p.dim_per_group - 1;
+            const float bias = p.dt_bias ? __ldg(p.dt_bias + l.g * p.dim_per_group + dl) : 0.f;
+            const bool in = t0 + t < L;
+            const float uv = bwd_to_f(act_s[buf][kU][rr][t]);
+            float dt = 0.f, sg = 0.f;
+            if (in) softplus_sigmoid<ACCURATE>(bwd_to_f(act_s[buf][kDelta][rr][t]) + bias, dt, sg);
+            if (!main) {
+                sc[t][rr] = make_float4(dt, dt * uv, 0.f, uv);
+                continue;
+            }
+            const float dy = live ? bwd_to_f(act_s[buf][kDy][rr][t]) : 0.f;
+            float gg = dy, dzf = 0.f;
+            if (gated) {
+                const float zv = bwd_to_f(act_s[buf][kZ][rr][t]);
+                const float sz = sigmoid_f<ACCURATE>(zv);
+                gg = dy * zv * sz;
+                dzf = dy * sz * fmaf(zv, 1.f - sz, 1.f);
+            }
+            sc[t][rr] = make_float4(dt, dt * uv, gg, uv);
+            sc2[t][rr] = make_float2(sg, dzf);
+        }
+        for (int item = threadIdx.x; item < (main ? 2 : 1) * N * TT; item += THREADS) {
+            const int t = item % TT, n = (item / TT) % N, isC = item / (TT * N);
+            const int q = n >> 1;
+            const int slot = (q % P2) * LN + q / P2;
+            reinterpret_cast<float*>(&bcf[t][slot])[isC * 2 + (n & 1)] = bwd_to_f(bc_s[buf][isC][n][t]);
+        }
+    };
 
     // ---- forward sweep: the state at every tile start ----
+    fetch(0, 0, false);
     for (int i = 0; i < ntile; ++i) {
-        const int t0 = s0 + i * TT;
-        ckpt[i][threadIdx.x] = make_float4(h[0], h[1], h[2], h[3]);
-        bwd_stage_bc<T, N>(p, l.bg, t0, true, false, bcf);
-        float uu[TT], dv[TT];
-        bwd_load_steps<T>(urow + t0, L - t0, vec, uu);
-        bwd_load_steps<T>(drow + t0, L - t0, vec, dv);
+        const int buf = i & 1;
+        if (i + 1 < ntile) {
+            fetch(i + 1, buf ^ 1, false);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        prepare(s0 + i * TT, buf, false);
+        __syncthreads();
+        ckpt[i][threadIdx.x] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
-            const float dt = (t0 + t < L) ? softplus<ACCURATE>(dv[t] + bias) : 0.f;
-            const float dtu = dt * uu[t];
+            const float4 q = sc[t][l.r];
 #pragma unroll
-            for (int k = 0; k < Sh::P2; ++k) {
-                const float4 q = bcf[t][k * LN + l.j];
-                h[2 * k] = fmaf(decay<ACCURATE>(dt * a2[2 * k]), h[2 * k], dtu * q.x);
-                h[2 * k + 1] = fmaf(decay<ACCURATE>(dt * a2[2 * k + 1]), h[2 * k + 1], dtu * q.y);
+            for (int k = 0; k < P2; ++k) {
+                const float4 bq = bcf[t][k * LN + l.j];
+                h[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), h[k], __fmul2_rn(f2(q.y), f2(bq.x, bq.y)));
             }
         }
     }
 
     bool xw;
     const int xid0 = xchan_first_id<LN, Sh::NV>(l.lane, xw);
-    float dA_acc[S];
+    float2 dA_acc[P2];
 #pragma unroll
-    for (int s = 0; s < S; ++s) dA_acc[s] = 0.f;
+    for (int k = 0; k < P2; ++k) dA_acc[k] = f2(0.f);
     float dD_acc = 0.f, db_acc = 0.f;
 
     // ---- the tiles backwards ----
-    for (int i = ntile - 1; i >= 0; --i) {
+    fetch(ntile - 1, 0, true);
+    for (int ii = 0; ii < ntile; ++ii) {
+        const int i = ntile - 1 - ii;
+        const int buf = ii & 1;
         const int t0 = s0 + i * TT;
-        bwd_stage_bc<T, N>(p, l.bg, t0, true, true, bcf);
-        float uu[TT], dv[TT], zz[TT], gy[TT];
-        bwd_load_steps<T>(urow + t0, L - t0, vec, uu);
-        bwd_load_steps<T>(drow + t0, L - t0, vec, dv);
-        bwd_load_steps<T>(yrow + t0, L - t0, vec, gy);
-        if (gated) bwd_load_steps<T>(zrow + t0, L - t0, vec, zz);
-        if (!l.active) {
-#pragma unroll
-            for (int t = 0; t < TT; ++t) gy[t] = 0.f;
+        if (i > 0) {
+            fetch(i - 1, buf ^ 1, true);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
+        __syncthreads();
+        prepare(t0, buf, true);
+        __syncthreads();
 
-        // Recompute the tile's states from its checkpoint; hist[t] = state
-        // before step t; the readout s_t is summed over the channel's lanes.
-        float hist[TT][S], dts[TT], sg[TT], ys[TT];
+        // Recompute the tile's states from its checkpoint: hist[t] = state
+        // before step t; ys[t] = the ungated output s_t.
+        float2 hist[TT][P2];
+        float ys[TT];
+        float2 hh[P2];
         {
             const float4 c4 = ckpt[i][threadIdx.x];
-            float hh[S] = {c4.x, c4.y, c4.z, c4.w};
+            hh[0] = f2(c4.x, c4.y);
+            hh[1] = f2(c4.z, c4.w);
+        }
 #pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                const bool in = t0 + t < L;
-                const float v = dv[t] + bias;
-                const float dt = in ? softplus<ACCURATE>(v) : 0.f;
-                dts[t] = dt;
-                sg[t] = in ? sigmoid_f<ACCURATE>(v) : 0.f;
-                const float dtu = dt * uu[t];
-                float y = 0.f;
+        for (int t = 0; t < TT; ++t) {
+            const float4 q = sc[t][l.r];
+            float2 y2 = f2(0.f);
 #pragma unroll
-                for (int k = 0; k < Sh::P2; ++k) {
-                    const float4 q = bcf[t][k * LN + l.j];
-                    hist[t][2 * k] = hh[2 * k];
-                    hist[t][2 * k + 1] = hh[2 * k + 1];
-                    hh[2 * k] = fmaf(decay<ACCURATE>(dt * a2[2 * k]), hh[2 * k], dtu * q.x);
-                    hh[2 * k + 1] = fmaf(decay<ACCURATE>(dt * a2[2 * k + 1]), hh[2 * k + 1], dtu * q.y);
-                    y = fmaf(q.z, hh[2 * k], y);
-                    y = fmaf(q.w, hh[2 * k + 1], y);
-                }
-                ys[t] = lane_sum<LN>(y) + dsk * uu[t];
+            for (int k = 0; k < P2; ++k) {
+                const float4 bq = bcf[t][k * LN + l.j];
+                hist[t][k] = hh[k];
+                hh[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), hh[k], __fmul2_rn(f2(q.y), f2(bq.x, bq.y)));
+                y2 = __ffma2_rn(f2(bq.z, bq.w), hh[k], y2);
             }
-            // The state after the tile's last step (h_t of that step).
-#pragma unroll
-            for (int s = 0; s < S; ++s) h[s] = hh[s];
+            ys[t] = fmaf(dsk, q.w, lane_sum<LN>(y2.x + y2.y));
         }
 
         // The adjoint, backwards over the tile.
 #pragma unroll
         for (int t = TT - 1; t >= 0; --t) {
-            float g = gy[t], dzv = 0.f;
-            if (gated) {
-                const float sz = sigmoid_f<ACCURATE>(zz[t]);
-                dzv = gy[t] * ys[t] * sz * fmaf(zz[t], 1.f - sz, 1.f);
-                g = gy[t] * zz[t] * sz;
-            }
-            const float dt = dts[t];
-            const float dtu = dt * uu[t];
+            const float4 q = sc[t][l.r];   // Delta, Delta u, g, u
+            const float2 q2 = sc2[t][l.r]; // sigmoid(delta + bias), dz factor
             float vals[Sh::NV];
-            float sb = 0.f, sd = 0.f;
+            float2 sb2 = f2(0.f), sd2 = f2(0.f);
 #pragma unroll
-            for (int k = 0; k < Sh::P2; ++k) {
-                const float4 q = bcf[t][k * LN + l.j];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int s = 2 * k + e;
-                    const float Bv = e ? q.y : q.x;
-                    const float Cv = e ? q.w : q.z;
-                    const float hcur = (t == TT - 1) ? h[s] : hist[t + 1 < TT ? t + 1 : t][s];
-                    const float hprev = hist[t][s];
-                    const float a = decay<ACCURATE>(dt * a2[s]);
-                    const float lam = fmaf(g, Cv, mu[s]);
-                    vals[s] = lam * dtu;
-                    vals[S + s] = g * hcur;
-                    sb = fmaf(lam, Bv, sb);
-                    const float ah = a * hprev;
-                    sd = fmaf(lam, fmaf(Bv, uu[t], Ar[s] * ah), sd);
-                    dA_acc[s] = fmaf(lam * dt, ah, dA_acc[s]);
-                    mu[s] = a * lam;
-                }
+            for (int k = 0; k < P2; ++k) {
+                const float4 bq = bcf[t][k * LN + l.j];
+                const float2 Bv = f2(bq.x, bq.y), Cv = f2(bq.z, bq.w);
+                const float2 hcur = (t == TT - 1) ? hh[k] : hist[t + 1 < TT ? t + 1 : t][k];
+                const float2 a = decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k]));
+                const float2 lam = __ffma2_rn(f2(q.z), Cv, mu[k]);
+                const float2 db = __fmul2_rn(lam, f2(q.y));
+                const float2 dc = __fmul2_rn(f2(q.z), hcur);
+                vals[2 * k] = db.x;
+                vals[2 * k + 1] = db.y;
+                vals[S + 2 * k] = dc.x;
+                vals[S + 2 * k + 1] = dc.y;
+                sb2 = __ffma2_rn(lam, Bv, sb2);
+                const float2 ah = __fmul2_rn(a, hist[t][k]);
+                sd2 = __ffma2_rn(lam, __ffma2_rn(Bv, f2(q.w), __fmul2_rn(Ar[k], ah)), sd2);
+                dA_acc[k] = __ffma2_rn(__fmul2_rn(lam, f2(q.x)), ah, dA_acc[k]);
+                mu[k] = __fmul2_rn(a, lam);
             }
-            sb = lane_sum<LN>(sb);
-            sd = lane_sum<LN>(sd);
-            const float duv = fmaf(g, dsk, dt * sb);
-            const float ddv = sd * sg[t];
-            dD_acc = fmaf(g, uu[t], dD_acc);
+            const float sb = lane_sum<LN>(sb2.x + sb2.y);
+            const float sd = lane_sum<LN>(sd2.x + sd2.y);
+            const float duv = fmaf(q.z, dsk, q.x * sb);
+            const float ddv = sd * q2.x;
+            dD_acc = fmaf(q.z, q.w, dD_acc);
             db_acc += ddv;
             if (l.j == 0 % LN) outs[0][l.r][t] = duv;
             if (l.j == 1 % LN) outs[1][l.r][t] = ddv;
-            if (l.j == 2 % LN) outs[2][l.r][t] = dzv;
+            if (l.j == 2 % LN) outs[2][l.r][t] = q2.y * ys[t];
 
             // dB, dC: sum over the warp's channels, then stage per warp.
             xchan_reduce<16, LN, Sh::NV>(vals, l.lane);
             if (xw) {
 #pragma unroll
-                for (int q = 0; q < Sh::CF; ++q) {
-                    const int id = xid0 + q;
-                    const int tensor = id / S;
-                    const int n = l.j * S + id % S;
-                    red[l.warp][t][tensor * N + n] = vals[q];
+                for (int qq = 0; qq < Sh::CF; ++qq) {
+                    const int id = xid0 + qq;
+                    red[l.warp][t][(id / S) * N + l.j * S + id % S] = vals[qq];
                 }
             }
         }
@@ -561,24 +719,21 @@ scan_bwd_kernel(const BwdParams p) {
                 float v = 0.f;
 #pragma unroll
                 for (int w = 0; w < kBwdWarps; ++w) v += red[w][t][k];
-                const int tensor = k / N;
-                const int n = k % N;
-                float* dst = tensor ? p.dC : p.dB;
-                atomicAdd(dst + (static_cast<long long>(l.bg) * N + n) * L + t0 + t, v);
+                float* dst = (k / N) ? p.dC : p.dB;
+                atomicAdd(dst + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + t, v);
             }
         }
         // du, ddelta, dz rows of the tile.
         {
             constexpr int VP = 16 / static_cast<int>(sizeof(T));
-            const int dloc0 = (blockIdx.x % p.blocks_per_group) * CH;
             for (int e = threadIdx.x; e < 3 * CH * (TT / VP); e += THREADS) {
                 const int part = e % (TT / VP);
                 const int rr = (e / (TT / VP)) % CH;
                 const int x = e / (TT / VP) / CH;
                 if (x == 2 && !gated) continue;
                 if (dloc0 + rr >= p.dim_per_group) continue;
-                const long long drow_out = (static_cast<long long>(l.b) * p.dim + l.g * p.dim_per_group + dloc0 + rr) * L;
-                T* dst = static_cast<T*>(x == 0 ? p.du : (x == 1 ? p.ddelta : p.dz)) + drow_out + t0 + part * VP;
+                const long long orow = (static_cast<long long>(l.b) * p.dim + l.g * p.dim_per_group + dloc0 + rr) * L;
+                T* dst = static_cast<T*>(x == 0 ? p.du : (x == 1 ? p.ddelta : p.dz)) + orow + t0 + part * VP;
                 float f[VP];
 #pragma unroll
                 for (int k = 0; k < VP; ++k) f[k] = outs[x][rr][part * VP + k];
@@ -590,11 +745,15 @@ scan_bwd_kernel(const BwdParams p) {
     // dh0 (the adjoint leaving the first step of the sequence).
     if (c == 0 && p.dh0 && l.active) {
 #pragma unroll
-        for (int s = 0; s < S; ++s) p.dh0[l.bd * N + l.j * S + s] = mu[s];
+        for (int k = 0; k < P2; ++k)
+            *reinterpret_cast<float2*>(p.dh0 + l.bd * N + l.j * S + 2 * k) = mu[k];
     }
     if (l.active) {
 #pragma unroll
-        for (int s = 0; s < S; ++s) atomicAdd(p.dA + static_cast<long long>(l.d) * N + l.j * S + s, dA_acc[s]);
+        for (int k = 0; k < P2; ++k) {
+            atomicAdd(p.dA + static_cast<long long>(l.d) * N + l.j * S + 2 * k, dA_acc[k].x);
+            atomicAdd(p.dA + static_cast<long long>(l.d) * N + l.j * S + 2 * k + 1, dA_acc[k].y);
+        }
         if (l.j == 0) {
             if (p.dD) atomicAdd(p.dD + l.d, dD_acc);
             if (p.ddt_bias) atomicAdd(p.ddt_bias + l.d, db_acc);

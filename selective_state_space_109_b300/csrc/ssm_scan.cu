@@ -739,7 +739,13 @@ cudaError_t launch_bwd_n(const ssm::BwdParams& p, cudaStream_t st) {
                     static_cast<unsigned>(p.nchunks), 1);
     const dim3 block(ssm::kBwdWarps * 32);
     if (p.nchunks > 1) {
-        ssm::scan_bwd_summary_kernel<T, N, kAcc><<<dim3(grid.x, grid.y, 2), block, 0, st>>>(p);
+        // The summary pass holds more states per lane: its own channel blocks.
+        ssm::BwdParams ps = p;
+        constexpr int sch = ssm::BwdSumShape<N>::CH;
+        ps.blocks_per_group = (p.dim_per_group + sch - 1) / sch;
+        const dim3 sgrid(static_cast<unsigned>(static_cast<long long>(ps.blocks_per_group) * p.batch * p.ngroups),
+                         static_cast<unsigned>(p.nchunks), 2);
+        ssm::scan_bwd_summary_kernel<T, N, kAcc><<<sgrid, block, 0, st>>>(ps);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         const long long BD = static_cast<long long>(p.batch) * p.dim;
@@ -749,7 +755,12 @@ cudaError_t launch_bwd_n(const ssm::BwdParams& p, cudaStream_t st) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    ssm::scan_bwd_kernel<T, N, kAcc><<<grid, block, 0, st>>>(p);
+    auto kern = ssm::scan_bwd_kernel<T, N, kAcc>;
+    constexpr int smem = ssm::BwdLayout<T, N>::BYTES;
+    static unsigned long long done = 0;
+    const cudaError_t e = ensure_smem(kern, smem, &done);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, block, smem, st>>>(p);
     return cudaGetLastError();
 }
 
