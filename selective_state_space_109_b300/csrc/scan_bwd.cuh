@@ -19,10 +19,10 @@
 // Structure.  Time is cut into chunks of bwd_chunk_steps(N) steps; a CTA owns CH
 // channels of one (sequence, group) and one chunk.  Both recurrences run
 // across chunks through summaries, as in the forward pass:
-//   1. summary pass (two modes in one launch): forward, from a zero state,
-//      the chunk's decay product P and end state E; backward, from a zero
-//      adjoint, the adjoint M that leaves the chunk at its start
-//      (mu = Abar_t lam_t after the chunk's first step);
+//   1. summary pass: per chunk, from a zero state, the decay product P and
+//      end state E; and, from a zero adjoint at the chunk's end, the adjoint
+//      M that leaves the chunk at its start (mu = Abar_t lam_t after the
+//      chunk's first step), accumulated forwards in the same walk;
 //   2. carry pass: h entering chunk c+1 = P_c h + E_c (from h0), and the
 //      adjoint entering chunk c-1 from the right = P_c mu + M_c (from dh_final);
 //   3. main pass: from the state entering its chunk, a forward sweep stores
@@ -228,10 +228,15 @@ __device__ __forceinline__ BwdLane bwd_lane(const BwdParams& p) {
 }
 
 // ---------------------------------------------------------------------------
-// 1. Chunk summaries.  blockIdx.z = 0: forward (P_c, E_c); 1: backward M_c.
-// Needs no exchange between lanes, so a lane holds up to 16 states (one lane
-// per channel up to N = 16).  The per-step scalars (Delta, Delta u or the
-// gate gradient g) are computed once per (channel, step) into shared memory.
+// 1. Chunk summaries, both in one forward walk over the chunk [s, e):
+//      P_c = prod_t Abar_t,  E_c = the end state from a zero state,
+//      M_c = the adjoint leaving the chunk at its start when none enters at
+//            its end = sum_t (prod_{r=s..t} Abar_r) g_t C_t,
+//    the last accumulated forwards with the running product, so the decays
+//    are computed once for both.  No exchange between lanes is needed, so a
+//    lane holds up to 16 states (one lane per channel up to N = 16).  The
+//    per-step scalars (Delta, Delta u, g) are computed once per (channel,
+//    step) into shared memory.
 // ---------------------------------------------------------------------------
 template <int N>
 struct BwdSumShape {
@@ -242,23 +247,34 @@ struct BwdSumShape {
     static constexpr int NQP = N / 2 + 1;
 };
 
+template <typename T, int N>
+struct BwdSumLayout {
+    using Sh = BwdSumShape<N>;
+    static constexpr int TT = kBwdTT;
+    static constexpr int ACT = 0;                                                        // T [2][4][CH][TT]
+    static constexpr int BC = ACT + 2 * 4 * Sh::CH * TT * static_cast<int>(sizeof(T));  // T [2][2][N][TT]
+    static constexpr int SC = BC + 2 * 2 * N * TT * static_cast<int>(sizeof(T));        // float4 [TT][CH]
+    static constexpr int BCF = SC + TT * Sh::CH * 16;                                    // float4 [TT][NQP]
+    static constexpr int BYTES = BCF + TT * Sh::NQP * 16;
+};
+
 template <typename T, int N, bool ACCURATE>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 scan_bwd_summary_kernel(const BwdParams p) {
     using Sh = BwdSumShape<N>;
+    using Lay = BwdSumLayout<T, N>;
     constexpr int S = Sh::S, LN = Sh::LN, CH = Sh::CH, TT = kBwdTT;
     constexpr int THREADS = kBwdWarps * 32;
-    __shared__ __align__(16) T act_s[2][3][CH][TT];
-    __shared__ __align__(16) T bc_s[2][N][TT];
-    __shared__ __align__(16) float2 sc[TT][CH];
-    __shared__ __align__(16) float2 bcf[TT][Sh::NQP];
+    extern __shared__ __align__(16) unsigned char smem[];
+    T (*act_s)[4][CH][TT] = reinterpret_cast<T (*)[4][CH][TT]>(smem + Lay::ACT);
+    T (*bc_s)[2][N][TT] = reinterpret_cast<T (*)[2][N][TT]>(smem + Lay::BC);
+    float4 (*sc)[CH] = reinterpret_cast<float4 (*)[CH]>(smem + Lay::SC);
+    float4 (*bcf)[Sh::NQP] = reinterpret_cast<float4 (*)[Sh::NQP]>(smem + Lay::BCF);
 
     const int c = blockIdx.y;
-    const bool fwd = blockIdx.z == 0;
-    if (!fwd && c == 0) return;  // M_0 is not needed (uniform over the CTA)
     const int lane = threadIdx.x & 31;
     const int j = lane % LN;
-    const int r = (threadIdx.x) / LN;  // channel row within the CTA
+    const int r = threadIdx.x / LN;  // channel row within the CTA
     const int cb = blockIdx.x % p.blocks_per_group;
     const int bg = blockIdx.x / p.blocks_per_group;
     const int g = bg % p.ngroups;
@@ -275,126 +291,94 @@ scan_bwd_summary_kernel(const BwdParams p) {
     const bool vec = p.vec_ok != 0;
     const bool gated = p.z != nullptr;
 
-    // Activation tensors staged: forward u, delta; backward delta, z, dy.
-    const int nact = fwd ? 2 : (gated ? 3 : 2);
     auto act_ptr = [&](int x) -> const T* {
-        if (fwd) return static_cast<const T*>(x == 0 ? p.u : p.delta);
-        if (x == 0) return static_cast<const T*>(p.delta);
-        return static_cast<const T*>((x == 1 && gated) ? p.z : p.dy);
+        return static_cast<const T*>(x == kU ? p.u : (x == kDelta ? p.delta : (x == kZ ? p.z : p.dy)));
     };
     auto fetch = [&](int tile, int buf) {
         const int t0 = s0 + tile * TT;
         const int valid = L - t0;
-        const int na = nact * CH;
-        for (int item = threadIdx.x; item < na + N; item += THREADS) {
+        constexpr int na = 4 * CH;
+        for (int item = threadIdx.x; item < na + 2 * N; item += THREADS) {
             if (item < na) {
                 const int x = item / CH, rr = item % CH;
+                if (x == kZ && !gated) continue;
                 const int dl = min(dloc0 + rr, p.dim_per_group - 1);
                 const long long row = (static_cast<long long>(b) * p.dim + g * p.dim_per_group + dl) * L + t0;
                 bwd_stage_row<T>(&act_s[buf][x][rr][0], act_ptr(x) + row, valid, vec);
             } else {
-                const int n = item - na;
-                const T* src = static_cast<const T*>(fwd ? p.B : p.C) + (static_cast<long long>(bg) * N + n) * L + t0;
-                bwd_stage_row<T>(&bc_s[buf][n][0], src, valid, vec);
+                const int k = item - na;
+                const int isC = k / N, n = k % N;
+                const T* src = static_cast<const T*>(isC ? p.C : p.B) + (static_cast<long long>(bg) * N + n) * L + t0;
+                bwd_stage_row<T>(&bc_s[buf][isC][n][0], src, valid, vec);
             }
         }
         cp_async_commit();
     };
 
-    float2 a2[Sh::P], st[Sh::P];
+    float2 a2[Sh::P], hs[Sh::P], pr[Sh::P], ms[Sh::P];
 #pragma unroll
     for (int k = 0; k < Sh::P; ++k) {
         const float2 av = __ldg(reinterpret_cast<const float2*>(p.A + static_cast<long long>(d) * N + j * S) + k);
         a2[k] = f2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
-        st[k] = f2(0.f);
+        hs[k] = f2(0.f);
+        pr[k] = f2(1.f);
+        ms[k] = f2(0.f);
     }
-    float dsum = 0.f, dcomp = 0.f;
 
-    const int first = fwd ? 0 : ntile - 1;
-    fetch(first, 0);
-    for (int ii = 0; ii < ntile; ++ii) {
-        const int i = fwd ? ii : ntile - 1 - ii;
-        const int buf = ii & 1;
-        if (ii + 1 < ntile) {
-            fetch(fwd ? i + 1 : i - 1, buf ^ 1);
+    fetch(0, 0);
+    for (int i = 0; i < ntile; ++i) {
+        const int buf = i & 1;
+        if (i + 1 < ntile) {
+            fetch(i + 1, buf ^ 1);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
         __syncthreads();
         const int t0 = s0 + i * TT;
-        // Per-(channel, step) scalars and the widened B or C rows.
+        // Per-(channel, step) scalars and the widened B, C rows.
         for (int item = threadIdx.x; item < TT * CH; item += THREADS) {
             const int t = item / CH, rr = item % CH;
-            const int dl = min(dloc0 + rr, p.dim_per_group - 1);
+            const bool live = dloc0 + rr < p.dim_per_group;
+            const int dl = live ? dloc0 + rr : p.dim_per_group - 1;
             const float bias = p.dt_bias ? __ldg(p.dt_bias + g * p.dim_per_group + dl) : 0.f;
             const bool in = t0 + t < L;
-            if (fwd) {
-                const float dt = in ? softplus<ACCURATE>(bwd_to_f(act_s[buf][1][rr][t]) + bias) : 0.f;
-                sc[t][rr] = f2(dt, dt * bwd_to_f(act_s[buf][0][rr][t]));
-            } else {
-                const float dt = in ? softplus<ACCURATE>(bwd_to_f(act_s[buf][0][rr][t]) + bias) : 0.f;
-                float gg;
-                if (gated) {
-                    const float zv = bwd_to_f(act_s[buf][1][rr][t]);
-                    gg = bwd_to_f(act_s[buf][2][rr][t]) * zv * sigmoid_f<ACCURATE>(zv);
-                } else {
-                    gg = bwd_to_f(act_s[buf][1][rr][t]);
-                }
-                sc[t][rr] = f2(dt, gg);
+            const float dt = in ? softplus<ACCURATE>(bwd_to_f(act_s[buf][kDelta][rr][t]) + bias) : 0.f;
+            float gg = live ? bwd_to_f(act_s[buf][kDy][rr][t]) : 0.f;
+            if (gated) {
+                const float zv = bwd_to_f(act_s[buf][kZ][rr][t]);
+                gg *= zv * sigmoid_f<ACCURATE>(zv);
             }
+            sc[t][rr] = make_float4(dt, dt * bwd_to_f(act_s[buf][kU][rr][t]), gg, 0.f);
         }
-        for (int item = threadIdx.x; item < TT * N; item += THREADS) {
-            const int t = item % TT, n = item / TT;
+        for (int item = threadIdx.x; item < 2 * N * TT; item += THREADS) {
+            const int t = item % TT, n = (item / TT) % N, isC = item / (TT * N);
             const int q = n >> 1;
             const int slot = (q % Sh::P) * LN + q / Sh::P;
-            reinterpret_cast<float*>(&bcf[t][slot])[n & 1] = bwd_to_f(bc_s[buf][n][t]);
+            reinterpret_cast<float*>(&bcf[t][slot])[isC * 2 + (n & 1)] = bwd_to_f(bc_s[buf][isC][n][t]);
         }
         __syncthreads();
-        if (fwd) {
 #pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                const float2 q = sc[t][r];
-                if (ACCURATE) {
-                    const float yk = q.x - dcomp;
-                    const float tk = dsum + yk;
-                    dcomp = (tk - dsum) - yk;
-                    dsum = tk;
-                } else {
-                    dsum += q.x;
-                }
+        for (int t = 0; t < TT; ++t) {
+            const float4 q = sc[t][r];
 #pragma unroll
-                for (int k = 0; k < Sh::P; ++k) {
-                    const float2 bq = bcf[t][k * LN + j];
-                    st[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), st[k], __fmul2_rn(f2(q.y), bq));
-                }
-            }
-        } else {
-#pragma unroll
-            for (int t = TT - 1; t >= 0; --t) {
-                const float2 q = sc[t][r];
-#pragma unroll
-                for (int k = 0; k < Sh::P; ++k) {
-                    const float2 cq = bcf[t][k * LN + j];
-                    const float2 lam = __ffma2_rn(f2(q.y), cq, st[k]);
-                    st[k] = __fmul2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), lam);
-                }
+            for (int k = 0; k < Sh::P; ++k) {
+                const float4 bq = bcf[t][k * LN + j];
+                const float2 a = decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k]));
+                hs[k] = __ffma2_rn(a, hs[k], __fmul2_rn(f2(q.y), f2(bq.x, bq.y)));
+                pr[k] = __fmul2_rn(pr[k], a);
+                ms[k] = __ffma2_rn(pr[k], __fmul2_rn(f2(q.z), f2(bq.z, bq.w)), ms[k]);
             }
         }
     }
     if (active) {
-        if (fwd) {
-            float* out = p.fagg + (static_cast<long long>(c) * BD + bd) * (2 * N) + j * S;
+        float* fo = p.fagg + (static_cast<long long>(c) * BD + bd) * (2 * N) + j * S;
+        float* bo = p.bagg + (static_cast<long long>(c) * BD + bd) * N + j * S;
 #pragma unroll
-            for (int k = 0; k < Sh::P; ++k) {
-                const float2 pr = decay2<ACCURATE>(__fmul2_rn(a2[k], f2(dsum)));
-                reinterpret_cast<float2*>(out)[k] = pr;
-                reinterpret_cast<float2*>(out + N)[k] = st[k];
-            }
-        } else {
-            float* out = p.bagg + (static_cast<long long>(c) * BD + bd) * N + j * S;
-#pragma unroll
-            for (int k = 0; k < Sh::P; ++k) reinterpret_cast<float2*>(out)[k] = st[k];
+        for (int k = 0; k < Sh::P; ++k) {
+            reinterpret_cast<float2*>(fo)[k] = pr[k];
+            reinterpret_cast<float2*>(fo + N)[k] = hs[k];
+            reinterpret_cast<float2*>(bo)[k] = ms[k];
         }
     }
 }
@@ -481,11 +465,10 @@ struct BwdLayout {
     static constexpr int BYTES = OUTS + 3 * Sh::CH * (TT + 1) * 4;
 };
 
-#ifndef SSM_BWD_MIN_BLOCKS
-#define SSM_BWD_MIN_BLOCKS 3
-#endif
+// Three CTAs per SM: at four the register cap (128) spills the tile's
+// recomputed states, which measured 40% slower on B300.
 template <typename T, int N, bool ACCURATE>
-__global__ void __launch_bounds__(kBwdWarps * 32, SSM_BWD_MIN_BLOCKS)
+__global__ void __launch_bounds__(kBwdWarps * 32, 3)
 scan_bwd_kernel(const BwdParams p) {
     using Sh = BwdShape<N>;
     using Lay = BwdLayout<T, N>;

@@ -744,9 +744,14 @@ cudaError_t launch_bwd_n(const ssm::BwdParams& p, cudaStream_t st) {
         constexpr int sch = ssm::BwdSumShape<N>::CH;
         ps.blocks_per_group = (p.dim_per_group + sch - 1) / sch;
         const dim3 sgrid(static_cast<unsigned>(static_cast<long long>(ps.blocks_per_group) * p.batch * p.ngroups),
-                         static_cast<unsigned>(p.nchunks), 2);
-        ssm::scan_bwd_summary_kernel<T, N, kAcc><<<sgrid, block, 0, st>>>(ps);
-        cudaError_t e = cudaGetLastError();
+                         static_cast<unsigned>(p.nchunks), 1);
+        auto skern = ssm::scan_bwd_summary_kernel<T, N, kAcc>;
+        constexpr int ssmem = ssm::BwdSumLayout<T, N>::BYTES;
+        static unsigned long long sdone = 0;
+        cudaError_t e = ensure_smem(skern, ssmem, &sdone);
+        if (e != cudaSuccess) return e;
+        skern<<<sgrid, block, ssmem, st>>>(ps);
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         const long long BD = static_cast<long long>(p.batch) * p.dim;
         const long long n = BD * N;
