@@ -623,9 +623,8 @@ scan_bwd_kernel(const BwdParams p) {
         __syncthreads();
 
         // Recompute the tile's states from its checkpoint: hist[t] = state
-        // before step t; ys[t] = the ungated output s_t.
+        // before step t.  The ungated output s_t gives dz_t = dy_t s_t silu'(z_t).
         float2 hist[TT][P2];
-        float ys[TT];
         float2 hh[P2];
         {
             const float4 c4 = ckpt[i][threadIdx.x];
@@ -643,7 +642,8 @@ scan_bwd_kernel(const BwdParams p) {
                 hh[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), hh[k], __fmul2_rn(f2(q.y), f2(bq.x, bq.y)));
                 y2 = __ffma2_rn(f2(bq.z, bq.w), hh[k], y2);
             }
-            ys[t] = fmaf(dsk, q.w, lane_sum<LN>(y2.x + y2.y));
+            const float ys = fmaf(dsk, q.w, lane_sum<LN>(y2.x + y2.y));
+            if (l.j == 2 % LN) outs[2][l.r][t] = sc2[t][l.r].y * ys;
         }
 
         // The adjoint, backwards over the tile.
@@ -680,7 +680,6 @@ scan_bwd_kernel(const BwdParams p) {
             db_acc += ddv;
             if (l.j == 0 % LN) outs[0][l.r][t] = duv;
             if (l.j == 1 % LN) outs[1][l.r][t] = ddv;
-            if (l.j == 2 % LN) outs[2][l.r][t] = q2.y * ys[t];
 
             // dB, dC: sum over the warp's channels, then stage per warp.
             xchan_reduce<16, LN, Sh::NV>(vals, l.lane);
