@@ -233,14 +233,15 @@ __device__ __forceinline__ BwdLane bwd_lane(const BwdParams& p) {
 //      M_c = the adjoint leaving the chunk at its start when none enters at
 //            its end = sum_t (prod_{r=s..t} Abar_r) g_t C_t,
 //    the last accumulated forwards with the running product, so the decays
-//    are computed once for both.  No exchange between lanes is needed, so a
-//    lane holds up to 16 states (one lane per channel up to N = 16).  The
-//    per-step scalars (Delta, Delta u, g) are computed once per (channel,
-//    step) into shared memory.
+//    are computed once for both.  No exchange between lanes is needed; a lane
+//    holds up to 8 states (two lanes per channel at N = 16: at 16 the grid of
+//    the benchmark shape had too few CTAs to hide latency).  The per-step
+//    scalars (Delta, Delta u, g) are computed once per (channel, step) into
+//    shared memory.
 // ---------------------------------------------------------------------------
 template <int N>
 struct BwdSumShape {
-    static constexpr int S = N < 16 ? N : 16;   // states per lane
+    static constexpr int S = N < 8 ? N : 8;     // states per lane
     static constexpr int LN = N / S;            // lanes per channel
     static constexpr int CH = kBwdWarps * 32 / LN;
     static constexpr int P = S / 2;             // state pairs per lane
@@ -623,8 +624,9 @@ scan_bwd_kernel(const BwdParams p) {
         __syncthreads();
 
         // Recompute the tile's states from its checkpoint: hist[t] = state
-        // before step t.  The ungated output s_t gives dz_t = dy_t s_t silu'(z_t).
+        // before step t; ys[t] = the ungated output s_t.
         float2 hist[TT][P2];
+        float ys[TT];
         float2 hh[P2];
         {
             const float4 c4 = ckpt[i][threadIdx.x];
@@ -642,8 +644,7 @@ scan_bwd_kernel(const BwdParams p) {
                 hh[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), hh[k], __fmul2_rn(f2(q.y), f2(bq.x, bq.y)));
                 y2 = __ffma2_rn(f2(bq.z, bq.w), hh[k], y2);
             }
-            const float ys = fmaf(dsk, q.w, lane_sum<LN>(y2.x + y2.y));
-            if (l.j == 2 % LN) outs[2][l.r][t] = sc2[t][l.r].y * ys;
+            ys[t] = fmaf(dsk, q.w, lane_sum<LN>(y2.x + y2.y));
         }
 
         // The adjoint, backwards over the tile.
@@ -680,6 +681,7 @@ scan_bwd_kernel(const BwdParams p) {
             db_acc += ddv;
             if (l.j == 0 % LN) outs[0][l.r][t] = duv;
             if (l.j == 1 % LN) outs[1][l.r][t] = ddv;
+            if (l.j == 2 % LN) outs[2][l.r][t] = q2.y * ys[t];  // dz_t = dy_t s_t silu'(z_t)
 
             // dB, dC: sum over the warp's channels, then stage per warp.
             xchan_reduce<16, LN, Sh::NV>(vals, l.lane);
