@@ -170,20 +170,26 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS, "sm_max_mhz": 2032.0}, "fallback"
 
 
-def kernel_source_hash():
+# Device sources of the chunked forward call's kernels (summary, carry and
+# fused passes): a DRAM-traffic record stays valid while these and the launch
+# plan are unchanged.
+FWD_SCAN_SOURCES = ("scan_tma.cuh", "tma.cuh", "ssm_device.cuh")
+
+
+def kernel_source_hash(names=FWD_SCAN_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_109_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name in names:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key: str):
+def ncu_traffic(kernel_key: str, plan=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current kernel sources and launch plan; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -191,6 +197,8 @@ def ncu_traffic(kernel_key: str):
     except (OSError, ValueError):
         return None
     if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    if plan is not None and rec.get("plan") != plan:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -637,7 +645,7 @@ def run_ours(args):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     alu_peak = sms * sm_max * 1e6 * UPDATES_PER_SM_CLK / 1e9  # Gupd/s
     alu_achieved = r["upd_per_step"] / per_launch_s / 1e9
-    traffic = ncu_traffic("scan_chunked_call/" + HEADLINE)
+    traffic = ncu_traffic("scan_chunked_call/" + HEADLINE, r["plan"])
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -831,6 +839,10 @@ def write_traffic(csv_path, workload):
     for (_, name), b in launches.items():
         per_kernel.setdefault(name, []).append(b)
     kernels = {k: sum(v) / len(v) for k, v in per_kernel.items()}
+    from selective_state_space_109_b300 import inputs as I
+    from selective_state_space_109_b300 import ssm
+    w = I.WORKLOADS[workload]
+    plan = ssm.scan_plan(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], I.io_torch_dtype(w["io"]))
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -841,6 +853,7 @@ def write_traffic(csv_path, workload):
         "dram_bytes_per_launch": round(sum(kernels.values())),
         "kernels": {k: round(v) for k, v in kernels.items()},
         "source_hash": kernel_source_hash(),
+        "plan": plan,
         "from": os.path.basename(csv_path)}
     with open(path, "w") as f:
         json.dump(data, f, indent=1, sort_keys=True)
