@@ -135,3 +135,39 @@ def test_bwd_matches_finite_difference_of_the_kernel(ssm):
     fd = (loss(eps) - loss(-eps)) / (2 * eps)
     an = sum(float((gr[k].double() * dirs[n].double()).sum()) for n, k in zip(names, keys))
     assert abs(fd - an) <= 2e-3 * max(1.0, abs(an)), (fd, an)
+
+
+def channel_slice_bwd(x, dy, d):
+    """The oracle's backward for channel d over every batch row (B, C shared by
+    the single group): per-channel outputs and the channel's dA, dD, ddt_bias.
+    Only the channel's rows are copied to the host."""
+    sl = lambda t: None if t is None else to_np(t[:, d:d + 1])
+    return oracle.scan_bwd(sl(x.u), sl(x.delta), to_np(x.A[d:d + 1]), to_np(x.B), to_np(x.C), sl(dy), z=sl(x.z),
+                           Dskip=to_np(x.D[d:d + 1]), dt_bias=to_np(x.dt_bias[d:d + 1]), h0=sl(x.h0))
+
+
+@pytest.mark.parametrize("name", ["scan_bf16_b8_d2048_l4096", "scan_bf16_b1_d5120_l65536_final_state"])
+def test_bwd_full_size_sampled_channels(ssm, name):
+    """The larger scan shapes at full size (the long one: 1024 time chunks):
+    every output of 6 sampled channels (all batch rows), and the channel
+    sums dA, dD, ddt_bias of those channels, against the oracle run on the
+    channel alone."""
+    w = I.WORKLOADS[name]
+    x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], 1, io="bf16", recipe=w["recipe"],
+                           seed=2, device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(3)
+    dy = torch.randn((w["batch"], w["dim"], w["seqlen"]), generator=g).to(torch.bfloat16).cuda()
+    got = ssm.scan_bwd(x.u, x.delta, x.A, x.B, x.C, dy, z=x.z, D=x.D, dt_bias=x.dt_bias)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(4)
+    chans = sorted({0, w["dim"] - 1, *[int(v) for v in rng.integers(0, w["dim"], 4)]})
+    for d in chans:
+        ref = channel_slice_bwd(x, dy, d)
+        for k in ("du", "ddelta", "dz"):
+            e = rel_l2(to_np(got[k][:, d]), ref[k][:, 0])
+            assert e <= TOL["bf16"][0], f"{name} d={d} {k}: rel_l2={e:.3e}"
+        for k in ("dA", "dD", "ddt_bias", "dh0"):
+            gk = to_np(got[k])[d] if k != "dh0" else to_np(got[k])[:, d]
+            rk = ref[k][0] if k != "dh0" else ref[k][:, 0]
+            e = rel_l2(gk, rk)
+            assert e <= TOL["bf16"][1], f"{name} d={d} {k}: rel_l2={e:.3e}"

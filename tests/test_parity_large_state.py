@@ -80,3 +80,16 @@ def test_decode_large_state(ssm, io, N):
                                         dt_bias=to_np(prm["dt_bias"]))
     assert_close(to_np(y), ref_y, io, f"decode N={N} io={io}")
     assert rel_l2(to_np(state), ref_st) <= STATE_REL_L2
+
+
+def test_n64_full_size_bf16_b2_d1536_l2048(ssm):
+    """The benchmark's N = 64 shape in full (its own launch plan), every output."""
+    w = I.WORKLOADS["scan_bf16_b2_d1536_l2048_n64"]
+    x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], 1, io="bf16", recipe=w["recipe"],
+                           seed=0, device="cuda")
+    y, hf = chunked(ssm, x)
+    torch.cuda.synchronize()
+    ref_y, ref_h = oracle_scan(x, final_state=True)
+    e = assert_close(to_np(y), ref_y, "bf16", "N=64 b2 d1536 L2048")
+    assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
+    print(f"N=64 full-size rel_l2 = {e:.3e}")
