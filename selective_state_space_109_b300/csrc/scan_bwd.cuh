@@ -196,7 +196,7 @@ struct BwdShape {
     static constexpr int P2 = S / 2;          // state pairs per lane
     static constexpr int NV = 2 * S;          // dB, dC values per lane and step
     static constexpr int CF = NV / CPW > 1 ? NV / CPW : 1;  // values left per lane after the channel sum
-    static_assert(N % S == 0 && LN >= 1 && LN <= 16, "N in {4, 8, 16, 32, 64}");
+    static_assert(N % S == 0 && LN >= 1 && LN <= 32, "N in {4, 8, 16, 32, 64, 128}");
 };
 
 // Channel (b, d) and chunk of this thread; inactive lanes (past the group's

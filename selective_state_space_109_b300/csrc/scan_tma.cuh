@@ -114,29 +114,33 @@ struct TmaScanLayout {
     static_assert(ACT_BYTES % (8 * TileShape<T>::kRowBytes) == 0, "activation tiles must keep the swizzle phase");
 };
 
-// Loads H consecutive elements (H * sizeof(T) = 4, 8 or 16 bytes) from shared memory.
+// Loads H consecutive elements (H * sizeof(T) = 2, 4, 8 or 16 bytes) from shared memory.
 template <typename T, int H>
 __device__ __forceinline__ void lds_row(const unsigned char* p, float (&f)[H]) {
     constexpr int BYTES = H * static_cast<int>(sizeof(T));
-    uint32_t w[BYTES / 4];
-    if constexpr (BYTES == 16) {
-        const uint4 v = *reinterpret_cast<const uint4*>(p);
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-    } else if constexpr (BYTES == 8) {
-        const uint2 v = *reinterpret_cast<const uint2*>(p);
-        w[0] = v.x; w[1] = v.y;
+    if constexpr (BYTES == 2) {
+        f[0] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
     } else {
-        static_assert(BYTES == 4, "4, 8 or 16 bytes");
-        w[0] = *reinterpret_cast<const uint32_t*>(p);
-    }
-    if constexpr (sizeof(T) == 4) {
+        uint32_t w[BYTES / 4];
+        if constexpr (BYTES == 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        } else if constexpr (BYTES == 8) {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            w[0] = v.x; w[1] = v.y;
+        } else {
+            static_assert(BYTES == 4, "2, 4, 8 or 16 bytes");
+            w[0] = *reinterpret_cast<const uint32_t*>(p);
+        }
+        if constexpr (sizeof(T) == 4) {
 #pragma unroll
-        for (int k = 0; k < H; ++k) f[k] = __uint_as_float(w[k]);
-    } else {
+            for (int k = 0; k < H; ++k) f[k] = __uint_as_float(w[k]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < BYTES / 4; ++k) {
-            f[2 * k] = __uint_as_float(w[k] << 16);
-            f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+            for (int k = 0; k < BYTES / 4; ++k) {
+                f[2 * k] = __uint_as_float(w[k] << 16);
+                f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+            }
         }
     }
 }
@@ -145,23 +149,28 @@ __device__ __forceinline__ void lds_row(const unsigned char* p, float (&f)[H]) {
 template <typename T, int H>
 __device__ __forceinline__ void sts_row(unsigned char* p, const float (&f)[H]) {
     constexpr int BYTES = H * static_cast<int>(sizeof(T));
-    uint32_t w[BYTES / 4];
-    if constexpr (sizeof(T) == 4) {
-#pragma unroll
-        for (int k = 0; k < H; ++k) w[k] = __float_as_uint(f[k]);
+    if constexpr (BYTES == 2) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(f[0]);
+        *reinterpret_cast<unsigned short*>(p) = *reinterpret_cast<const unsigned short*>(&h);
     } else {
+        uint32_t w[BYTES / 4];
+        if constexpr (sizeof(T) == 4) {
 #pragma unroll
-        for (int k = 0; k < BYTES / 4; ++k) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
-            w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int k = 0; k < H; ++k) w[k] = __float_as_uint(f[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < BYTES / 4; ++k) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+                w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
         }
-    }
-    if constexpr (BYTES == 16) {
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else if constexpr (BYTES == 8) {
-        *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
-    } else {
-        *reinterpret_cast<uint32_t*>(p) = w[0];
+        if constexpr (BYTES == 16) {
+            *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else if constexpr (BYTES == 8) {
+            *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        } else {
+            *reinterpret_cast<uint32_t*>(p) = w[0];
+        }
     }
 }
 
@@ -203,7 +212,10 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     constexpr int P = S / 2;           // fp32x2 state pairs per lane
     constexpr int NQ = N / 2;          // state pairs per step
     constexpr int NQP = Lay::BCF_ROW;  // widened row stride (pairs)
-    constexpr int H = VPC / LANES;     // steps per lane per 16-byte chunk
+    // Steps a lane owns per 16-byte chunk.  With more lanes than steps
+    // (N = 128: 8 lanes of 16 states), lanes j >= VPC own none.
+    constexpr int H = VPC >= LANES ? VPC / LANES : 1;
+    constexpr bool SPARE = LANES > VPC;
     // Per-step scalar work (softplus, Delta u, gate) in fp32x2 pairs of steps.
     constexpr bool PACKED = !ACCURATE && (H % 2 == 0);
     constexpr int CH = Lay::CH;
@@ -223,6 +235,8 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int r = warp * (32 / LANES) + lane / LANES;  // channel row within the CTA
     const int j = lane % LANES;                        // sub-lane within the channel
+    const int jj = SPARE ? j % VPC : j;                // its step slot in a chunk
+    const bool own = !SPARE || j < VPC;                // it owns steps
     const int cw = lane / LANES;                       // channel within the warp
     unsigned char* xs_warp = smem + Lay::XS_OFFSET + warp * 2 * Lay::XS_BUF;
 
@@ -357,7 +371,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         // (Abar = 1, no input: the state passes through unchanged).
         auto run_chunk = [&](const int c, auto masked) {
             constexpr bool MASKED = decltype(masked)::value;
-            const uint32_t off = swz_act(r, c) + j * H * static_cast<int>(sizeof(T));
+            const uint32_t off = swz_act(r, c) + jj * H * static_cast<int>(sizeof(T));
             float uu[H], dt[H], du[H];
             {
                 float dv[H];
@@ -369,7 +383,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                         const float2 v = __fadd2_rn(make_float2(dv[k], dv[k + 1]), make_float2(bias, bias));
                         float2 d2 = softplus2_fast(v);
                         if constexpr (MASKED) {
-                            const int t = t0 + c * VPC + j * H + k;
+                            const int t = t0 + c * VPC + jj * H + k;
                             if (t >= p.seqlen) d2.x = 0.f;
                             if (t + 1 >= p.seqlen) d2.y = 0.f;
                         }
@@ -382,7 +396,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                     for (int k = 0; k < H; ++k) {
                         dt[k] = softplus<ACCURATE>(dv[k] + bias);
                         if constexpr (MASKED) {
-                            if (t0 + c * VPC + j * H + k >= p.seqlen) dt[k] = 0.f;
+                            if (t0 + c * VPC + jj * H + k >= p.seqlen) dt[k] = 0.f;
                         }
                         du[k] = dt[k] * uu[k];
                     }
@@ -393,8 +407,10 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             [[maybe_unused]] float4* xrow = nullptr;
             if constexpr (LANES > 1) {
                 xrow = reinterpret_cast<float4*>(xs_warp + (c & 1) * Lay::XS_BUF + cw * Lay::XS_STRIDE);
+                if (own) {
 #pragma unroll
-                for (int k = 0; k < H; ++k) xrow[j * H + k] = make_float4(dt[k], dt[k], du[k], du[k]);
+                    for (int k = 0; k < H; ++k) xrow[jj * H + k] = make_float4(dt[k], dt[k], du[k], du[k]);
+                }
                 __syncwarp();
             }
 
@@ -449,7 +465,18 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             }
 
             if constexpr (FULL) {
-                reduce_scatter<LANES, H>(acc, j);
+                if constexpr (SPARE) {
+                    // Sum over the lane bits above the chunk's steps, then a
+                    // reduce-scatter over the owners' bits.
+#pragma unroll
+                    for (int m = LANES / 2; m >= VPC; m >>= 1) {
+#pragma unroll
+                        for (int kk = 0; kk < VPC; ++kk) acc[kk] += __shfl_xor_sync(0xffffffffu, acc[kk], m);
+                    }
+                    reduce_scatter<VPC, 1>(acc, j);
+                } else {
+                    reduce_scatter<LANES, H>(acc, j);
+                }
                 float zz[H];
                 if (has_z) lds_row<T, H>(z_t + off, zz);
                 float out[H];
@@ -469,7 +496,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                         out[k] = yv;
                     }
                 }
-                sts_row<T, H>(u_t + off, out);  // y in place of u
+                if (own) sts_row<T, H>(u_t + off, out);  // y in place of u
             }
         };
 

@@ -35,7 +35,11 @@ ssm_status_t cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool supported_dstate(int n) { return n == 4 || n == 8 || n == 16 || n == 32 || n == 64; }
+bool supported_dstate(int n) { return n == 4 || n == 8 || n == 16 || n == 32 || n == 64 || n == 128; }
+
+// N = 128 runs on the TMA-staged kernel only (8 lanes of 16 states): rows must
+// be whole 16-byte packets.
+bool dstate_needs_tma(int n) { return n > 64; }
 
 // Lanes that may share one channel's N states: each lane keeps an even number
 // of them, at most 16 (the register budget of the update loop).
@@ -57,6 +61,8 @@ ssm_status_t check_scan_args(const void* u, const void* delta, const void* z, co
     if (dim % ngroups != 0) return SSM_ERR_INVALID_ARG;
     if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
     if (!supported_dstate(dstate)) return SSM_ERR_UNSUPPORTED;
+    if (dstate_needs_tma(dstate) && (static_cast<long long>(seqlen) * (io == SSM_F32 ? 4 : 2)) % 16 != 0)
+        return SSM_ERR_UNSUPPORTED;
     if (batch == 0) return SSM_OK;
     if (!A) return SSM_ERR_INVALID_ARG;
     if (seqlen > 0 && (!u || !delta || !B || !C || !y)) return SSM_ERR_INVALID_ARG;
@@ -175,7 +181,8 @@ int tma_smem_bytes(int lanes) {
     switch (lanes) {
         case 1: return ssm::TmaScanLayout<T, N, L1, kTmaWarps, MODE>::SMEM_BYTES;
         case 2: return ssm::TmaScanLayout<T, N, (N <= 32 ? 2 : L1), kTmaWarps, MODE>::SMEM_BYTES;
-        default: return ssm::TmaScanLayout<T, N, (N >= 8 ? 4 : 2), kTmaWarps, MODE>::SMEM_BYTES;
+        case 8: return ssm::TmaScanLayout<T, N, (N >= 128 ? 8 : L1), kTmaWarps, MODE>::SMEM_BYTES;
+        default: return ssm::TmaScanLayout<T, N, (N >= 8 ? (N <= 64 ? 4 : L1) : 2), kTmaWarps, MODE>::SMEM_BYTES;
     }
 }
 
@@ -184,11 +191,13 @@ int tma_smem_for(ssm_dtype_t io, int dstate, int lanes) {
     if (io == SSM_F32) {
         if (dstate == 32) return tma_smem_bytes<float, 32, MODE>(lanes);
         if (dstate == 64) return tma_smem_bytes<float, 64, MODE>(lanes);
+        if (dstate == 128) return tma_smem_bytes<float, 128, MODE>(lanes);
         return dstate == 4 ? tma_smem_bytes<float, 4, MODE>(lanes)
                            : dstate == 8 ? tma_smem_bytes<float, 8, MODE>(lanes) : tma_smem_bytes<float, 16, MODE>(lanes);
     }
     if (dstate == 32) return tma_smem_bytes<__nv_bfloat16, 32, MODE>(lanes);
     if (dstate == 64) return tma_smem_bytes<__nv_bfloat16, 64, MODE>(lanes);
+    if (dstate == 128) return tma_smem_bytes<__nv_bfloat16, 128, MODE>(lanes);
     return dstate == 4 ? tma_smem_bytes<__nv_bfloat16, 4, MODE>(lanes)
                        : dstate == 8 ? tma_smem_bytes<__nv_bfloat16, 8, MODE>(lanes)
                                      : tma_smem_bytes<__nv_bfloat16, 16, MODE>(lanes);
@@ -239,7 +248,7 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
                    int chunk_cap) {
     const int dpg = dim / ngroups;
     const int kmax = std::max(1, std::min(chunk_cap, max_chunks_for(seqlen, io)));
-    const int lmax = dstate >= 8 ? 4 : 2;
+    const int lmax = dstate >= 128 ? 8 : (dstate >= 8 ? 4 : 2);
     const int lmin = min_lanes_for(dstate);
     // Time units: ~0.54 ns of an SM each on B300 (one step of a CTA of
     // 16-state lanes is 128 units).
@@ -383,7 +392,8 @@ cudaError_t launch_tma_lanes(const ScanMaps& m, const ssm::TmaScanParams& p, int
     switch (lanes) {
         case 1: if constexpr (N <= 16) return launch_tma<T, N, 1, MODE>(m, p, grid_y, st); break;
         case 2: if constexpr (N <= 32) return launch_tma<T, N, 2, MODE>(m, p, grid_y, st); break;
-        case 4: if constexpr (N >= 8) return launch_tma<T, N, 4, MODE>(m, p, grid_y, st); break;
+        case 4: if constexpr (N >= 8 && N <= 64) return launch_tma<T, N, 4, MODE>(m, p, grid_y, st); break;
+        case 8: if constexpr (N >= 128) return launch_tma<T, N, 8, MODE>(m, p, grid_y, st); break;
         default: break;
     }
     return cudaErrorInvalidValue;
@@ -398,6 +408,7 @@ cudaError_t launch_tma_n(const ScanMaps& m, const ssm::TmaScanParams& p, int dst
         case 16: return launch_tma_lanes<T, 16, MODE>(m, p, lanes, grid_y, st);
         case 32: return launch_tma_lanes<T, 32, MODE>(m, p, lanes, grid_y, st);
         case 64: return launch_tma_lanes<T, 64, MODE>(m, p, lanes, grid_y, st);
+        case 128: return launch_tma_lanes<T, 128, MODE>(m, p, lanes, grid_y, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -466,6 +477,7 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
         else if (dstate == 8) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<8, kMaxChunks>, agg, h0, BD, plan.chunks);
         else if (dstate == 32) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<32, kMaxChunks>, agg, h0, BD, plan.chunks);
         else if (dstate == 64) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<64, kMaxChunks>, agg, h0, BD, plan.chunks);
+        else if (dstate == 128) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<128, kMaxChunks>, agg, h0, BD, plan.chunks);
         else e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<16, kMaxChunks>, agg, h0, BD, plan.chunks);
         if (e != cudaSuccess) return cuda_fail(e);
     }
@@ -607,7 +619,7 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
         }
         return SSM_OK;
     }
-    if (tma_eligible(seqlen, io) && !force_generic()) {
+    if (tma_eligible(seqlen, io) && (!force_generic() || dstate_needs_tma(dstate))) {
         const bool chunks_ok = workspace != nullptr;
         const int cap = chunks_ok ? chunks_fitting(workspace_bytes, batch, dim, dstate) : 1;
         const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, cap);
@@ -776,6 +788,7 @@ cudaError_t launch_bwd_t(const ssm::BwdParams& p, int dstate, cudaStream_t st) {
         case 8: return launch_bwd_n<T, 8>(p, st);
         case 32: return launch_bwd_n<T, 32>(p, st);
         case 64: return launch_bwd_n<T, 64>(p, st);
+        case 128: return launch_bwd_n<T, 128>(p, st);
         default: return launch_bwd_n<T, 16>(p, st);
     }
 }
@@ -879,7 +892,8 @@ ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngrou
         *kernels = (batch > 0 && chunked) ? 1 : 0;  // h_final copy for an empty sequence
         return SSM_OK;
     }
-    if (tma_eligible(seqlen, io) && !force_generic()) {
+    if (dstate_needs_tma(dstate) && !tma_eligible(seqlen, io)) return SSM_ERR_UNSUPPORTED;
+    if (tma_eligible(seqlen, io) && (!force_generic() || dstate_needs_tma(dstate))) {
         const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunked != 0 ? kMaxChunks : 1);
         *lanes = plan.lanes; *chunks = plan.chunks; *kernels = plan.chunks > 1 ? 3 : 1; *staged = 1;
     } else {
@@ -1041,12 +1055,14 @@ ssm_status_t ssm_state_update_pooled(float* state_pool, const int* state_indices
         else if (dstate == 8) SSM_DECODE_LAUNCH(float, 8, true);
         else if (dstate == 32) SSM_DECODE_LAUNCH(float, 32, true);
         else if (dstate == 64) SSM_DECODE_LAUNCH(float, 64, true);
+        else if (dstate == 128) SSM_DECODE_LAUNCH(float, 128, true);
         else SSM_DECODE_LAUNCH(float, 16, true);
     } else {
         if (dstate == 4) SSM_DECODE_LAUNCH(__nv_bfloat16, 4, false);
         else if (dstate == 8) SSM_DECODE_LAUNCH(__nv_bfloat16, 8, false);
         else if (dstate == 32) SSM_DECODE_LAUNCH(__nv_bfloat16, 32, false);
         else if (dstate == 64) SSM_DECODE_LAUNCH(__nv_bfloat16, 64, false);
+        else if (dstate == 128) SSM_DECODE_LAUNCH(__nv_bfloat16, 128, false);
         else SSM_DECODE_LAUNCH(__nv_bfloat16, 16, false);
     }
 #undef SSM_DECODE_LAUNCH
@@ -1068,6 +1084,7 @@ ssm_status_t ssm_scan_fwd_varlen(const void* u, const void* delta, const void* z
                                  const void* C, const float* Dskip, const float* dt_bias, const float* h0,
                                  const int* cu_seqlens, void* y, float* h_final, int dim, int dstate, int total,
                                  int ngroups, int nseq, ssm_dtype_t io, void* stream) {
+    if (dstate_needs_tma(dstate)) return SSM_ERR_UNSUPPORTED;  // the packed scan runs on the generic kernel
     const ssm_status_t s = check_scan_args(u, delta, z, A, B, C, Dskip, dt_bias, y, h0, h_final, 1, dim, dstate,
                                            total, ngroups, io);
     if (s != SSM_OK) return s;

@@ -38,7 +38,8 @@ __global__ void __launch_bounds__(128)
 state_update_kernel(const DecodeParams p) {
     constexpr int SPL = 4;          // states per lane
     constexpr int QL = N / SPL;     // lanes per (b, d)
-    static_assert(N % SPL == 0 && (QL == 1 || QL == 2 || QL == 4 || QL == 8 || QL == 16), "N in {4, ..., 64}");
+    static_assert(N % SPL == 0 && (QL == 1 || QL == 2 || QL == 4 || QL == 8 || QL == 16 || QL == 32),
+                  "N in {4, ..., 128}");
 
     const int gx = blockIdx.x * blockDim.x + threadIdx.x;
     const int d = gx / QL;

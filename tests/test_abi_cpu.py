@@ -69,7 +69,8 @@ def test_scan_argument_errors(lib):
     assert scan(lib, L=-5) == 1
     assert scan(lib, dim=6, G=4) == 1          # dim % ngroups
     assert scan(lib, N=12) == 2                # unsupported state size
-    assert scan(lib, N=128) == 2               # N up to 64
+    assert scan(lib, N=256) == 2               # N up to 128
+    assert scan(lib, N=128, L=9) == 2          # N = 128 needs rows of whole 16-byte packets
     assert scan(lib, io=7) == 2
     assert scan(lib, B=MIS) == 3               # misaligned
     assert scan(lib, z=MIS) == 3
@@ -147,6 +148,7 @@ def test_varlen_and_pooled_argument_errors(lib):
     assert varlen(cu=None) == 1
     assert varlen(cu=MIS) == 3
     assert varlen(N=12) == 2
+    assert varlen(N=128) == 2                 # the packed scan stops at N = 64
     assert varlen(dim=6, G=4) == 1
 
     def pooled(idx=None, nslots=2, batch=2):
@@ -176,7 +178,7 @@ def test_bwd_argument_errors(lib):
     assert bwd(du=P) == 1                          # du aliases u
     assert bwd(dim=6, G=4) == 1
     assert bwd(N=12) == 2
-    assert bwd(N=128) == 2
+    assert bwd(N=256) == 2
     assert bwd(io=9) == 2
     assert bwd(dy=MIS) == 3
     assert bwd(dh0=MIS) == 3

@@ -1,7 +1,8 @@
-"""GPU parity of the scan and decode step with large state sizes (N = 32 and
-64, several lanes sharing one channel's states) against the fp64 oracle: the
-TMA-staged path single pass and time-chunked, the generic path, the packed
-variable-length scan and the decode step."""
+"""GPU parity of the scan and decode step with large state sizes (N = 32, 64
+and 128, several lanes sharing one channel's states) against the fp64 oracle:
+the TMA-staged path single pass and time-chunked, the generic path, the packed
+variable-length scan and the decode step.  N = 128 (8 lanes of 16 states, more
+lanes than the steps of a 16-byte fp32 chunk) runs on the staged path only."""
 import numpy as np
 import pytest
 import torch
@@ -24,7 +25,7 @@ def chunked(ssm, x, h0=None):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [32, 64])
+@pytest.mark.parametrize("N", [32, 64, 128])
 @pytest.mark.parametrize("chunks", [1, 3])
 def test_staged_large_state(ssm, monkeypatch, io, N, chunks):
     monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
@@ -66,7 +67,7 @@ def test_varlen_large_state(ssm, io, N):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [32, 64])
+@pytest.mark.parametrize("N", [32, 64, 128])
 def test_decode_large_state(ssm, io, N):
     prm = I.decode_params(200, N, device="cuda")
     state = I.make_decode_state(5, 200, N, seed=3, device="cuda")
@@ -93,3 +94,20 @@ def test_n64_full_size_bf16_b2_d1536_l2048(ssm):
     e = assert_close(to_np(y), ref_y, "bf16", "N=64 b2 d1536 L2048")
     assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
     print(f"N=64 full-size rel_l2 = {e:.3e}")
+
+
+def test_n128_single_pass_and_unsupported_forms(ssm):
+    """N = 128 through the entry point without a workspace (one pass), and the
+    forms it does not take: rows that are not whole 16-byte packets, and the
+    packed scan."""
+    x = I.make_scan_inputs(2, 48, 128, 96, 1, io="bf16", recipe="scaled", seed=7, device="cuda")
+    y = ssm.scan_fwd(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias)
+    torch.cuda.synchronize()
+    assert_close(to_np(y), oracle_scan(x), "bf16", "N=128 single pass")
+    odd = I.make_scan_inputs(1, 16, 128, 37, 1, io="bf16", recipe="scaled", seed=8, device="cuda")
+    with pytest.raises(ssm.SsmError):
+        ssm.scan_fwd(odd.u, odd.delta, odd.A, odd.B, odd.C, z=odd.z, D=odd.D, dt_bias=odd.dt_bias)
+    v = I.make_varlen_inputs(16, 128, [5, 11], io="bf16", seed=9, device="cuda", row_multiple=8)
+    with pytest.raises(ssm.SsmError):
+        ssm.scan_fwd_varlen(v["u"], v["delta"], v["A"], v["B"], v["C"], v["cu_seqlens"], z=v["z"], D=v["D"],
+                            dt_bias=v["dt_bias"])
