@@ -622,7 +622,8 @@ def run_ours(args):
     extra = {}
     if not args.skip_extra and world == 1:
         for name in ("scan_bf16_b8_d2048_l4096", "scan_bf16_b1_d5120_l65536_final_state",
-                     "scan_bf16_b2_d1536_l2048_n64", "scan_bf16_b2_d1536_l2048_n128"):
+                     "scan_bf16_b2_d1536_l2048_n64", "scan_bf16_b2_d1536_l2048_n128",
+                     "scan_bf16_b2_d1536_l2048_n256"):
             wx = I.WORKLOADS[name]
             rx = bench_scan_device(ssm, I, torch, wx, max(4, min(args.steps, 40)), 3, preroll_s=0.0)
             extra[name] = dict(GBps=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3) / 1e9, 1),

@@ -44,8 +44,8 @@
  * - stream is a cudaStream_t (NULL = legacy default stream).  Every call is
  *   asynchronous on that stream; argument errors are returned before anything
  *   is enqueued.
- * - Supported dstate: 4, 8, 16, 32, 64, 128 (others return SSM_ERR_UNSUPPORTED).
- *   dstate 128 runs on the TMA-staged kernels only: the scans take it when
+ * - Supported dstate: 4, 8, 16, 32, 64, 128, 256 (others return SSM_ERR_UNSUPPORTED).
+ *   dstate 128 and 256 run on the TMA-staged kernels only: the scans take them when
  *   seqlen * element size is a multiple of 16 bytes (SSM_ERR_UNSUPPORTED
  *   otherwise), ssm_scan_fwd_varlen not at all.
  * - batch == 0 is an empty problem: the call returns SSM_OK without touching
@@ -66,7 +66,7 @@ extern "C" {
 typedef enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = 1,        /* null required pointer, bad size, dim % ngroups != 0 */
-    SSM_ERR_UNSUPPORTED = 2,        /* dstate not in {4, 8, 16, 32, 64, 128}, unknown io type */
+    SSM_ERR_UNSUPPORTED = 2,        /* dstate not in {4, 8, ..., 256}, unknown io type */
     SSM_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
     SSM_ERR_WORKSPACE_TOO_SMALL = 4,/* workspace_bytes below the size query's answer */
     SSM_ERR_TIMEOUT = 5,            /* a bounded device-side wait gave up (see ssm_workspace_status) */

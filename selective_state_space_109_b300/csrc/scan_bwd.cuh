@@ -31,7 +31,8 @@
 //      its checkpoint, and the adjoint runs back over the tile, producing every
 //      gradient of the tile's steps.
 //
-// Lanes: LN = N/4 consecutive lanes share a channel, 4 states each.  The
+// Lanes: LN = N/S consecutive lanes share a channel, S = 4 states each (8 at
+// N = 256).  The
 // per-step sums over states (the readout, du, dDelta) are butterfly-reduced
 // over the LN lanes; dB and dC sum over the channels of the group: a
 // reduce-scatter over the channels of a warp, a sum over the CTA's warps in
@@ -47,7 +48,9 @@ namespace ssm {
 
 constexpr int kBwdTT = 8;       // steps per tile
 constexpr int kBwdWarps = 4;
-constexpr int kBwdStates = 4;   // states per lane
+// States per lane of the main pass: 4 (N/4 lanes a channel), 8 at N = 256 so
+// that a channel stays within a warp.
+__host__ __device__ constexpr int bwd_states_per_lane(int n) { return n > 128 ? 8 : 4; }
 
 // Tiles per time chunk: their start states are held in shared memory (16 KB
 // per 8 tiles); fewer at N = 64, whose dB/dC staging is larger.
@@ -188,7 +191,7 @@ __device__ __forceinline__ int xchan_first_id(int lane, bool& writer) {
 
 template <int N>
 struct BwdShape {
-    static constexpr int S = kBwdStates;
+    static constexpr int S = bwd_states_per_lane(N);
     static constexpr int LN = N / S;          // lanes per channel
     static constexpr int CPW = 32 / LN;       // channels per warp
     static constexpr int CH = kBwdWarps * CPW;
@@ -196,7 +199,7 @@ struct BwdShape {
     static constexpr int P2 = S / 2;          // state pairs per lane
     static constexpr int NV = 2 * S;          // dB, dC values per lane and step
     static constexpr int CF = NV / CPW > 1 ? NV / CPW : 1;  // values left per lane after the channel sum
-    static_assert(N % S == 0 && LN >= 1 && LN <= 32, "N in {4, 8, 16, 32, 64, 128}");
+    static_assert(N % S == 0 && LN >= 1 && LN <= 32, "N in {4, 8, 16, 32, 64, 128, 256}");
 };
 
 // Channel (b, d) and chunk of this thread; inactive lanes (past the group's
@@ -455,8 +458,8 @@ struct BwdLayout {
     using Sh = BwdShape<N>;
     static constexpr int TT = kBwdTT;
     static constexpr int THREADS = kBwdWarps * 32;
-    static constexpr int CKPT = 0;                                                  // float4 [tiles][THREADS]
-    static constexpr int ACT = CKPT + bwd_chunk_tiles(N) * THREADS * 16;           // T [2][4][CH][TT]
+    static constexpr int CKPT = 0;                                                  // float4 [tiles * S/4][THREADS]
+    static constexpr int ACT = CKPT + bwd_chunk_tiles(N) * (Sh::S / 4) * THREADS * 16;  // T [2][4][CH][TT]
     static constexpr int BC = ACT + 2 * 4 * Sh::CH * TT * static_cast<int>(sizeof(T));  // T [2][2][N][TT]
     static constexpr int SC = BC + 2 * 2 * N * TT * static_cast<int>(sizeof(T));   // float4 [TT][CH]
     static constexpr int SC2 = SC + TT * Sh::CH * 16;                               // float2 [TT][CH]
@@ -588,7 +591,9 @@ scan_bwd_kernel(const BwdParams p) {
         __syncthreads();
         prepare(s0 + i * TT, buf, false);
         __syncthreads();
-        ckpt[i][threadIdx.x] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+#pragma unroll
+        for (int v = 0; v < S / 4; ++v)
+            ckpt[i * (S / 4) + v][threadIdx.x] = make_float4(h[2 * v].x, h[2 * v].y, h[2 * v + 1].x, h[2 * v + 1].y);
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
             const float4 q = sc[t][l.r];
@@ -628,10 +633,11 @@ scan_bwd_kernel(const BwdParams p) {
         float2 hist[TT][P2];
         float ys[TT];
         float2 hh[P2];
-        {
-            const float4 c4 = ckpt[i][threadIdx.x];
-            hh[0] = f2(c4.x, c4.y);
-            hh[1] = f2(c4.z, c4.w);
+#pragma unroll
+        for (int v = 0; v < S / 4; ++v) {
+            const float4 c4 = ckpt[i * (S / 4) + v][threadIdx.x];
+            hh[2 * v] = f2(c4.x, c4.y);
+            hh[2 * v + 1] = f2(c4.z, c4.w);
         }
 #pragma unroll
         for (int t = 0; t < TT; ++t) {

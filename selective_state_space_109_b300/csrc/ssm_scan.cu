@@ -35,10 +35,10 @@ ssm_status_t cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool supported_dstate(int n) { return n == 4 || n == 8 || n == 16 || n == 32 || n == 64 || n == 128; }
+bool supported_dstate(int n) { return n == 4 || n == 8 || n == 16 || n == 32 || n == 64 || n == 128 || n == 256; }
 
-// N = 128 runs on the TMA-staged kernel only (8 lanes of 16 states): rows must
-// be whole 16-byte packets.
+// N = 128 and 256 run on the TMA-staged kernel only (8 or 16 lanes of 16
+// states): rows must be whole 16-byte packets.
 bool dstate_needs_tma(int n) { return n > 64; }
 
 // Lanes that may share one channel's N states: each lane keeps an even number
@@ -181,7 +181,8 @@ int tma_smem_bytes(int lanes) {
     switch (lanes) {
         case 1: return ssm::TmaScanLayout<T, N, L1, kTmaWarps, MODE>::SMEM_BYTES;
         case 2: return ssm::TmaScanLayout<T, N, (N <= 32 ? 2 : L1), kTmaWarps, MODE>::SMEM_BYTES;
-        case 8: return ssm::TmaScanLayout<T, N, (N >= 128 ? 8 : L1), kTmaWarps, MODE>::SMEM_BYTES;
+        case 8: return ssm::TmaScanLayout<T, N, (N == 128 ? 8 : L1), kTmaWarps, MODE>::SMEM_BYTES;
+        case 16: return ssm::TmaScanLayout<T, N, (N == 256 ? 16 : L1), kTmaWarps, MODE>::SMEM_BYTES;
         default: return ssm::TmaScanLayout<T, N, (N >= 8 ? (N <= 64 ? 4 : L1) : 2), kTmaWarps, MODE>::SMEM_BYTES;
     }
 }
@@ -192,12 +193,14 @@ int tma_smem_for(ssm_dtype_t io, int dstate, int lanes) {
         if (dstate == 32) return tma_smem_bytes<float, 32, MODE>(lanes);
         if (dstate == 64) return tma_smem_bytes<float, 64, MODE>(lanes);
         if (dstate == 128) return tma_smem_bytes<float, 128, MODE>(lanes);
+        if (dstate == 256) return tma_smem_bytes<float, 256, MODE>(lanes);
         return dstate == 4 ? tma_smem_bytes<float, 4, MODE>(lanes)
                            : dstate == 8 ? tma_smem_bytes<float, 8, MODE>(lanes) : tma_smem_bytes<float, 16, MODE>(lanes);
     }
     if (dstate == 32) return tma_smem_bytes<__nv_bfloat16, 32, MODE>(lanes);
     if (dstate == 64) return tma_smem_bytes<__nv_bfloat16, 64, MODE>(lanes);
     if (dstate == 128) return tma_smem_bytes<__nv_bfloat16, 128, MODE>(lanes);
+    if (dstate == 256) return tma_smem_bytes<__nv_bfloat16, 256, MODE>(lanes);
     return dstate == 4 ? tma_smem_bytes<__nv_bfloat16, 4, MODE>(lanes)
                        : dstate == 8 ? tma_smem_bytes<__nv_bfloat16, 8, MODE>(lanes)
                                      : tma_smem_bytes<__nv_bfloat16, 16, MODE>(lanes);
@@ -248,7 +251,7 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
                    int chunk_cap) {
     const int dpg = dim / ngroups;
     const int kmax = std::max(1, std::min(chunk_cap, max_chunks_for(seqlen, io)));
-    const int lmax = dstate >= 128 ? 8 : (dstate >= 8 ? 4 : 2);
+    const int lmax = dstate >= 128 ? dstate / 16 : (dstate >= 8 ? 4 : 2);
     const int lmin = min_lanes_for(dstate);
     // Time units: ~0.54 ns of an SM each on B300 (one step of a CTA of
     // 16-state lanes is 128 units).
@@ -393,7 +396,8 @@ cudaError_t launch_tma_lanes(const ScanMaps& m, const ssm::TmaScanParams& p, int
         case 1: if constexpr (N <= 16) return launch_tma<T, N, 1, MODE>(m, p, grid_y, st); break;
         case 2: if constexpr (N <= 32) return launch_tma<T, N, 2, MODE>(m, p, grid_y, st); break;
         case 4: if constexpr (N >= 8 && N <= 64) return launch_tma<T, N, 4, MODE>(m, p, grid_y, st); break;
-        case 8: if constexpr (N >= 128) return launch_tma<T, N, 8, MODE>(m, p, grid_y, st); break;
+        case 8: if constexpr (N == 128) return launch_tma<T, N, 8, MODE>(m, p, grid_y, st); break;
+        case 16: if constexpr (N == 256) return launch_tma<T, N, 16, MODE>(m, p, grid_y, st); break;
         default: break;
     }
     return cudaErrorInvalidValue;
@@ -409,6 +413,7 @@ cudaError_t launch_tma_n(const ScanMaps& m, const ssm::TmaScanParams& p, int dst
         case 32: return launch_tma_lanes<T, 32, MODE>(m, p, lanes, grid_y, st);
         case 64: return launch_tma_lanes<T, 64, MODE>(m, p, lanes, grid_y, st);
         case 128: return launch_tma_lanes<T, 128, MODE>(m, p, lanes, grid_y, st);
+        case 256: return launch_tma_lanes<T, 256, MODE>(m, p, lanes, grid_y, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -478,6 +483,7 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
         else if (dstate == 32) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<32, kMaxChunks>, agg, h0, BD, plan.chunks);
         else if (dstate == 64) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<64, kMaxChunks>, agg, h0, BD, plan.chunks);
         else if (dstate == 128) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<128, kMaxChunks>, agg, h0, BD, plan.chunks);
+        else if (dstate == 256) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<256, kMaxChunks>, agg, h0, BD, plan.chunks);
         else e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<16, kMaxChunks>, agg, h0, BD, plan.chunks);
         if (e != cudaSuccess) return cuda_fail(e);
     }
@@ -789,6 +795,7 @@ cudaError_t launch_bwd_t(const ssm::BwdParams& p, int dstate, cudaStream_t st) {
         case 32: return launch_bwd_n<T, 32>(p, st);
         case 64: return launch_bwd_n<T, 64>(p, st);
         case 128: return launch_bwd_n<T, 128>(p, st);
+        case 256: return launch_bwd_n<T, 256>(p, st);
         default: return launch_bwd_n<T, 16>(p, st);
     }
 }
@@ -863,7 +870,7 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const void* z, const
     p.dA = dA; p.dB = dB; p.dC = dC; p.dD = dDskip; p.ddt_bias = ddt_bias; p.dh0 = dh0;
     p.batch = batch; p.dim = dim; p.seqlen = seqlen; p.ngroups = ngroups;
     p.dim_per_group = dim / ngroups;
-    const int ch = ssm::kBwdWarps * 32 / (dstate / ssm::kBwdStates);
+    const int ch = ssm::kBwdWarps * 32 / (dstate / ssm::bwd_states_per_lane(dstate));
     p.blocks_per_group = (p.dim_per_group + ch - 1) / ch;
     p.nchunks = bwd_nchunks(seqlen, dstate);
     p.vec_ok = (static_cast<long long>(seqlen) * es) % 16 == 0;
@@ -1044,7 +1051,8 @@ ssm_status_t ssm_state_update_pooled(float* state_pool, const int* state_indices
     }
     constexpr int kBPT = 8;
     constexpr int kThreads = 128;
-    const long long threads_x = static_cast<long long>(dim) * (dstate / 4);
+    // One lane per 16-byte state packet (8 states at N = 256, 4 otherwise).
+    const long long threads_x = static_cast<long long>(dim) * (dstate / (dstate > 128 ? 8 : 4));
     dim3 grid(static_cast<unsigned>((threads_x + kThreads - 1) / kThreads),
               static_cast<unsigned>((batch + kBPT - 1) / kBPT));
     if (grid.y > 65535u) return SSM_ERR_INVALID_ARG;
@@ -1056,6 +1064,7 @@ ssm_status_t ssm_state_update_pooled(float* state_pool, const int* state_indices
         else if (dstate == 32) SSM_DECODE_LAUNCH(float, 32, true);
         else if (dstate == 64) SSM_DECODE_LAUNCH(float, 64, true);
         else if (dstate == 128) SSM_DECODE_LAUNCH(float, 128, true);
+        else if (dstate == 256) SSM_DECODE_LAUNCH(float, 256, true);
         else SSM_DECODE_LAUNCH(float, 16, true);
     } else {
         if (dstate == 4) SSM_DECODE_LAUNCH(__nv_bfloat16, 4, false);
@@ -1063,6 +1072,7 @@ ssm_status_t ssm_state_update_pooled(float* state_pool, const int* state_indices
         else if (dstate == 32) SSM_DECODE_LAUNCH(__nv_bfloat16, 32, false);
         else if (dstate == 64) SSM_DECODE_LAUNCH(__nv_bfloat16, 64, false);
         else if (dstate == 128) SSM_DECODE_LAUNCH(__nv_bfloat16, 128, false);
+        else if (dstate == 256) SSM_DECODE_LAUNCH(__nv_bfloat16, 256, false);
         else SSM_DECODE_LAUNCH(__nv_bfloat16, 16, false);
     }
 #undef SSM_DECODE_LAUNCH

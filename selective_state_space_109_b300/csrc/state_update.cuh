@@ -7,10 +7,11 @@
 // (cuishuaiwen.com "Mamba & State-Space Sequence Models", Core mechanics;
 // intvml.com "DL0170 Mamba Selective SSM vs Attention", point (5)).
 //
-// The step is bound by HBM traffic on the state (read + write once).  Four
+// The step is bound by HBM traffic on the state (read + write once).  N/4
 // lanes share one (b,d) with four states each (one 16-byte state packet per
-// lane, so a warp moves 512 contiguous bytes); a thread walks BPT sequences
-// of the batch so that its A row is loaded once and reused.
+// lane, so a warp moves 512 contiguous bytes; at N = 256, 32 lanes of eight
+// states); a thread walks BPT sequences of the batch so that its A row is
+// loaded once and reused.
 #pragma once
 
 #include "ssm_device.cuh"
@@ -36,10 +37,11 @@ struct DecodeParams {
 template <typename T, int N, int BPT, bool ACCURATE>
 __global__ void __launch_bounds__(128)
 state_update_kernel(const DecodeParams p) {
-    constexpr int SPL = 4;          // states per lane
-    constexpr int QL = N / SPL;     // lanes per (b, d)
+    constexpr int SPL = N > 128 ? 8 : 4;  // states per lane (whole 16-byte packets)
+    constexpr int NV4 = SPL / 4;          // float4 packets per lane
+    constexpr int QL = N / SPL;           // lanes per (b, d)
     static_assert(N % SPL == 0 && (QL == 1 || QL == 2 || QL == 4 || QL == 8 || QL == 16 || QL == 32),
-                  "N in {4, ..., 128}");
+                  "N in {4, ..., 256}");
 
     const int gx = blockIdx.x * blockDim.x + threadIdx.x;
     const int d = gx / QL;
@@ -49,9 +51,13 @@ state_update_kernel(const DecodeParams p) {
     const int dc = active ? d : p.dim - 1;
     const int g = dc / p.dim_per_group;
 
-    const float4 av = __ldg(reinterpret_cast<const float4*>(p.A + static_cast<long long>(dc) * N) + q);
     constexpr float sc = decay_scale<ACCURATE>();
-    const float4 a2 = make_float4(av.x * sc, av.y * sc, av.z * sc, av.w * sc);
+    float a2[SPL];
+#pragma unroll
+    for (int v = 0; v < NV4; ++v) {
+        const float4 av = __ldg(reinterpret_cast<const float4*>(p.A + static_cast<long long>(dc) * N) + q * NV4 + v);
+        a2[4 * v] = av.x * sc; a2[4 * v + 1] = av.y * sc; a2[4 * v + 2] = av.z * sc; a2[4 * v + 3] = av.w * sc;
+    }
     const float bias = p.dt_bias ? __ldg(p.dt_bias + dc) : 0.f;
     const float dsk = p.D ? __ldg(p.D + dc) : 0.f;
 
@@ -69,25 +75,27 @@ state_update_kernel(const DecodeParams p) {
         const int slot = p.slots ? __ldg(p.slots + b) : b;
         if (slot < 0 || slot >= p.nslots) continue;  // a padding row (uniform over the CTA)
         const long long bd = static_cast<long long>(b) * p.dim + dc;
-        float4* sp = reinterpret_cast<float4*>(p.state + (static_cast<long long>(slot) * p.dim + dc) * N) + q;
-        const float4 s = active ? *sp : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4* sp = reinterpret_cast<float4*>(p.state + (static_cast<long long>(slot) * p.dim + dc) * N) + q * NV4;
+        float s[SPL];
+#pragma unroll
+        for (int v = 0; v < NV4; ++v) {
+            const float4 sv = active ? sp[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+            s[4 * v] = sv.x; s[4 * v + 1] = sv.y; s[4 * v + 2] = sv.z; s[4 * v + 3] = sv.w;
+        }
         const float uv = Elem<T>::load(up + bd);
         const float dt = softplus<ACCURATE>(Elem<T>::load(dp + bd) + bias);
         const float du = dt * uv;
         const long long bc = (static_cast<long long>(b) * p.ngroups + g) * N + q * SPL;
-        float bv[4], cv[4];
+        float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            bv[k] = Elem<T>::load(Bp + bc + k);
-            cv[k] = Elem<T>::load(Cp + bc + k);
+        for (int k = 0; k < SPL; ++k) {
+            s[k] = fmaf(decay<ACCURATE>(dt * a2[k]), s[k], du * Elem<T>::load(Bp + bc + k));
+            acc = fmaf(Elem<T>::load(Cp + bc + k), s[k], acc);
         }
-        float4 hn;
-        hn.x = fmaf(decay<ACCURATE>(dt * a2.x), s.x, du * bv[0]);
-        hn.y = fmaf(decay<ACCURATE>(dt * a2.y), s.y, du * bv[1]);
-        hn.z = fmaf(decay<ACCURATE>(dt * a2.z), s.z, du * bv[2]);
-        hn.w = fmaf(decay<ACCURATE>(dt * a2.w), s.w, du * bv[3]);
-        if (active) *sp = hn;
-        float acc = cv[0] * hn.x + cv[1] * hn.y + cv[2] * hn.z + cv[3] * hn.w;
+        if (active) {
+#pragma unroll
+            for (int v = 0; v < NV4; ++v) sp[v] = make_float4(s[4 * v], s[4 * v + 1], s[4 * v + 2], s[4 * v + 3]);
+        }
 #pragma unroll
         for (int m = QL / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
         if (active && q == 0) {

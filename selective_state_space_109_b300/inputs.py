@@ -213,10 +213,12 @@ WORKLOADS = {
     "scan_bf16_b1_d5120_l65536_final_state": dict(kind="scan", batch=1, dim=5120, dstate=16,
                                                   seqlen=65536, ngroups=1, io="bf16",
                                                   recipe="scaled", final_state=True),
-    # Large state: the b2 d1536 L2048 shape with N = 64 and 128 states per channel.
+    # Large state: the b2 d1536 L2048 shape with N = 64, 128 and 256 states per channel.
     "scan_bf16_b2_d1536_l2048_n64": dict(kind="scan", batch=2, dim=1536, dstate=64, seqlen=2048,
                                          ngroups=1, io="bf16", recipe="scaled"),
     "scan_bf16_b2_d1536_l2048_n128": dict(kind="scan", batch=2, dim=1536, dstate=128, seqlen=2048,
+                                          ngroups=1, io="bf16", recipe="scaled"),
+    "scan_bf16_b2_d1536_l2048_n256": dict(kind="scan", batch=2, dim=1536, dstate=256, seqlen=2048,
                                           ngroups=1, io="bf16", recipe="scaled"),
     "decode_b256_d5120": dict(kind="decode", batch=256, dim=5120, dstate=16, ngroups=1,
                               io="bf16", recipe="scaled", steps=1024),

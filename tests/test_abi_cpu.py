@@ -69,7 +69,7 @@ def test_scan_argument_errors(lib):
     assert scan(lib, L=-5) == 1
     assert scan(lib, dim=6, G=4) == 1          # dim % ngroups
     assert scan(lib, N=12) == 2                # unsupported state size
-    assert scan(lib, N=256) == 2               # N up to 128
+    assert scan(lib, N=512) == 2               # N up to 256
     assert scan(lib, N=128, L=9) == 2          # N = 128 needs rows of whole 16-byte packets
     assert scan(lib, io=7) == 2
     assert scan(lib, B=MIS) == 3               # misaligned
@@ -178,7 +178,7 @@ def test_bwd_argument_errors(lib):
     assert bwd(du=P) == 1                          # du aliases u
     assert bwd(dim=6, G=4) == 1
     assert bwd(N=12) == 2
-    assert bwd(N=256) == 2
+    assert bwd(N=512) == 2
     assert bwd(io=9) == 2
     assert bwd(dy=MIS) == 3
     assert bwd(dh0=MIS) == 3

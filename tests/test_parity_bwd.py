@@ -67,7 +67,7 @@ def check(got, ref, io, what):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [4, 8, 16, 32, 64, 128])
+@pytest.mark.parametrize("N", [4, 8, 16, 32, 64, 128, 256])
 def test_bwd_matches_oracle(ssm, io, N):
     # 2 groups of 35 channels (channel blocks end inside a group); L = 300:
     # several chunks and a ragged last tile.

@@ -1,8 +1,9 @@
-"""GPU parity of the scan and decode step with large state sizes (N = 32, 64
-and 128, several lanes sharing one channel's states) against the fp64 oracle:
-the TMA-staged path single pass and time-chunked, the generic path, the packed
-variable-length scan and the decode step.  N = 128 (8 lanes of 16 states, more
-lanes than the steps of a 16-byte fp32 chunk) runs on the staged path only."""
+"""GPU parity of the scan and decode step with large state sizes (N = 32, 64,
+128 and 256, several lanes sharing one channel's states) against the fp64
+oracle: the TMA-staged path single pass and time-chunked, the generic path,
+the packed variable-length scan and the decode step.  N = 128 and 256 (8 or 16
+lanes of 16 states, more lanes than the steps of a 16-byte chunk) run on the
+staged path only."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +26,7 @@ def chunked(ssm, x, h0=None):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [32, 64, 128])
+@pytest.mark.parametrize("N", [32, 64, 128, 256])
 @pytest.mark.parametrize("chunks", [1, 3])
 def test_staged_large_state(ssm, monkeypatch, io, N, chunks):
     monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
@@ -67,7 +68,7 @@ def test_varlen_large_state(ssm, io, N):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [32, 64, 128])
+@pytest.mark.parametrize("N", [32, 64, 128, 256])
 def test_decode_large_state(ssm, io, N):
     prm = I.decode_params(200, N, device="cuda")
     state = I.make_decode_state(5, 200, N, seed=3, device="cuda")
