@@ -385,3 +385,33 @@ def scan_bwd(u, delta, A, B, C, dy, z=None, D=None, dt_bias=None, h0=None, dh_fi
     if st != 0:
         raise SsmError(st, "ssm_scan_bwd")
     return o
+
+
+class SelectiveScanFn(torch.autograd.Function):
+    """The scan as a differentiable torch op: forward ``scan_fwd_chunked``,
+    backward ``scan_bwd`` (no states stored between the two; the backward
+    recomputes them).  Gradients arrive in each input's dtype (dB, dC are
+    accumulated in fp32 and cast)."""
+
+    @staticmethod
+    def forward(ctx, u, delta, A, B, C, z, D, dt_bias, h0):
+        y, hf = scan_fwd_chunked(u, delta, A, B, C, z=z, D=D, dt_bias=dt_bias, h0=h0)
+        ctx.save_for_backward(u, delta, A, B, C, z, D, dt_bias, h0)
+        return y, hf
+
+    @staticmethod
+    def backward(ctx, dy, dhf):
+        u, delta, A, B, C, z, D, dt_bias, h0 = ctx.saved_tensors
+        dy = torch.zeros_like(u) if dy is None else dy.to(u.dtype).contiguous()
+        dhf = None if dhf is None else dhf.float().contiguous()
+        g = scan_bwd(u, delta, A, B, C, dy, z=z, D=D, dt_bias=dt_bias, h0=h0, dh_final=dhf,
+                     want_dh0=h0 is not None and ctx.needs_input_grad[8])
+        cast = lambda t, like: None if t is None else t.to(like.dtype)
+        return (g["du"], g["ddelta"], g["dA"], cast(g["dB"], B), cast(g["dC"], C), g["dz"], g["dD"],
+                g["ddt_bias"], g["dh0"])
+
+
+def selective_scan(u, delta, A, B, C, z=None, D=None, dt_bias=None, h0=None):
+    """Differentiable selective scan: returns (y, h_final); torch autograd
+    calls this library's backward pass."""
+    return SelectiveScanFn.apply(u, delta, A, B, C, z, D, dt_bias, h0)

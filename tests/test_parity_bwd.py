@@ -171,3 +171,23 @@ def test_bwd_full_size_sampled_channels(ssm, name):
             rk = ref[k][0] if k != "dh0" else ref[k][:, 0]
             e = rel_l2(gk, rk)
             assert e <= TOL["bf16"][1], f"{name} d={d} {k}: rel_l2={e:.3e}"
+
+
+def test_autograd_function_matches_scan_bwd(ssm):
+    """torch.autograd through selective_scan gives the library's gradients,
+    including the final state's, in each input's dtype."""
+    x = I.make_scan_inputs(2, 48, 16, 200, 2, io="bf16", recipe="scaled", seed=21, device="cuda", with_h0=True)
+    leaves = {k: getattr(x, k).clone().requires_grad_(True) for k in ("u", "delta", "z", "A", "B", "C", "D",
+                                                                        "dt_bias", "h0")}
+    y, hf = ssm.selective_scan(leaves["u"], leaves["delta"], leaves["A"], leaves["B"], leaves["C"], z=leaves["z"],
+                               D=leaves["D"], dt_bias=leaves["dt_bias"], h0=leaves["h0"])
+    g = torch.Generator(device="cpu").manual_seed(22)
+    dy = torch.randn(y.shape, generator=g).to(y.dtype).cuda()
+    dhf = torch.randn(hf.shape, generator=g).cuda()
+    torch.autograd.backward([y, hf], [dy, dhf])
+    ref = ssm.scan_bwd(x.u, x.delta, x.A, x.B, x.C, dy, z=x.z, D=x.D, dt_bias=x.dt_bias, h0=x.h0, dh_final=dhf)
+    pairs = dict(u="du", delta="ddelta", z="dz", A="dA", B="dB", C="dC", D="dD", dt_bias="ddt_bias", h0="dh0")
+    for k, r in pairs.items():
+        got = leaves[k].grad
+        assert got is not None and got.dtype == leaves[k].dtype, k
+        assert rel_l2(to_np(got), to_np(ref[r].to(got.dtype))) <= 1e-6, k
