@@ -16,8 +16,8 @@
 //   dA[n] += lam_t[n] Delta_t Abar_t[n] h_{t-1}[n],  dD += g_t u_t,
 //   ddt_bias += ddelta_t,  dh0[n] = Abar_0[n] lam_0[n].
 //
-// Structure.  Time is cut into chunks of bwd_chunk_steps(N) steps; a CTA owns CH
-// channels of one (sequence, group) and one chunk.  Both recurrences run
+// Structure.  Time is cut into chunks of bwd_chunk_steps(N) steps; a CTA owns
+// CH channels of one (sequence, group) and one chunk.  Both recurrences run
 // across chunks through summaries, as in the forward pass:
 //   1. summary pass: per chunk, from a zero state, the decay product P and
 //      end state E; and, from a zero adjoint at the chunk's end, the adjoint
@@ -32,9 +32,8 @@
 //      gradient of the tile's steps.
 //
 // Lanes: LN = N/S consecutive lanes share a channel, S = 4 states each (8 at
-// N = 256).  The
-// per-step sums over states (the readout, du, dDelta) are butterfly-reduced
-// over the LN lanes; dB and dC sum over the channels of the group: a
+// N = 256).  The per-step sums over states (the readout, du, dDelta) are
+// butterfly-reduced over the LN lanes; dB and dC sum over the channels of the group: a
 // reduce-scatter over the channels of a warp, a sum over the CTA's warps in
 // shared memory, then one atomic add per (state, step) per CTA into fp32
 // buffers.  dA, dD and ddt_bias collect in registers and are added atomically
@@ -53,7 +52,8 @@ constexpr int kBwdWarps = 4;
 __host__ __device__ constexpr int bwd_states_per_lane(int n) { return n > 128 ? 8 : 4; }
 
 // Tiles per time chunk: their start states are held in shared memory (16 KB
-// per 8 tiles); fewer at N = 64, whose dB/dC staging is larger.
+// per 8 tiles at 4 states a lane); fewer from N = 64 on, whose dB/dC staging
+// is larger.
 __host__ __device__ constexpr int bwd_chunk_tiles(int n) { return n >= 64 ? 8 : 16; }
 __host__ __device__ constexpr int bwd_chunk_steps(int n) { return kBwdTT * bwd_chunk_tiles(n); }
 
