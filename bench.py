@@ -4,9 +4,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step is one forward selective scan (fused discretisation, recurrence,
-readout, skip and gate) over one batch of the headline workload: bf16 I/O,
-fp32 state, batch 2, 1536 channels, N 16, L 2048, G 1.  Rank 0 prints one
-JSON line.  `value` is the whole-job rate of compulsory bytes (u, delta, z, y
+readout, skip and gate, the state carried across time chunks and the final
+state returned) over one batch of the headline workload, the largest scan
+workload: bf16 I/O, fp32 state, batch 1, 5120 channels, N 16, L 65536, G 1.
+Rank 0 prints one JSON line.  `value` is the whole-job rate of compulsory bytes (u, delta, z, y
 plus B, C) per second, device-timed with CUDA events around a CUDA graph of K
 launches over rotating input sets that together exceed 3x the L2 cache.  The
 same line carries the end-to-end rate through the public API with host
@@ -37,15 +38,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-HEADLINE = "scan_bf16_b2_d1536_l2048"
+HEADLINE = "scan_bf16_b1_d5120_l65536_final_state"
 DECODE = "decode_b256_d5120"
 METRIC = "selective-scan fwd GB/s and % of B300 HBM roofline; decode tokens/s"
 FALLBACK_HBM_GBS = 6400.0
-# Measured on this B300 (probe of MUFU.EX2 and FFMA/FFMA2 issue): 32 ex2 and
-# 128 fp32 lane-ops per SM per clock.  One state update (b, d, l, n) needs one
-# ex2 and four fp32 ops (Delta*A, Delta*u*B, the FMA of the recurrence, the FMA
-# of the readout): 32 updates per SM per clock from either pipe.
-UPDATES_PER_SM_CLK = 32.0
+# One state update (b, d, l, n) needs one MUFU.EX2 (the decay) and four fp32
+# FMA-pipe operations (Delta*A, Delta*u*B, the FMA of the recurrence, the FMA
+# of the readout).  The arithmetic roofline is the rate at which the slower of
+# the two pipes can supply that, measured live on the GPU by
+# ssm_probe_alu_rates (nominal B300 rates: 32 ex2 and 128 FMA per SM per
+# clock, i.e. 32 updates per SM per clock from either pipe).
+NOMINAL_UPDATES_PER_SM_CLK = 32.0
 
 
 # ---------------------------------------------------------------------------
@@ -173,7 +176,7 @@ def measured_peaks():
 # Device sources of the chunked forward call's kernels (summary, carry and
 # fused passes): a DRAM-traffic record stays valid while these and the launch
 # plan are unchanged.
-FWD_SCAN_SOURCES = ("scan_tma.cuh", "tma.cuh", "ssm_device.cuh")
+FWD_SCAN_SOURCES = ("scan_tma.cuh", "scan_ws.cuh", "scan_ws_inst.cuh", "tma.cuh", "ssm_device.cuh")
 
 
 def kernel_source_hash(names=FWD_SCAN_SOURCES):
@@ -562,23 +565,37 @@ def bench_bwd(ssm, I, torch, peaks, names=("scan_bf16_b2_d1536_l2048", "scan_bf1
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
 
+# Channels of the headline workload in one oracle sample: the oracle's cost
+# per channel does not depend on the values, so a sample of channels with the
+# workload's per-channel shape (L, N) and recipe is timed instead of all 5120.
+ORACLE_SAMPLE_CHANNELS = 512
+
+
+def oracle_sample_inputs(I, w, nd):
+    """fp64 inputs of `nd` channels with the workload's batch, L, N, groups and
+    recipe (seed 0), for timing the oracle."""
+    return I.make_scan_inputs(w["batch"], nd, w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
+                              recipe=w["recipe"], seed=0, device="cpu").as_f64()
+
+
 def oracle_baseline(I, w, budget_s=10.0):
     import oracle
-    x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
-                           recipe=w["recipe"], seed=0, device="cpu").as_f64()
+    nd = min(w["dim"], ORACLE_SAMPLE_CHANNELS)
+    x = oracle_sample_inputs(I, w, nd)
     threads = oracle.default_threads()
-    nbytes = I.compulsory_bytes_scan(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], w["io"])
+    nbytes = I.compulsory_bytes_scan(w["batch"], nd, w["dstate"], w["seqlen"], w["ngroups"], w["io"])
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.scan(**x, nthreads=threads)
+        oracle.scan(**x, nthreads=threads, return_final_state=True)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
     gbs = reps * nbytes / el / 1e9
     return dict(value=gbs, unit="GB/s", cores=threads, kind="oracle",
-                sample=f"{reps} full passes of the {HEADLINE} workload (fp64 C oracle, "
-                       f"{threads} threads over channels) in {el:.1f} s",
+                sample=f"{reps} passes over {nd} of the {w['dim']} channels of the {HEADLINE} workload "
+                       f"(batch {w['batch']}, L {w['seqlen']}, N {w['dstate']}; fp64 C oracle, {threads} threads "
+                       f"over channels) in {el:.1f} s",
                 seconds=el, passes=reps)
 
 
@@ -595,6 +612,7 @@ def run_ours(args):
 
     w = I.WORKLOADS[HEADLINE]
     peaks, peak_src = measured_peaks()
+    alu = ssm.probe_alu_rates(dev)  # the arithmetic pipes' rates on this GPU, for the roofline
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -621,7 +639,7 @@ def run_ours(args):
 
     extra = {}
     if not args.skip_extra and world == 1:
-        for name in ("scan_bf16_b8_d2048_l4096", "scan_bf16_b1_d5120_l65536_final_state",
+        for name in ("scan_bf16_b2_d1536_l2048", "scan_bf16_b8_d2048_l4096",
                      "scan_bf16_b2_d1536_l2048_n64", "scan_bf16_b2_d1536_l2048_n128",
                      "scan_bf16_b2_d1536_l2048_n256"):
             wx = I.WORKLOADS[name]
@@ -644,8 +662,9 @@ def run_ours(args):
         return
     sm_max = peaks.get("sm_max_mhz", 2032.0)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = sms * sm_max * 1e6 * UPDATES_PER_SM_CLK / 1e9  # Gupd/s
     alu_achieved = r["upd_per_step"] / per_launch_s / 1e9
+    upd_per_sm_ns = min(alu["ex2_per_sm_ns"], alu["ffma_per_sm_ns"] / 4.0)
+    alu_peak = sms * upd_per_sm_ns  # Gupd/s
     traffic = ncu_traffic("scan_chunked_call/" + HEADLINE, r["plan"])
     out = {
         "metric": METRIC,
@@ -662,6 +681,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": HEADLINE, "batch": w["batch"], "dim": w["dim"], "dstate": w["dstate"],
                    "seqlen": w["seqlen"], "ngroups": w["ngroups"], "io": "bf16", "state": "f32",
+                   "final_state": bool(w.get("final_state", False)),
                    "recipe": w["recipe"], "l2": f"inputs larger than L2: {r['nsets']} rotating input sets "
                                                 f"({r['nsets'] * r['bytes_per_step'] / 1e6:.0f} MB)",
                    "timing": "CUDA events around a CUDA graph of the K launches",
@@ -672,10 +692,17 @@ def run_ours(args):
                      "unit": "Gupd/s", "frac": round(alu_achieved / alu_peak, 4), "traffic": traffic,
                      "kernel": ("scan_tma_kernel summary pass + scan_carry_kernel + scan_tma_kernel fused "
                                 "pass (one chunked call)" if r["plan"]["kernels"] > 1
-                                else "scan_tma_kernel fused pass"),
+                                else "scan_ws_kernel fused pass (one call)"),
                      "plan": r["plan"],
-                     "peak_basis": f"{sms} SMs x {sm_max:.0f} MHz x 32 state updates/SM/clk "
-                                   "(MUFU.EX2 32/clk; FP32 128 lane-ops/clk at 4 per update)"},
+                     "peak_basis": (f"measured live by ssm_probe_alu_rates: MUFU.EX2 "
+                                    f"{alu['ex2_per_sm_ns']:.2f} and fp32 FMA {alu['ffma_per_sm_ns']:.2f} per SM "
+                                    f"per ns; one ex2 and four FMA-pipe operations per state update -> "
+                                    f"{upd_per_sm_ns:.2f} updates per SM per ns x {sms} SMs (nominal: "
+                                    f"{NOMINAL_UPDATES_PER_SM_CLK:.0f}/SM/clk x {sm_max:.0f} MHz = "
+                                    f"{sms * sm_max * 1e-3 * NOMINAL_UPDATES_PER_SM_CLK:.0f} Gupd/s)"),
+                     "scope": "the whole chunked call (summary, carry and fused passes) against the "
+                              "updates of one pass; the summary pass recomputes the decays of all chunks "
+                              "but the last"},
         "hbm_roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "peak_source": peak_src, "traffic": traffic},
@@ -706,30 +733,28 @@ def run_reference(args):
     from selective_state_space_109_b300 import inputs as I
     w = I.WORKLOADS[HEADLINE]
     import oracle
-    x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], io=w["io"],
-                           recipe=w["recipe"], seed=0, device="cpu").as_f64()
     threads = oracle.default_threads()
-    nbytes = I.compulsory_bytes_scan(w["batch"], w["dim"], w["dstate"], w["seqlen"], w["ngroups"], w["io"])
-    # Each step: the oracle over a bounded sample (a slice of channels) of the
-    # workload, sized so K + W steps end within a few minutes.
-    frac = float(os.environ.get("SSM_REF_SAMPLE", "0.25"))
-    nd = max(1, int(w["dim"] * frac))
-    sub = {k: (v[:, :nd] if k in ("u", "delta", "z") else v[:nd] if k in ("A", "Dskip", "dt_bias") else v)
-           for k, v in x.items() if v is not None}
-    sub_bytes = nbytes * nd / w["dim"]
+    # Each step: the oracle over a bounded sample (a block of channels with the
+    # workload's per-channel shape and recipe), sized so that K + W steps end
+    # within a few minutes.
+    nd = max(1, min(w["dim"], int(os.environ.get("SSM_REF_CHANNELS", "256"))))
+    sub = oracle_sample_inputs(I, w, nd)
+    sub_bytes = I.compulsory_bytes_scan(w["batch"], nd, w["dstate"], w["seqlen"], w["ngroups"], w["io"])
     for _ in range(args.warmup):
-        oracle.scan(**sub, nthreads=threads)
+        oracle.scan(**sub, nthreads=threads, return_final_state=True)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.scan(**sub, nthreads=threads)
+        oracle.scan(**sub, nthreads=threads, return_final_state=True)
     el = time.perf_counter() - t0
     value = sub_bytes * args.steps / el / 1e9
-    sample = f"{nd} of {w['dim']} channels x batch {w['batch']} x L {w['seqlen']} per step"
+    sample = (f"{nd} of {w['dim']} channels x batch {w['batch']} x L {w['seqlen']} per step "
+              f"(the workload's per-channel shape and recipe, seed 0)")
     out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": HEADLINE, "batch": w["batch"], "dim": w["dim"], "dstate": w["dstate"],
-                      "seqlen": w["seqlen"], "ngroups": w["ngroups"], "io": "bf16-rounded values in fp64"},
+                      "seqlen": w["seqlen"], "ngroups": w["ngroups"], "io": "bf16-rounded values in fp64",
+                      "final_state": True},
            "impl": "reference",
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                             "sample": sample},

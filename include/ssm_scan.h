@@ -188,7 +188,10 @@ ssm_status_t ssm_workspace_status(const void *workspace, size_t workspace_bytes,
  *   - every GPU that loads the library holds that array until the process exits;
  *   - the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current, so make the first call on
- *     a device before any stream capture;
+ *     a device before any stream capture; the address is looked up again when
+ *     the thread's current context is not the one it was found in (after a
+ *     cudaDeviceReset, or under a caller's own driver context, where the
+ *     library's module and its array are a different instance);
  *   - all calls share the array, which keeps the previous call's contents (each
  *     call clears the status word; the summaries are rewritten before they are
  *     read): calls that can overlap on the GPU -- other streams, other host
@@ -381,6 +384,20 @@ ssm_status_t ssm_scan_bwd(const void *u, const void *delta, const void *z, const
                           float *dB, float *dC, float *dDskip, float *ddt_bias, float *dh0, int batch, int dim,
                           int dstate, int seqlen, int ngroups, ssm_dtype_t io, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * ssm_probe_alu_rates -- measurement helper (no counterpart on the source
+ * pages): the arithmetic rates that bound the scan on the current device.
+ * One state update needs one MUFU.EX2 (the decay exp(Delta A)) and four fp32
+ * FMA-pipe operations (Delta*A, (Delta u)*B, the recurrence's FMA and the
+ * readout's FMA).  Runs two short kernels on stream, each with every SM fully
+ * occupied by independent chains of one operation, synchronises, and writes:
+ *   *ex2_per_sm_ns  : MUFU.EX2 results per SM per nanosecond
+ *   *ffma_per_sm_ns : fp32 FMAs per SM per nanosecond
+ * sink: a device float the kernels may write (they never do in practice).
+ * Errors: SSM_ERR_INVALID_ARG (NULL pointer), SSM_ERR_CUDA.
+ */
+ssm_status_t ssm_probe_alu_rates(float *sink, double *ex2_per_sm_ns, double *ffma_per_sm_ns, void *stream);
 
 #ifdef __cplusplus
 }

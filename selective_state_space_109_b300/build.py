@@ -18,17 +18,21 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libssmscan.so")
-SOURCES = [os.path.join(CSRC, "ssm_scan.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("ssm_scan.cu", "scan_ws_bf16.cu", "scan_ws_f32.cu", "alu_probe.cu")]
+OBJDIR = os.path.join(HERE, "_build")
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))] + \
     [os.path.join(INCLUDE, "ssm_scan.h")]
 
-NVCC_FLAGS = [
-    "-gencode", "arch=compute_103a,code=sm_103a",
-    "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
-    "-cudart", "static",
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Relocatable device code: the kernel translation units share the library's
+# device error word; each compiles on its own (in parallel), then nvcc links
+# the device code and the shared library.
+COMPILE_FLAGS = ARCH + [
+    "-O3", "-lineinfo", "-std=c++17", "-rdc=true",
+    "-Xcompiler", "-fPIC",
     "--expt-relaxed-constexpr",
 ]
+LINK_FLAGS = ARCH + ["-shared", "-rdc=true", "-cudart", "static"]
 
 
 def nvcc() -> str:
@@ -48,9 +52,21 @@ def is_stale() -> bool:
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     if not force and not is_stale():
         return LIB
-    cmd = [nvcc()] + NVCC_FLAGS + ["-I", INCLUDE, "-o", LIB + ".tmp"] + SOURCES
-    if ptxas_info:
-        cmd.insert(1, "-Xptxas=-v")
+    from concurrent.futures import ThreadPoolExecutor
+    os.makedirs(OBJDIR, exist_ok=True)
+
+    def compile_one(src):
+        obj = os.path.join(OBJDIR, os.path.basename(src).replace(".cu", ".o"))
+        cmd = [nvcc()] + COMPILE_FLAGS + (["-Xptxas=-v"] if ptxas_info else []) + \
+            ["-I", INCLUDE, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        subprocess.run(cmd, check=True)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    cmd = [nvcc()] + LINK_FLAGS + ["-o", LIB + ".tmp"] + objs
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)

@@ -1,0 +1,14 @@
+// scan_ws_bf16.cu -- the warp-specialised fused scan pass for bf16 I/O.
+#include <cuda_bf16.h>
+
+#include "scan_ws_inst.cuh"
+
+namespace ssm {
+
+int ws_smem_bytes_bf16(int dstate, int lanes, int nw) { return ws_detail::smem_any<__nv_bfloat16>(dstate, lanes, nw); }
+
+cudaError_t ws_launch_bf16(int dstate, int lanes, int nw, const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
+    return ws_detail::launch_any<__nv_bfloat16>(dstate, lanes, nw, m, p, st);
+}
+
+}  // namespace ssm

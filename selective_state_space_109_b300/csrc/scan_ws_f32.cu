@@ -1,0 +1,12 @@
+// scan_ws_f32.cu -- the warp-specialised fused scan pass for fp32 I/O.
+#include "scan_ws_inst.cuh"
+
+namespace ssm {
+
+int ws_smem_bytes_f32(int dstate, int lanes, int nw) { return ws_detail::smem_any<float>(dstate, lanes, nw); }
+
+cudaError_t ws_launch_f32(int dstate, int lanes, int nw, const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
+    return ws_detail::launch_any<float>(dstate, lanes, nw, m, p, st);
+}
+
+}  // namespace ssm

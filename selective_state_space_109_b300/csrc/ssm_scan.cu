@@ -22,7 +22,14 @@
 #include "scan_fwd.cuh"
 #include "decode_tma.cuh"
 #include "scan_tma.cuh"
+#include "scan_ws_api.h"
 #include "state_update.cuh"
+
+// The library's device error word (declared in tma.cuh): every kernel
+// translation unit of the library shares this one definition.
+namespace ssm {
+__device__ unsigned int g_ssm_device_error = 0;
+}
 
 namespace {
 
@@ -418,6 +425,34 @@ cudaError_t launch_tma_n(const ScanMaps& m, const ssm::TmaScanParams& p, int dst
     }
 }
 
+// The carry pass between the summary and fused passes: one thread per
+// (channel, state pair); it waits for the summary pass in-kernel (programmatic
+// stream serialization), so its launch overlaps that pass's tail.
+cudaError_t launch_carry(float* agg, const float* h0, int batch, int dim, int dstate, int chunks, cudaStream_t st) {
+    const long long BD = static_cast<long long>(batch) * dim;
+    const long long threads = BD * (dstate / 2);
+    const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    switch (dstate) {
+        case 4: return cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<4, kMaxChunks>, agg, h0, BD, chunks);
+        case 8: return cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<8, kMaxChunks>, agg, h0, BD, chunks);
+        case 16: return cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<16, kMaxChunks>, agg, h0, BD, chunks);
+        case 32: return cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<32, kMaxChunks>, agg, h0, BD, chunks);
+        case 64: return cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<64, kMaxChunks>, agg, h0, BD, chunks);
+        case 128: return cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<128, kMaxChunks>, agg, h0, BD, chunks);
+        case 256: return cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<256, kMaxChunks>, agg, h0, BD, chunks);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 // Enqueues the staged scan: with plan.chunks > 1 the summary pass over all
 // chunks but the last, then the full pass over every chunk.
 ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const float* A, const void* B,
@@ -464,31 +499,88 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
                           : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Aggregate>(ma, pa, dstate, agg_lanes,
                                                                                   plan.chunks - 1, st);
         if (e != cudaSuccess) return cuda_fail(e);
-        const long long BD = static_cast<long long>(batch) * dim;
-        const long long threads = BD * (dstate / 2);
-        const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-        // The carry pass waits for the summary pass in-kernel (programmatic
-        // stream serialization), so its launch overlaps the summary pass's tail.
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(blocks);
-        cfg.blockDim = dim3(256);
-        cfg.stream = st;
-        cudaLaunchAttribute attr{};
-        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr.val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        if (dstate == 4) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<4, kMaxChunks>, agg, h0, BD, plan.chunks);
-        else if (dstate == 8) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<8, kMaxChunks>, agg, h0, BD, plan.chunks);
-        else if (dstate == 32) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<32, kMaxChunks>, agg, h0, BD, plan.chunks);
-        else if (dstate == 64) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<64, kMaxChunks>, agg, h0, BD, plan.chunks);
-        else if (dstate == 128) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<128, kMaxChunks>, agg, h0, BD, plan.chunks);
-        else if (dstate == 256) e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<256, kMaxChunks>, agg, h0, BD, plan.chunks);
-        else e = cudaLaunchKernelEx(&cfg, ssm::scan_carry_kernel<16, kMaxChunks>, agg, h0, BD, plan.chunks);
+        e = launch_carry(agg, h0, batch, dim, dstate, plan.chunks, st);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st)
                       : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return SSM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Warp-specialised scan (scan_ws.cuh): plan and launch
+// ---------------------------------------------------------------------------
+
+struct WsPlan {
+    int lanes;  // lanes per channel
+    int nw;     // consumer warps per CTA
+};
+
+int ws_smem(ssm_dtype_t io, int dstate, int lanes, int nw) {
+    return io == SSM_F32 ? ssm::ws_smem_bytes_f32(dstate, lanes, nw)
+                         : ssm::ws_smem_bytes_bf16(dstate, lanes, nw);
+}
+
+// Plans that run one pass over the whole sequence (no time split) take the
+// warp-specialised kernel (scan_ws.cuh): measured 407 us against 455 us for
+// the CTA-synchronous fused pass on bf16 b8 d2048 L4096 (2 lanes), and 1-4%
+// faster at N = 128 and 256.  Chunked plans keep the CTA-synchronous passes,
+// which measured faster there (b1 d5120 L65536: 2.20 ms against 2.58 ms for
+// the best chunked plan of the warp-specialised kernel).  Consumer warps per
+// CTA: two when four would leave fewer than two CTAs per SM.
+// SSM_SCAN_KERNEL=tma forces the CTA-synchronous kernel (for comparisons).
+bool ws_single_pass(int batch, int dim, int dstate, int ngroups, ssm_dtype_t io, const ScanPlan& plan,
+                    WsPlan* out) {
+    const char* v = std::getenv("SSM_SCAN_KERNEL");
+    if (v && std::strcmp(v, "tma") == 0) return false;
+    if (plan.chunks != 1) return false;
+    const int dpg = dim / ngroups;
+    auto ctas = [&](int nw) {
+        const int ch = nw * 32 / plan.lanes;
+        return static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
+    };
+    int nw = ctas(4) < 2LL * kPlanSms ? 2 : 4;
+    const int fnw = env_int("SSM_FORCE_NW", 0);
+    if (fnw == 2 || fnw == 4 || fnw == 8) nw = fnw;
+    if (ws_smem(io, dstate, plan.lanes, nw) <= 0) nw = 4;
+    if (ws_smem(io, dstate, plan.lanes, nw) <= 0) return false;
+    *out = WsPlan{plan.lanes, nw};
+    return true;
+}
+
+// Encodes the TMA views of one pass whose CTAs hold `ch` channels.
+bool ws_encode(ssm::WsMaps* m, const void* u, const void* delta, const void* z, const void* B, const void* C,
+               ssm_dtype_t io, int seqlen, int dpg, long long bg, int dstate, int ch) {
+    const bool ok = encode_act(&m->u, u, io, seqlen, dpg, bg, ch) && encode_act(&m->d, delta, io, seqlen, dpg, bg, ch) &&
+                    (z ? encode_act(&m->z, z, io, seqlen, dpg, bg, ch) : true) &&
+                    encode_bc(&m->B, B, io, seqlen, bg * dstate, dstate) &&
+                    encode_bc(&m->C, C, io, seqlen, bg * dstate, dstate);
+    if (ok && !z) m->z = m->u;  // never read: has_z = 0
+    return ok;
+}
+
+// Enqueues the warp-specialised scan: one fused pass over the whole sequence
+// (from h0, final state written when asked).
+ssm_status_t run_scan_ws(const void* u, const void* delta, const void* z, const float* A, const void* B,
+                         const void* C, const float* Dskip, const float* dt_bias, const float* h0, void* y,
+                         float* h_final, int batch, int dim, int dstate, int seqlen, int ngroups,
+                         ssm_dtype_t io, const WsPlan& plan, unsigned int* status, cudaStream_t st) {
+    if (!encode_tiled()) return cuda_fail(cudaErrorNotSupported);
+    const int dpg = dim / ngroups;
+    const long long bg = static_cast<long long>(batch) * ngroups;
+    const int ch = plan.nw * 32 / plan.lanes;
+    ssm::WsMaps m;
+    if (!ws_encode(&m, u, delta, z, B, C, io, seqlen, dpg, bg, dstate, ch)) return cuda_fail(cudaErrorInvalidValue);
+    ssm::WsScanParams p{};
+    p.A = A; p.D = Dskip; p.dt_bias = dt_bias; p.h0 = h0; p.h_final = h_final; p.y = y;
+    p.status = status;
+    p.batch = batch; p.dim = dim; p.seqlen = seqlen; p.ngroups = ngroups; p.dim_per_group = dpg;
+    p.blocks_per_group = (dpg + ch - 1) / ch;
+    p.ntiles = (seqlen + tma_steps_per_tile(io) - 1) / tma_steps_per_tile(io);
+    p.has_z = z != nullptr;
+    const cudaError_t e = io == SSM_F32 ? ssm::ws_launch_f32(dstate, plan.lanes, plan.nw, m, p, st)
+                                        : ssm::ws_launch_bf16(dstate, plan.lanes, plan.nw, m, p, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return SSM_OK;
 }
@@ -588,6 +680,7 @@ cudaError_t launch_decode_tma(float* state, const int* slots, int nslots, const 
                                           ngroups, st);
 }
 
+
 bool force_generic() {
     const char* s = std::getenv("SSM_FORCE_PATH");
     return s && std::strcmp(s, "generic") == 0;
@@ -628,9 +721,13 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
     if (tma_eligible(seqlen, io) && (!force_generic() || dstate_needs_tma(dstate))) {
         const bool chunks_ok = workspace != nullptr;
         const int cap = chunks_ok ? chunks_fitting(workspace_bytes, batch, dim, dstate) : 1;
-        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, cap);
         float* agg = chunks_ok ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader) : nullptr;
         unsigned int* status = chunks_ok ? static_cast<unsigned int*>(workspace) : nullptr;
+        const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, cap);
+        WsPlan wplan{};
+        if (ws_single_pass(batch, dim, dstate, ngroups, io, plan, &wplan))
+            return run_scan_ws(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen,
+                               ngroups, io, wplan, status, st);
         return run_scan_tma(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen,
                             ngroups, io, plan, agg, status, st);
     }
@@ -662,23 +759,50 @@ __device__ __align__(256) unsigned char g_static_scratch[SSM_STATIC_SCRATCH_BYTE
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_scratch_mu;
-void* g_static_scratch_ptr[kMaxDevices] = {};
+struct StaticScratchEntry {
+    CUcontext ctx;  // context the address was looked up in
+    void* ptr;
+};
+StaticScratchEntry g_static_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_static_scratch on the current device; looked up once per
-// device, with that device current.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+    static const CtxGetCurrentFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<CtxGetCurrentFn>(nullptr);
+        return reinterpret_cast<CtxGetCurrentFn>(f);
+    }();
+    return fn;
+}
+
+// Device address of g_static_scratch in the current device's current context.
+// It is looked up once per device with that device current, and again whenever
+// the current context differs from the one it was looked up in (after a
+// cudaDeviceReset, or under a caller's own driver context, where the module --
+// and so the array -- is a different instance).
 ssm_status_t static_scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return SSM_ERR_UNSUPPORTED;
+    CUcontext ctx = nullptr;  // null until the runtime has made a context current on this thread
+    const CtxGetCurrentFn get = ctx_get_current();
+    if (!get || get(&ctx) != CUDA_SUCCESS) return cuda_fail(cudaErrorNotSupported);
     std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-    if (!g_static_scratch_ptr[dev]) {
+    StaticScratchEntry& ent = g_static_scratch_ptr[dev];
+    if (!ent.ptr || !ctx || ent.ctx != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        e = cudaGetSymbolAddress(&p, g_static_scratch);  // makes the device's context current if needed
         if (e != cudaSuccess) return cuda_fail(e);
-        g_static_scratch_ptr[dev] = p;
+        if (get(&ctx) != CUDA_SUCCESS) return cuda_fail(cudaErrorNotSupported);
+        ent.ctx = ctx;
+        ent.ptr = p;
     }
-    *out = g_static_scratch_ptr[dev];
+    *out = ent.ptr;
     return SSM_OK;
 }
 

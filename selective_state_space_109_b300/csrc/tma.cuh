@@ -17,9 +17,10 @@ namespace ssm {
 constexpr unsigned kDeviceErrTimeout = 1u;  // a bounded wait gave up
 constexpr unsigned kDeviceErrRange = 2u;    // an access fell outside its tensor and was skipped
 
-// Library-wide device error word (the library is a single translation unit,
-// so this is its only definition); read and cleared by ssm_device_status.
-__device__ unsigned int g_ssm_device_error = 0;
+// Library-wide device error word, defined once in ssm_scan.cu (the library is
+// built with relocatable device code, so every kernel translation unit shares
+// it); read and cleared by ssm_device_status.
+extern __device__ unsigned int g_ssm_device_error;
 
 // Wall-clock budget of one wait (ns, read from %globaltimer).  A healthy wait
 // here lasts microseconds; after two seconds the wait gives up.
@@ -49,6 +50,12 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
+}
+
+// Plain arrive (count 1) on the barrier's current phase; release semantics
+// for this thread's prior memory accesses.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {

@@ -75,6 +75,9 @@ def _load() -> ctypes.CDLL:
     L.ssm_scan_bwd_workspace_size.restype = Z
     L.ssm_scan_bwd.argtypes = [P] * 20 + [I] * 6 + [P, Z, P]
     L.ssm_scan_bwd.restype = I
+    D = ctypes.POINTER(ctypes.c_double)
+    L.ssm_probe_alu_rates.argtypes = [P, D, D, P]
+    L.ssm_probe_alu_rates.restype = I
     return L
 
 
@@ -209,6 +212,19 @@ def device_status(clear: bool = False, device=None) -> int:
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return int(lib.ssm_device_status(int(bool(clear)), _stream_handle(dev)))
+
+
+def probe_alu_rates(device=None) -> dict:
+    """MUFU.EX2 results and fp32 FMAs per SM per nanosecond on the device (see
+    ssm_probe_alu_rates in the C header); synchronises."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    ex2, ffma = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    with torch.cuda.device(dev):
+        st = lib.ssm_probe_alu_rates(_ptr(sink), ctypes.byref(ex2), ctypes.byref(ffma), _stream_handle(dev))
+    if st != 0:
+        raise SsmError(st, "ssm_probe_alu_rates")
+    return dict(ex2_per_sm_ns=ex2.value, ffma_per_sm_ns=ffma.value)
 
 
 def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None,

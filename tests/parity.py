@@ -78,3 +78,51 @@ def oracle_scan(x, *, h0=None, final_state=False, channels=None, nthreads=None):
     if final_state:
         return np.stack(ys), np.stack(hs)
     return np.stack(ys)
+
+
+def oracle_compare_blocks(x, y, hf=None, *, h0=None, block=256):
+    """Compares a whole scan output y [batch, dim, L] (and h_final [batch,
+    dim, N] when given) with the oracle, computed over blocks of ``block``
+    channels so that host memory stays bounded on the largest workloads.
+    Every element is compared: the rel-L2 sums are accumulated over the
+    blocks, and fp32 max-rel uses the rms of the whole reference.  Returns
+    (rel_l2_y, rel_l2_h or None, max_rel_y or None)."""
+    batch, dim, L = x.u.shape
+    G = x.B.shape[1]
+    f64 = lambda t: None if t is None else t.detach().to("cpu", torch.float32).double().numpy()
+    A, D, bias = f64(x.A), f64(x.D), f64(x.dt_bias)
+    h0n = f64(h0) if h0 is not None else (f64(x.h0) if x.h0 is not None else None)
+    num = den = hnum = hden = 0.0
+    diffs, refs = [], []
+    for d0 in range(0, dim, block):
+        d1 = min(dim, d0 + block)
+        if G == 1:
+            gs = slice(0, 1)
+        else:
+            dpg = dim // G
+            assert d0 // dpg == (d1 - 1) // dpg, "a block must stay inside one group"
+            gs = slice(d0 // dpg, d0 // dpg + 1)
+        sub = dict(u=f64(x.u[:, d0:d1]), delta=f64(x.delta[:, d0:d1]),
+                   z=None if x.z is None else f64(x.z[:, d0:d1]), A=A[d0:d1], B=f64(x.B[:, gs]),
+                   C=f64(x.C[:, gs]), Dskip=D[d0:d1], dt_bias=bias[d0:d1],
+                   h0=None if h0n is None else h0n[:, d0:d1])
+        out = oracle.scan(**sub, return_final_state=hf is not None)
+        ry, rh = (out if hf is not None else (out, None))
+        gy = f64(y[:, d0:d1])
+        num += float(np.sum((gy - ry) ** 2))
+        den += float(np.sum(ry * ry))
+        if x.u.dtype == torch.float32:
+            diffs.append(np.abs(gy - ry).ravel())
+            refs.append(np.abs(ry).ravel())
+        if hf is not None:
+            gh = f64(hf[:, d0:d1])
+            hnum += float(np.sum((gh - rh) ** 2))
+            hden += float(np.sum(rh * rh))
+    e_y = float(np.sqrt(num / den)) if den > 0 else float(np.sqrt(num))
+    e_h = (float(np.sqrt(hnum / hden)) if hden > 0 else float(np.sqrt(hnum))) if hf is not None else None
+    e_m = None
+    if diffs:
+        dd, rr = np.concatenate(diffs), np.concatenate(refs)
+        rms = float(np.sqrt(den / rr.size)) if rr.size else 0.0
+        e_m = float(np.max(dd / np.maximum(rr, MAX_REL_GUARD * rms if rms > 0 else 1e-30))) if rr.size else 0.0
+    return e_y, e_h, e_m

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from parity import STATE_REL_L2, assert_close, oracle_scan, rel_l2, to_np
+from parity import BF16_REL_L2, STATE_REL_L2, assert_close, oracle_compare_blocks, oracle_scan, rel_l2, to_np
 from selective_state_space_109_b300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -88,18 +88,16 @@ def test_vanishing_step_leaves_skip_path(ssm):
     assert rel_l2(to_np(y), want) <= 1e-6
 
 
-def test_long_sequence_final_state_sampled(ssm):
-    """bf16 I/O, batch 1, 5120 channels, L 65536, final state returned: full
-    size on the GPU, 12 channels (y and h_final) checked against the oracle."""
+def test_long_sequence_final_state_full(ssm):
+    """bf16 I/O, batch 1, 5120 channels, L 65536, final state returned, in the
+    benchmark's launch configuration: every element of y and of h_final
+    against the oracle (computed over blocks of channels)."""
     w = I.WORKLOADS["scan_bf16_b1_d5120_l65536_final_state"]
     x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], 1, io="bf16",
                            recipe=w["recipe"], seed=0, device="cuda")
     y, hf = chunked(ssm, x)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(1)
-    ch = sorted({(0, 0), (0, w["dim"] - 1)} | {(0, int(d)) for d in rng.choice(w["dim"], 10, replace=False)})
-    ref_y, ref_h = oracle_scan(x, channels=ch, final_state=True)
-    got_y = np.stack([to_np(y[b, d]) for b, d in ch])
-    got_h = np.stack([to_np(hf[b, d]) for b, d in ch])
-    assert_close(got_y, ref_y, "bf16", "long sequence y")
-    assert rel_l2(got_h, ref_h) <= STATE_REL_L2
+    e, eh, _ = oracle_compare_blocks(x, y, hf)
+    print(f"b1 d5120 l65536: y rel_l2 {e:.3e}, h_final rel_l2 {eh:.3e}")
+    assert e <= BF16_REL_L2, f"y rel_l2={e:.3e}"
+    assert eh <= STATE_REL_L2, f"h_final rel_l2={eh:.3e}"

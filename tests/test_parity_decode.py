@@ -82,6 +82,30 @@ def test_decode_b256_d5120_1024_steps_sampled(ssm):
     assert es <= STATE_REL_L2
 
 
+def test_decode_b256_d5120_full_tensor_steps(ssm):
+    """Full-size decode (batch 256, 5120 channels, N 16), the launch the
+    benchmark times: three consecutive steps on one resident state, every
+    element of y and of the state against the oracle."""
+    w = I.WORKLOADS["decode_b256_d5120"]
+    batch, dim, N = w["batch"], w["dim"], w["dstate"]
+    prm = I.decode_params(dim, N, recipe="scaled", seed=0, device="cuda")
+    state = I.make_decode_state(batch, dim, N, seed=0, device="cuda")
+    ref_state = to_np(state)
+    f = {k: to_np(v) for k, v in prm.items()}
+    for step in range(3):
+        tok = I.make_decode_token(batch, dim, N, step, io="bf16", seed=0, device="cuda")
+        y = run_step(ssm, state, tok, prm)
+        torch.cuda.synchronize()
+        t = {k: to_np(v) for k, v in tok.items()}
+        ref_state, ref_y = oracle.state_update(ref_state, t["u"], t["delta"], f["A"], t["B"], t["C"],
+                                               z=t["z"], Dskip=f["D"], dt_bias=f["dt_bias"])
+        e = rel_l2(to_np(y), ref_y)
+        es = rel_l2(to_np(state), ref_state)
+        print(f"step {step}: y rel_l2 {e:.3e}, state rel_l2 {es:.3e}")
+        assert e <= BF16_REL_L2, f"step {step}: y rel_l2 {e:.3e}"
+        assert es <= STATE_REL_L2, f"step {step}: state rel_l2 {es:.3e}"
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("dim,G", [(200, 1), (512, 2), (384, 1)])
 def test_staged_decode_steps(ssm, io, dim, G):

@@ -3,14 +3,16 @@
 Small cases run the whole tensor through the oracle and span several tiles,
 ragged tails, partial channel blocks, groups and every lanes-per-channel
 variant; the two large workloads run at full size on the GPU, in the launch
-configuration the benchmark times, and are compared on sampled channels."""
+configuration the benchmark times, and are compared element by element with
+the oracle run over blocks of channels."""
 import os
 
 import numpy as np
 import pytest
 import torch
 
-from parity import assert_close, oracle_scan, rel_l2, to_np, STATE_REL_L2
+from parity import (BF16_REL_L2, STATE_REL_L2, assert_close, oracle_compare_blocks, oracle_scan, rel_l2,
+                    to_np)
 from selective_state_space_109_b300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -126,22 +128,14 @@ def test_bf16_b2_d1536_l2048_full(ssm):
     print(f"rel_l2 = {e:.3e}")
 
 
-def sample_channels(batch, dim, k, seed=0):
-    rng = np.random.default_rng(seed)
-    picks = {(0, 0), (batch - 1, dim - 1)}
-    while len(picks) < k:
-        picks.add((int(rng.integers(batch)), int(rng.integers(dim))))
-    return sorted(picks)
-
-
-def test_bf16_b8_d2048_l4096_sampled(ssm):
-    """bf16 I/O: batch 8, 2048 channels, L 4096 at full size; 48 channels checked."""
+def test_bf16_b8_d2048_l4096_full(ssm):
+    """bf16 I/O: batch 8, 2048 channels, L 4096 at full size; every element of
+    y against the oracle (computed over blocks of channels)."""
     w = I.WORKLOADS["scan_bf16_b8_d2048_l4096"]
     x = I.make_scan_inputs(w["batch"], w["dim"], w["dstate"], w["seqlen"], 1, io="bf16",
                            recipe=w["recipe"], seed=0, device="cuda")
     y = run(ssm, x)
     torch.cuda.synchronize()
-    ch = sample_channels(w["batch"], w["dim"], 48)
-    ref = oracle_scan(x, channels=ch)
-    got = np.stack([to_np(y[b, d]) for b, d in ch])
-    assert_close(got, ref, "bf16", "b8 d2048 l4096 sampled")
+    e, _, _ = oracle_compare_blocks(x, y)
+    print(f"b8 d2048 l4096: y rel_l2 {e:.3e} over {y.numel()} elements")
+    assert e <= BF16_REL_L2, f"rel_l2={e:.3e}"

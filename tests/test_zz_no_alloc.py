@@ -3,7 +3,8 @@ allocate device memory (for example a plugin whose host runtime owns every
 device buffer and passes only inputs and outputs, or a decode loop that must
 not call cudaMalloc/cudaFree because they can wait on in-flight GPU work).  Its
 scratch is a fixed library-owned array, so the GPU test checks that two calls
-in a row through the C ABI give what the workspace entry point gives.
+in a row through the C ABI give what the workspace entry point gives, and
+what the fp64 oracle gives.
 
 This file is named to be collected last: if it fails, a run that stops at the
 first failure has already run every other test."""
@@ -12,7 +13,8 @@ import ctypes
 import pytest
 import torch
 
-from parity import BF16_REL_L2, F32_REL_L2, STATE_REL_L2, rel_l2, to_np
+from parity import (BF16_REL_L2, F32_REL_L2, STATE_REL_L2, assert_close, oracle_compare_blocks, oracle_scan,
+                    rel_l2, to_np)
 from selective_state_space_109_b300 import inputs as I
 
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -38,13 +40,18 @@ def _call_static(ssm, x, y, hf, h0=None):
 
 
 @pytest.mark.gpu
-def test_static_scratch_matches_workspace_entry_point_twice():
+def test_static_scratch_matches_workspace_entry_point_twice(monkeypatch):
     ssm = _lib()
-    # Two different problems back to back: both plan several time chunks, so
-    # the second call reuses the scratch array the first one filled.
+    # Two different problems back to back, each split into four time chunks
+    # (forced, and checked through the plan query), so the carry runs through
+    # the static array and the second call reuses the array the first filled.
+    monkeypatch.setenv("SSM_FORCE_CHUNKS", "4")
     cases = [dict(batch=2, dim=128, dstate=16, seqlen=2048, ngroups=1, io="bf16", seed=41, h0=False),
              dict(batch=1, dim=96, dstate=16, seqlen=1000, ngroups=2, io="f32", seed=42, h0=True)]
     for c in cases:
+        dt = torch.float32 if c["io"] == "f32" else torch.bfloat16
+        plan = ssm.scan_plan(c["batch"], c["dim"], c["dstate"], c["seqlen"], c["ngroups"], dt)
+        assert plan["chunks"] == 4, plan
         x = I.make_scan_inputs(c["batch"], c["dim"], c["dstate"], c["seqlen"], c["ngroups"], io=c["io"],
                                recipe="scaled", seed=c["seed"], device="cuda", with_h0=c["h0"])
         h0 = x.h0 if c["h0"] else None
@@ -57,6 +64,10 @@ def test_static_scratch_matches_workspace_entry_point_twice():
         tol = F32_REL_L2 if c["io"] == "f32" else BF16_REL_L2
         assert rel_l2(to_np(y), to_np(y_ref)) <= tol
         assert rel_l2(to_np(hf), to_np(h_ref)) <= STATE_REL_L2
+        # ... and the static call's own result against the fp64 oracle.
+        ref_y, ref_h = oracle_scan(x, h0=h0, final_state=True)
+        assert_close(to_np(y), ref_y, c["io"], "static entry point")
+        assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
     assert ssm.device_status() == 0
 
 
@@ -90,4 +101,6 @@ def test_static_scratch_caps_the_chunk_count(monkeypatch):
     torch.cuda.synchronize()
     assert rel_l2(to_np(y), to_np(y_ref)) <= BF16_REL_L2
     assert rel_l2(to_np(hf), to_np(h_ref)) <= STATE_REL_L2
+    e, eh, _ = oracle_compare_blocks(x, y, hf)
+    assert e <= BF16_REL_L2 and eh <= STATE_REL_L2, (e, eh)
     assert ssm.device_status() == 0
