@@ -650,6 +650,22 @@ def run_ours(args):
                                                           / 1e9 / peaks["hbm_gbs"], 4),
                                Gupd_per_s=round(rx["upd_per_step"] / (rx["ms_per_launch"] * 1e-3) / 1e9, 1),
                                plan=rx["plan"])
+        # The time-segmented variant (time split inside each warp by an
+        # associative scan over (Abar, Bbar x) pairs), measured beside the
+        # default plans it loses to.
+        for name, lanes, seg in (("scan_bf16_b2_d1536_l2048", 4, 4),
+                                 ("scan_bf16_b1_d5120_l65536_final_state", 4, 2)):
+            os.environ["SSM_FORCE_SEG"], os.environ["SSM_FORCE_LANES"] = str(seg), str(lanes)
+            try:
+                wx = I.WORKLOADS[name]
+                rx = bench_scan_device(ssm, I, torch, wx, max(4, min(args.steps, 20)), 3, preroll_s=0.0)
+            finally:
+                del os.environ["SSM_FORCE_SEG"], os.environ["SSM_FORCE_LANES"]
+            extra[f"{name}_segmented_l{lanes}s{seg}"] = dict(
+                GBps=round(rx["bytes_per_step"] / (rx["ms_per_launch"] * 1e-3) / 1e9, 1),
+                us_per_launch=round(rx["ms_per_launch"] * 1e3, 2),
+                Gupd_per_s=round(rx["upd_per_step"] / (rx["ms_per_launch"] * 1e-3) / 1e9, 1),
+                plan={"lanes": lanes, "segments": seg, "kernels": 1, "staged": True})
         extra.update(bench_conv(ssm, I, torch, peaks))
         extra.update(bench_varlen(ssm, I, torch, peaks))
         extra.update(bench_bwd(ssm, I, torch, peaks))

@@ -37,11 +37,13 @@
 
 namespace ssm {
 
-template <typename T, int N, int LANES, int NW, int STAGES>
+// SEG > 1: the time-segmented variant (see the consumer section): a tile row
+// is SEG 16-byte chunks, one per time segment.
+template <typename T, int N, int LANES, int NW, int STAGES, int SEG = 1>
 struct WsLayout {
-    static constexpr int RB = kScanRowBytes;                          // bytes of a row per tile
+    static constexpr int RB = SEG == 1 ? kScanRowBytes : 16 * SEG;    // bytes of a row per tile
     static constexpr int TS = RB / static_cast<int>(sizeof(T));       // steps per tile
-    static constexpr int CH = NW * 32 / LANES;                        // channels per CTA
+    static constexpr int CH = NW * 32 / (LANES * SEG);                // channels per CTA
     static constexpr int ACT_BYTES = CH * RB;                         // one activation tile
     static constexpr int BC_BYTES = N * RB;                           // one raw B or C tile
     static constexpr int NACT = 3;                                    // u, delta, z
@@ -56,13 +58,13 @@ struct WsLayout {
     // (Delta, Delta, Delta u, Delta u) per step per channel, for LANES > 1.
     static constexpr int VPC = 16 / static_cast<int>(sizeof(T));
     static constexpr int XS_STRIDE = VPC * 16 + 16;
-    static constexpr int XS_BUF = (32 / LANES) * XS_STRIDE;
+    static constexpr int XS_BUF = (32 / LANES) * XS_STRIDE;  // one row per group of LANES lanes
     static constexpr int XS_BYTES = LANES > 1 ? NW * 2 * XS_BUF : 0;
     static constexpr int XS_OFFSET = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFFSET = XS_OFFSET + XS_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFFSET + 3 * STAGES * 8 + 1024;  // + alignment slack
     static constexpr int THREADS = (NW + 1) * 32;
-    static_assert(ACT_BYTES % 256 == 0, "activation tiles must keep the 32-byte swizzle phase");
+    static_assert(ACT_BYTES % (8 * RB) == 0, "activation tiles must keep the swizzle phase");
     static_assert(BC_BYTES % 128 == 0, "B/C tiles must stay 128-byte aligned");
 };
 
@@ -100,21 +102,21 @@ __device__ __forceinline__ void stg_row(T* p, const float (&f)[H]) {
 // that ptxas keeps registers within what that residency leaves: enough CTAs
 // for 16 consumer warps per SM (four per scheduler), at most what shared
 // memory allows (228 KB, 1 KB reserved per CTA).
-template <typename T, int N, int LANES, int NW, int STAGES>
+template <typename T, int N, int LANES, int NW, int STAGES, int SEG = 1>
 constexpr int ws_min_blocks() {
-    constexpr int per = WsLayout<T, N, LANES, NW, STAGES>::SMEM_BYTES + 1024;
+    constexpr int per = WsLayout<T, N, LANES, NW, STAGES, SEG>::SMEM_BYTES + 1024;
     constexpr int by_smem = (228 * 1024) / per;
     constexpr int want = 16 / NW;
     constexpr int b = by_smem < want ? by_smem : want;
     return b < 1 ? 1 : b;
 }
 
-template <typename T, int N, int LANES, int NW, int STAGES, bool ACCURATE>
-__global__ void __launch_bounds__((NW + 1) * 32, (ws_min_blocks<T, N, LANES, NW, STAGES>()))
+template <typename T, int N, int LANES, int NW, int STAGES, bool ACCURATE, int SEG = 1>
+__global__ void __launch_bounds__((NW + 1) * 32, (ws_min_blocks<T, N, LANES, NW, STAGES, SEG>()))
 scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
                const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B,
                const __grid_constant__ CUtensorMap tm_C, const WsScanParams p) {
-    using Lay = WsLayout<T, N, LANES, NW, STAGES>;
+    using Lay = WsLayout<T, N, LANES, NW, STAGES, SEG>;
     constexpr int TS = Lay::TS;
     constexpr int VPC = Lay::VPC;             // steps per 16-byte chunk
     constexpr int CHUNKS = Lay::RB / 16;      // 16-byte chunks per tile row
@@ -127,6 +129,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
     constexpr bool PACKED = !ACCURATE && (H % 2 == 0);
     constexpr int CONSUMERS = NW * 32;
     static_assert(S >= 2 && S % 2 == 0, "each lane holds an even number of states");
+    static_assert(SEG == 1 || LANES > 1, "the time-segmented variant shares its scalars through the scratch rows");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -236,130 +239,175 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
     }
 
     // ----------------------------------------------------------------------
-    // Consumer warps.
+    // Consumer warps, time-segmented variant (SEG > 1): the warp's lanes are
+    // (channel, segment, sub-lane) triples.  A tile row holds SEG 16-byte
+    // chunks of time; the LANES lanes of segment j work on chunk j.  Each
+    // segment first runs the recurrence from a zero state over its chunk
+    // (the summary pair (P, E): P = exp(A * sum Delta), E = end state), then
+    // the SEG pairs of a channel are combined by a warp-shuffle scan over
+    // (Abar, Bbar x) pairs -- (P1, E1) then (P2, E2) gives (P2 P1, P2 E1 + E2)
+    // (eightmm.github.io "Mamba", Scan View) -- into the state entering each
+    // segment, and each segment runs the recurrence again from that state with
+    // the readout.  Every decay is computed twice; the per-step scalars once.
     // ----------------------------------------------------------------------
-    const int r = warp * (32 / LANES) + lane / LANES;  // channel row within the CTA
-    const int j = lane % LANES;                        // sub-lane within the channel
-    const int jj = SPARE ? j % VPC : j;                // its step slot in a chunk
-    const bool own = !SPARE || j < VPC;                // it owns steps
-    const int cw = lane / LANES;                       // channel within the warp
-    unsigned char* xs_warp = smem + Lay::XS_OFFSET + warp * 2 * Lay::XS_BUF;
+    if constexpr (SEG > 1) {
+        constexpr int CPW = 32 / (LANES * SEG);           // channels per warp
+        const int j = lane % LANES;                       // sub-lane within the channel
+        const int seg = (lane / LANES) % SEG;             // time segment = chunk of the tile
+        const int cw = lane / (LANES * SEG);              // channel within the warp
+        const int grp = lane / LANES;                     // (channel, segment) group
+        const int r = warp * CPW + cw;                    // channel row within the CTA
+        const int jj = SPARE ? j % VPC : j;
+        const bool own = !SPARE || j < VPC;
+        unsigned char* xs_warp = smem + Lay::XS_OFFSET + warp * 2 * Lay::XS_BUF;
+        const int last_src = cw * LANES * SEG + (SEG - 1) * LANES + j;  // lane of the last segment
 
-    const int dloc = dloc0 + r;
-    const bool active = dloc < p.dim_per_group;
-    const int d = g * p.dim_per_group + (active ? dloc : 0);
-    const long long bd = static_cast<long long>(b) * p.dim + d;
+        const int dloc = dloc0 + r;
+        const bool active = dloc < p.dim_per_group;
+        const int d = g * p.dim_per_group + (active ? dloc : 0);
+        const long long bd = static_cast<long long>(b) * p.dim + d;
 
-    float2 a2[P], h[P];
-    {
-        const float* Ad = p.A + static_cast<long long>(d) * N + j * S;
+        float2 a2[P], hc[P];  // decay constants; state entering the tile
+        {
+            const float* Ad = p.A + static_cast<long long>(d) * N + j * S;
 #pragma unroll
-        for (int k = 0; k < P; ++k) {
-            const float2 av = __ldg(reinterpret_cast<const float2*>(Ad) + k);
-            a2[k] = make_float2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
-            h[k] = make_float2(0.f, 0.f);
-        }
-        if (p.h0 && active) {
-            const float2* h0v = reinterpret_cast<const float2*>(p.h0 + bd * N + j * S);
+            for (int k = 0; k < P; ++k) {
+                const float2 av = __ldg(reinterpret_cast<const float2*>(Ad) + k);
+                a2[k] = make_float2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
+                hc[k] = make_float2(0.f, 0.f);
+            }
+            if (p.h0 && active) {
+                const float2* h0v = reinterpret_cast<const float2*>(p.h0 + bd * N + j * S);
 #pragma unroll
-            for (int k = 0; k < P; ++k) h[k] = __ldg(h0v + k);
+                for (int k = 0; k < P; ++k) hc[k] = __ldg(h0v + k);
+            }
         }
-    }
-    const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
-    const float dsk = p.D ? __ldg(p.D + d) : 0.f;
-    T* yrow = static_cast<T*>(p.y) + bd * p.seqlen;
+        const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
+        const float dsk = p.D ? __ldg(p.D + d) : 0.f;
+        T* yrow = static_cast<T*>(p.y) + bd * p.seqlen;
 
 #pragma unroll 1
-    for (int i = 0; i < nt; ++i) {
-        const int s = i % STAGES;
-        const uint32_t par = static_cast<uint32_t>((i / STAGES) & 1);
-        if (!mbar_wait(&full_bar[s], par, p.status) || !mbar_wait(&ready_bar[s], par, p.status)) break;
-        const unsigned char* st = stage_ptr(s);
-        const unsigned char* u_t = st;
-        const unsigned char* d_t = st + Lay::ACT_BYTES;
-        const unsigned char* z_t = st + 2 * Lay::ACT_BYTES;
-        const float* bcf = reinterpret_cast<const float*>(st + Lay::BCF_OFFSET);
-        const int t0 = i * TS;
+        for (int i = 0; i < nt; ++i) {
+            const int s = i % STAGES;
+            const uint32_t par = static_cast<uint32_t>((i / STAGES) & 1);
+            if (!mbar_wait(&full_bar[s], par, p.status) || !mbar_wait(&ready_bar[s], par, p.status)) break;
+            const unsigned char* st = stage_ptr(s);
+            const float* bcf = reinterpret_cast<const float*>(st + Lay::BCF_OFFSET);
+            const int c = seg;
+            const int tl = i * TS + c * VPC + jj * H;  // first step of this lane's share
+            const uint32_t off = swz_rows<Lay::RB>(r, c) + jj * H * static_cast<int>(sizeof(T));
 
-        // One 16-byte chunk (VPC steps) of this lane's channel row.  MASKED:
-        // the tile runs past the sequence end, so steps beyond it get Delta = 0
-        // (Abar = 1, no input: the state passes through unchanged).
-        auto run_chunk = [&](const int c, auto masked) {
-            constexpr bool MASKED = decltype(masked)::value;
-            const uint32_t off = swz_act(r, c) + jj * H * static_cast<int>(sizeof(T));
+            // Per-step scalars of the lane's share of its chunk, shared with the
+            // other lanes of the (channel, segment) group through the scratch row.
             float uu[H], dt[H], du[H];
             {
                 float dv[H];
-                lds_row<T, H>(u_t + off, uu);
-                lds_row<T, H>(d_t + off, dv);
-                if constexpr (PACKED) {
+                lds_row<T, H>(st + off, uu);
+                lds_row<T, H>(st + Lay::ACT_BYTES + off, dv);
 #pragma unroll
-                    for (int k = 0; k < H; k += 2) {
-                        const float2 v = __fadd2_rn(make_float2(dv[k], dv[k + 1]), make_float2(bias, bias));
-                        float2 d2 = softplus2_fast(v);
-                        if constexpr (MASKED) {
-                            const int t = t0 + c * VPC + jj * H + k;
-                            if (t >= p.seqlen) d2.x = 0.f;
-                            if (t + 1 >= p.seqlen) d2.y = 0.f;
-                        }
-                        const float2 u2 = __fmul2_rn(d2, make_float2(uu[k], uu[k + 1]));
-                        dt[k] = d2.x; dt[k + 1] = d2.y;
-                        du[k] = u2.x; du[k + 1] = u2.y;
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < H; ++k) {
-                        dt[k] = softplus<ACCURATE>(dv[k] + bias);
-                        if constexpr (MASKED) {
-                            if (t0 + c * VPC + jj * H + k >= p.seqlen) dt[k] = 0.f;
-                        }
-                        du[k] = dt[k] * uu[k];
-                    }
+                for (int k = 0; k < H; ++k) {
+                    dt[k] = softplus<ACCURATE>(dv[k] + bias);
+                    if (tl + k >= p.seqlen) dt[k] = 0.f;  // past the end: Abar = 1, no input
+                    du[k] = dt[k] * uu[k];
                 }
             }
-            // The channel's lanes share (Delta, Delta, Delta u, Delta u) for
-            // every step of the chunk through the warp's scratch rows.
-            [[maybe_unused]] float4* xrow = nullptr;
-            if constexpr (LANES > 1) {
-                xrow = reinterpret_cast<float4*>(xs_warp + (c & 1) * Lay::XS_BUF + cw * Lay::XS_STRIDE);
-                if (own) {
+            float4* xrow = reinterpret_cast<float4*>(xs_warp + (i & 1) * Lay::XS_BUF + grp * Lay::XS_STRIDE);
+            if (own) {
 #pragma unroll
-                    for (int k = 0; k < H; ++k) xrow[jj * H + k] = make_float4(dt[k], dt[k], du[k], du[k]);
-                }
-                __syncwarp();
+                for (int k = 0; k < H; ++k) xrow[jj * H + k] = make_float4(dt[k], dt[k], du[k], du[k]);
             }
+            __syncwarp();
 
+            // Walk 1: the segment's summary from a zero state.
+            float2 pe[P], ee[P];
+            {
+                float dsum = 0.f, dcomp = 0.f;
+#pragma unroll
+                for (int k = 0; k < P; ++k) ee[k] = make_float2(0.f, 0.f);
+                // Two steps at a time: unrolled further, ptxas hoists the decays
+                // of every step (nothing else paces them) and spills.
+#pragma unroll 2
+                for (int kk = 0; kk < VPC; ++kk) {
+                    const float4 e = xrow[kk];
+                    const float2 dt2 = make_float2(e.x, e.y), du2 = make_float2(e.z, e.w);
+                    if constexpr (ACCURATE) {
+                        const float yk = e.x - dcomp;
+                        const float tk = dsum + yk;
+                        dcomp = (tk - dsum) - yk;
+                        dsum = tk;
+                    } else {
+                        dsum += e.x;
+                    }
+                    const float4* q4 = reinterpret_cast<const float4*>(bcf) + (c * VPC + kk) * NQP + j;
+#pragma unroll
+                    for (int k = 0; k < P; ++k) {
+                        const float4 q = q4[k * LANES];
+                        const float2 x = __fmul2_rn(dt2, a2[k]);
+                        const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+                        ee[k] = __ffma2_rn(abar, ee[k], __fmul2_rn(du2, make_float2(q.x, q.y)));
+                    }
+                }
+                const float2 ds2 = make_float2(dsum, dsum);
+#pragma unroll
+                for (int k = 0; k < P; ++k) {
+                    const float2 x = __fmul2_rn(ds2, a2[k]);
+                    pe[k] = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+                }
+            }
+            // Inclusive scan of the summaries over the channel's segments.
+#pragma unroll
+            for (int o = 1; o < SEG; o <<= 1) {
+#pragma unroll
+                for (int k = 0; k < P; ++k) {
+                    const float px = __shfl_up_sync(0xffffffffu, pe[k].x, o * LANES);
+                    const float py = __shfl_up_sync(0xffffffffu, pe[k].y, o * LANES);
+                    const float ex = __shfl_up_sync(0xffffffffu, ee[k].x, o * LANES);
+                    const float ey = __shfl_up_sync(0xffffffffu, ee[k].y, o * LANES);
+                    if (seg >= o) {
+                        ee[k] = __ffma2_rn(pe[k], make_float2(ex, ey), ee[k]);
+                        pe[k] = __fmul2_rn(pe[k], make_float2(px, py));
+                    }
+                }
+            }
+            // State entering this segment: the tile's incoming state through
+            // the segments before it.
+            float2 h[P];
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                const float px = __shfl_up_sync(0xffffffffu, pe[k].x, LANES);
+                const float py = __shfl_up_sync(0xffffffffu, pe[k].y, LANES);
+                const float ex = __shfl_up_sync(0xffffffffu, ee[k].x, LANES);
+                const float ey = __shfl_up_sync(0xffffffffu, ee[k].y, LANES);
+                h[k] = seg == 0 ? hc[k] : __ffma2_rn(make_float2(px, py), hc[k], make_float2(ex, ey));
+            }
+            // Walk 2: the recurrence from that state, with the readout.  The
+            // decays are evaluated again rather than kept from walk 1 (holding
+            // them would need a register per step and state).
             float acc[VPC];
 #pragma unroll
             for (int kk = 0; kk < VPC; ++kk) {
-                float2 dt2, du2;
-                if constexpr (LANES == 1) {
-                    dt2 = make_float2(dt[kk], dt[kk]);
-                    du2 = make_float2(du[kk], du[kk]);
-                } else {
-                    const float4 e = xrow[kk];
-                    dt2 = make_float2(e.x, e.y);
-                    du2 = make_float2(e.z, e.w);
-                }
-                const int row = c * VPC + kk;
-                const float4* q4 = reinterpret_cast<const float4*>(bcf) + row * NQP + j;
+                const float4 e = xrow[kk];
+                const float2 dt2 = make_float2(e.x, e.y), du2 = make_float2(e.z, e.w);
+                const float4* q4 = reinterpret_cast<const float4*>(bcf) + (c * VPC + kk) * NQP + j;
                 float2 y2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < P; ++k) {
                     const float4 q = q4[k * LANES];
                     const float2 x = __fmul2_rn(dt2, a2[k]);
-                    const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
-                    const float2 bx = __fmul2_rn(du2, make_float2(q.x, q.y));
-                    h[k] = __ffma2_rn(abar, h[k], bx);
+                    const float2 abar = make_float2(decay_again<ACCURATE>(x.x), decay_again<ACCURATE>(x.y));
+                    h[k] = __ffma2_rn(du2, make_float2(q.x, q.y), __fmul2_rn(abar, h[k]));
                     y2 = __ffma2_rn(make_float2(q.z, q.w), h[k], y2);
                 }
                 acc[kk] = y2.x + y2.y;
             }
-            if constexpr (LANES > 1) __syncwarp();  // the scratch row is rewritten two chunks on
-
+            // The next tile starts from the last segment's end state.
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                hc[k].x = __shfl_sync(0xffffffffu, h[k].x, last_src);
+                hc[k].y = __shfl_sync(0xffffffffu, h[k].y, last_src);
+            }
+            // Readout summed over the group's lanes, skip term, gate, store.
             if constexpr (SPARE) {
-                // Sum over the lane bits above the chunk's steps, then a
-                // reduce-scatter over the owners' bits.
 #pragma unroll
                 for (int m = LANES / 2; m >= VPC; m >>= 1) {
 #pragma unroll
@@ -370,51 +418,209 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
                 reduce_scatter<LANES, H>(acc, j);
             }
             float zz[H];
-            if (has_z) lds_row<T, H>(z_t + off, zz);
+            if (has_z) lds_row<T, H>(st + 2 * Lay::ACT_BYTES + off, zz);
             float out[H];
-            if constexpr (PACKED) {
 #pragma unroll
-                for (int k = 0; k < H; k += 2) {
-                    float2 y2 = __ffma2_rn(make_float2(dsk, dsk), make_float2(uu[k], uu[k + 1]),
-                                           make_float2(acc[k], acc[k + 1]));
-                    if (has_z) y2 = __fmul2_rn(y2, silu2_fast(make_float2(zz[k], zz[k + 1])));
-                    out[k] = y2.x; out[k + 1] = y2.y;
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < H; ++k) {
-                    float yv = fmaf(dsk, uu[k], acc[k]);
-                    if (has_z) yv *= silu<ACCURATE>(zz[k]);
-                    out[k] = yv;
-                }
+            for (int k = 0; k < H; ++k) {
+                float yv = fmaf(dsk, uu[k], acc[k]);
+                if (has_z) yv *= silu<ACCURATE>(zz[k]);
+                out[k] = yv;
             }
-            const int tl = t0 + c * VPC + jj * H;  // first step of this lane's share
             if (own && active) {
-                if constexpr (MASKED) {
+                if (tl + H <= p.seqlen) {
+                    stg_row<T, H>(yrow + tl, out);
+                } else {
 #pragma unroll
                     for (int k = 0; k < H; ++k)
                         if (tl + k < p.seqlen) Elem<T>::store(yrow + tl + k, out[k]);
-                } else {
-                    stg_row<T, H>(yrow + tl, out);
                 }
             }
-        };
-
-        if (t0 + TS <= p.seqlen) {
-#pragma unroll
-            for (int c = 0; c < CHUNKS; ++c) run_chunk(c, std::false_type{});
-        } else {
-#pragma unroll 1
-            for (int c = 0; c < CHUNKS; ++c) run_chunk(c, std::true_type{});
+            mbar_arrive(&empty_bar[s]);
         }
-        mbar_arrive(&empty_bar[s]);
-    }
-
-    if (!active) return;
-    if (p.h_final) {
-        float2* hf = reinterpret_cast<float2*>(p.h_final + bd * N + j * S);
+        if (active && p.h_final && seg == 0) {
+            float2* hf = reinterpret_cast<float2*>(p.h_final + bd * N + j * S);
 #pragma unroll
-        for (int k = 0; k < P; ++k) hf[k] = h[k];
+            for (int k = 0; k < P; ++k) hf[k] = hc[k];
+        }
+    } else {
+        const int r = warp * (32 / LANES) + lane / LANES;  // channel row within the CTA
+        const int j = lane % LANES;                        // sub-lane within the channel
+        const int jj = SPARE ? j % VPC : j;                // its step slot in a chunk
+        const bool own = !SPARE || j < VPC;                // it owns steps
+        const int cw = lane / LANES;                       // channel within the warp
+        unsigned char* xs_warp = smem + Lay::XS_OFFSET + warp * 2 * Lay::XS_BUF;
+
+        const int dloc = dloc0 + r;
+        const bool active = dloc < p.dim_per_group;
+        const int d = g * p.dim_per_group + (active ? dloc : 0);
+        const long long bd = static_cast<long long>(b) * p.dim + d;
+
+        float2 a2[P], h[P];
+        {
+            const float* Ad = p.A + static_cast<long long>(d) * N + j * S;
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                const float2 av = __ldg(reinterpret_cast<const float2*>(Ad) + k);
+                a2[k] = make_float2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
+                h[k] = make_float2(0.f, 0.f);
+            }
+            if (p.h0 && active) {
+                const float2* h0v = reinterpret_cast<const float2*>(p.h0 + bd * N + j * S);
+#pragma unroll
+                for (int k = 0; k < P; ++k) h[k] = __ldg(h0v + k);
+            }
+        }
+        const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
+        const float dsk = p.D ? __ldg(p.D + d) : 0.f;
+        T* yrow = static_cast<T*>(p.y) + bd * p.seqlen;
+
+#pragma unroll 1
+        for (int i = 0; i < nt; ++i) {
+            const int s = i % STAGES;
+            const uint32_t par = static_cast<uint32_t>((i / STAGES) & 1);
+            if (!mbar_wait(&full_bar[s], par, p.status) || !mbar_wait(&ready_bar[s], par, p.status)) break;
+            const unsigned char* st = stage_ptr(s);
+            const unsigned char* u_t = st;
+            const unsigned char* d_t = st + Lay::ACT_BYTES;
+            const unsigned char* z_t = st + 2 * Lay::ACT_BYTES;
+            const float* bcf = reinterpret_cast<const float*>(st + Lay::BCF_OFFSET);
+            const int t0 = i * TS;
+
+            // One 16-byte chunk (VPC steps) of this lane's channel row.  MASKED:
+            // the tile runs past the sequence end, so steps beyond it get Delta = 0
+            // (Abar = 1, no input: the state passes through unchanged).
+            auto run_chunk = [&](const int c, auto masked) {
+                constexpr bool MASKED = decltype(masked)::value;
+                const uint32_t off = swz_rows<Lay::RB>(r, c) + jj * H * static_cast<int>(sizeof(T));
+                float uu[H], dt[H], du[H];
+                {
+                    float dv[H];
+                    lds_row<T, H>(u_t + off, uu);
+                    lds_row<T, H>(d_t + off, dv);
+                    if constexpr (PACKED) {
+#pragma unroll
+                        for (int k = 0; k < H; k += 2) {
+                            const float2 v = __fadd2_rn(make_float2(dv[k], dv[k + 1]), make_float2(bias, bias));
+                            float2 d2 = softplus2_fast(v);
+                            if constexpr (MASKED) {
+                                const int t = t0 + c * VPC + jj * H + k;
+                                if (t >= p.seqlen) d2.x = 0.f;
+                                if (t + 1 >= p.seqlen) d2.y = 0.f;
+                            }
+                            const float2 u2 = __fmul2_rn(d2, make_float2(uu[k], uu[k + 1]));
+                            dt[k] = d2.x; dt[k + 1] = d2.y;
+                            du[k] = u2.x; du[k + 1] = u2.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < H; ++k) {
+                            dt[k] = softplus<ACCURATE>(dv[k] + bias);
+                            if constexpr (MASKED) {
+                                if (t0 + c * VPC + jj * H + k >= p.seqlen) dt[k] = 0.f;
+                            }
+                            du[k] = dt[k] * uu[k];
+                        }
+                    }
+                }
+                // The channel's lanes share (Delta, Delta, Delta u, Delta u) for
+                // every step of the chunk through the warp's scratch rows.
+                [[maybe_unused]] float4* xrow = nullptr;
+                if constexpr (LANES > 1) {
+                    xrow = reinterpret_cast<float4*>(xs_warp + (c & 1) * Lay::XS_BUF + cw * Lay::XS_STRIDE);
+                    if (own) {
+#pragma unroll
+                        for (int k = 0; k < H; ++k) xrow[jj * H + k] = make_float4(dt[k], dt[k], du[k], du[k]);
+                    }
+                    __syncwarp();
+                }
+
+                float acc[VPC];
+#pragma unroll
+                for (int kk = 0; kk < VPC; ++kk) {
+                    float2 dt2, du2;
+                    if constexpr (LANES == 1) {
+                        dt2 = make_float2(dt[kk], dt[kk]);
+                        du2 = make_float2(du[kk], du[kk]);
+                    } else {
+                        const float4 e = xrow[kk];
+                        dt2 = make_float2(e.x, e.y);
+                        du2 = make_float2(e.z, e.w);
+                    }
+                    const int row = c * VPC + kk;
+                    const float4* q4 = reinterpret_cast<const float4*>(bcf) + row * NQP + j;
+                    float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < P; ++k) {
+                        const float4 q = q4[k * LANES];
+                        const float2 x = __fmul2_rn(dt2, a2[k]);
+                        const float2 abar = make_float2(decay<ACCURATE>(x.x), decay<ACCURATE>(x.y));
+                        const float2 bx = __fmul2_rn(du2, make_float2(q.x, q.y));
+                        h[k] = __ffma2_rn(abar, h[k], bx);
+                        y2 = __ffma2_rn(make_float2(q.z, q.w), h[k], y2);
+                    }
+                    acc[kk] = y2.x + y2.y;
+                }
+                if constexpr (LANES > 1) __syncwarp();  // the scratch row is rewritten two chunks on
+
+                if constexpr (SPARE) {
+                    // Sum over the lane bits above the chunk's steps, then a
+                    // reduce-scatter over the owners' bits.
+#pragma unroll
+                    for (int m = LANES / 2; m >= VPC; m >>= 1) {
+#pragma unroll
+                        for (int kk = 0; kk < VPC; ++kk) acc[kk] += __shfl_xor_sync(0xffffffffu, acc[kk], m);
+                    }
+                    reduce_scatter<VPC, 1>(acc, j);
+                } else {
+                    reduce_scatter<LANES, H>(acc, j);
+                }
+                float zz[H];
+                if (has_z) lds_row<T, H>(z_t + off, zz);
+                float out[H];
+                if constexpr (PACKED) {
+#pragma unroll
+                    for (int k = 0; k < H; k += 2) {
+                        float2 y2 = __ffma2_rn(make_float2(dsk, dsk), make_float2(uu[k], uu[k + 1]),
+                                               make_float2(acc[k], acc[k + 1]));
+                        if (has_z) y2 = __fmul2_rn(y2, silu2_fast(make_float2(zz[k], zz[k + 1])));
+                        out[k] = y2.x; out[k + 1] = y2.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < H; ++k) {
+                        float yv = fmaf(dsk, uu[k], acc[k]);
+                        if (has_z) yv *= silu<ACCURATE>(zz[k]);
+                        out[k] = yv;
+                    }
+                }
+                const int tl = t0 + c * VPC + jj * H;  // first step of this lane's share
+                if (own && active) {
+                    if constexpr (MASKED) {
+#pragma unroll
+                        for (int k = 0; k < H; ++k)
+                            if (tl + k < p.seqlen) Elem<T>::store(yrow + tl + k, out[k]);
+                    } else {
+                        stg_row<T, H>(yrow + tl, out);
+                    }
+                }
+            };
+
+            if (t0 + TS <= p.seqlen) {
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c) run_chunk(c, std::false_type{});
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < CHUNKS; ++c) run_chunk(c, std::true_type{});
+            }
+            mbar_arrive(&empty_bar[s]);
+        }
+
+        if (!active) return;
+        if (p.h_final) {
+            float2* hf = reinterpret_cast<float2*>(p.h_final + bd * N + j * S);
+#pragma unroll
+            for (int k = 0; k < P; ++k) hf[k] = h[k];
+        }
     }
 }
 

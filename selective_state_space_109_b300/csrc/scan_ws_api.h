@@ -31,13 +31,16 @@ struct WsMaps {
 };
 
 // Dynamic shared memory of one kernel variant, or 0 if that variant is not
-// built.
-int ws_smem_bytes_bf16(int dstate, int lanes, int nw);
-int ws_smem_bytes_f32(int dstate, int lanes, int nw);
+// built.  seg = 1: the plain pass; seg > 1: the time-segmented variant (a tile
+// row of 16 * seg bytes, one 16-byte chunk per segment).
+int ws_smem_bytes_bf16(int dstate, int lanes, int nw, int seg);
+int ws_smem_bytes_f32(int dstate, int lanes, int nw, int seg);
 
 // Enqueues the pass (grid: blocks_per_group * ngroups * batch CTAs).
 // cudaErrorInvalidValue if the variant is not built.
-cudaError_t ws_launch_bf16(int dstate, int lanes, int nw, const WsMaps& m, const WsScanParams& p, cudaStream_t st);
-cudaError_t ws_launch_f32(int dstate, int lanes, int nw, const WsMaps& m, const WsScanParams& p, cudaStream_t st);
+cudaError_t ws_launch_bf16(int dstate, int lanes, int nw, int seg, const WsMaps& m, const WsScanParams& p,
+                           cudaStream_t st);
+cudaError_t ws_launch_f32(int dstate, int lanes, int nw, int seg, const WsMaps& m, const WsScanParams& p,
+                          cudaStream_t st);
 
 }  // namespace ssm

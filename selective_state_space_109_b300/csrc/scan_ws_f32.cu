@@ -3,10 +3,13 @@
 
 namespace ssm {
 
-int ws_smem_bytes_f32(int dstate, int lanes, int nw) { return ws_detail::smem_any<float>(dstate, lanes, nw); }
+int ws_smem_bytes_f32(int dstate, int lanes, int nw, int seg) {
+    return ws_detail::smem_any<float>(dstate, lanes, nw, seg);
+}
 
-cudaError_t ws_launch_f32(int dstate, int lanes, int nw, const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
-    return ws_detail::launch_any<float>(dstate, lanes, nw, m, p, st);
+cudaError_t ws_launch_f32(int dstate, int lanes, int nw, int seg, const WsMaps& m, const WsScanParams& p,
+                           cudaStream_t st) {
+    return ws_detail::launch_any<float>(dstate, lanes, nw, seg, m, p, st);
 }
 
 }  // namespace ssm

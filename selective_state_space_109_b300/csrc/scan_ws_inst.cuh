@@ -10,9 +10,13 @@
 namespace ssm {
 namespace ws_detail {
 
-// The (state size, lanes per channel, consumer warps) variants that are built.
-template <int N, int LANES, int NW>
+// The (state size, lanes per channel, consumer warps, time segments) variants
+// that are built.  SEG > 1 (the time-segmented variant) is built for N = 16
+// with four consumer warps: 2 lanes x 2, 4 or 8 segments and 4 lanes x 2 or
+// 4 segments (a tile row of 16 * SEG bytes keeps at least eight rows per CTA).
+template <int N, int LANES, int NW, int SEG>
 constexpr bool built() {
+    if (SEG > 1) return N == 16 && NW == 4 && ((LANES == 2 && SEG <= 8) || (LANES == 4 && SEG <= 4));
     if (NW == 4) {
         switch (N) {
             case 4: return LANES == 1 || LANES == 2;
@@ -32,27 +36,27 @@ constexpr bool built() {
 // Ring depth: four stages while a stage stays small, fewer for the large
 // widened B/C tiles of big state sizes.  (Three stages to fit a fourth CTA
 // per SM measured slower: 400 -> 430 us on the b8 d2048 L4096 shape.)
-template <typename T, int N, int LANES, int NW>
+template <typename T, int N, int LANES, int NW, int SEG>
 constexpr int stages() {
-    constexpr int bytes = WsLayout<T, N, LANES, NW, 4>::STAGE_BYTES;
+    constexpr int bytes = WsLayout<T, N, LANES, NW, 4, SEG>::STAGE_BYTES;
     return bytes <= 24 * 1024 ? 4 : (bytes <= 48 * 1024 ? 3 : 2);
 }
 
-template <typename T, int N, int LANES, int NW>
+template <typename T, int N, int LANES, int NW, int SEG>
 int smem_bytes() {
-    if constexpr (built<N, LANES, NW>()) {
-        return WsLayout<T, N, LANES, NW, stages<T, N, LANES, NW>()>::SMEM_BYTES;
+    if constexpr (built<N, LANES, NW, SEG>()) {
+        return WsLayout<T, N, LANES, NW, stages<T, N, LANES, NW, SEG>(), SEG>::SMEM_BYTES;
     } else {
         return 0;
     }
 }
 
-template <typename T, int N, int LANES, int NW>
+template <typename T, int N, int LANES, int NW, int SEG>
 cudaError_t launch(const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
-    if constexpr (built<N, LANES, NW>()) {
-        constexpr int STAGES = stages<T, N, LANES, NW>();
-        using Lay = WsLayout<T, N, LANES, NW, STAGES>;
-        auto kern = scan_ws_kernel<T, N, LANES, NW, STAGES, sizeof(T) == 4>;
+    if constexpr (built<N, LANES, NW, SEG>()) {
+        constexpr int STAGES = stages<T, N, LANES, NW, SEG>();
+        using Lay = WsLayout<T, N, LANES, NW, STAGES, SEG>;
+        auto kern = scan_ws_kernel<T, N, LANES, NW, STAGES, sizeof(T) == 4, SEG>;
         // Opt in to the dynamic shared memory once per device.
         static std::atomic<unsigned long long> done{0};
         int dev = 0;
@@ -66,8 +70,7 @@ cudaError_t launch(const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
         }
         const long long gx = static_cast<long long>(p.blocks_per_group) * p.ngroups * p.batch;
         if (gx > 0x7fffffffLL || gx <= 0) return cudaErrorInvalidConfiguration;
-        scan_ws_kernel<T, N, LANES, NW, STAGES, sizeof(T) == 4>
-            <<<static_cast<unsigned>(gx), Lay::THREADS, Lay::SMEM_BYTES, st>>>(m.u, m.d, m.z, m.B, m.C, p);
+        kern<<<static_cast<unsigned>(gx), Lay::THREADS, Lay::SMEM_BYTES, st>>>(m.u, m.d, m.z, m.B, m.C, p);
         return cudaGetLastError();
     } else {
         (void)m; (void)p; (void)st;
@@ -75,72 +78,81 @@ cudaError_t launch(const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
     }
 }
 
-template <typename T, int N, int NW>
+template <typename T, int N, int NW, int SEG>
 int smem_lanes(int lanes) {
     switch (lanes) {
-        case 1: return smem_bytes<T, N, 1, NW>();
-        case 2: return smem_bytes<T, N, 2, NW>();
-        case 4: return smem_bytes<T, N, 4, NW>();
-        case 8: return smem_bytes<T, N, 8, NW>();
-        case 16: return smem_bytes<T, N, 16, NW>();
+        case 1: return smem_bytes<T, N, 1, NW, SEG>();
+        case 2: return smem_bytes<T, N, 2, NW, SEG>();
+        case 4: return smem_bytes<T, N, 4, NW, SEG>();
+        case 8: return smem_bytes<T, N, 8, NW, SEG>();
+        case 16: return smem_bytes<T, N, 16, NW, SEG>();
         default: return 0;
     }
 }
 
-template <typename T, int N, int NW>
+template <typename T, int N, int NW, int SEG>
 cudaError_t launch_lanes(int lanes, const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
     switch (lanes) {
-        case 1: return launch<T, N, 1, NW>(m, p, st);
-        case 2: return launch<T, N, 2, NW>(m, p, st);
-        case 4: return launch<T, N, 4, NW>(m, p, st);
-        case 8: return launch<T, N, 8, NW>(m, p, st);
-        case 16: return launch<T, N, 16, NW>(m, p, st);
+        case 1: return launch<T, N, 1, NW, SEG>(m, p, st);
+        case 2: return launch<T, N, 2, NW, SEG>(m, p, st);
+        case 4: return launch<T, N, 4, NW, SEG>(m, p, st);
+        case 8: return launch<T, N, 8, NW, SEG>(m, p, st);
+        case 16: return launch<T, N, 16, NW, SEG>(m, p, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <typename T, int NW>
+template <typename T, int NW, int SEG>
 int smem_n(int dstate, int lanes) {
     switch (dstate) {
-        case 4: return smem_lanes<T, 4, NW>(lanes);
-        case 8: return smem_lanes<T, 8, NW>(lanes);
-        case 16: return smem_lanes<T, 16, NW>(lanes);
-        case 32: return smem_lanes<T, 32, NW>(lanes);
-        case 64: return smem_lanes<T, 64, NW>(lanes);
-        case 128: return smem_lanes<T, 128, NW>(lanes);
-        case 256: return smem_lanes<T, 256, NW>(lanes);
+        case 4: return smem_lanes<T, 4, NW, SEG>(lanes);
+        case 8: return smem_lanes<T, 8, NW, SEG>(lanes);
+        case 16: return smem_lanes<T, 16, NW, SEG>(lanes);
+        case 32: return smem_lanes<T, 32, NW, SEG>(lanes);
+        case 64: return smem_lanes<T, 64, NW, SEG>(lanes);
+        case 128: return smem_lanes<T, 128, NW, SEG>(lanes);
+        case 256: return smem_lanes<T, 256, NW, SEG>(lanes);
         default: return 0;
     }
 }
 
-template <typename T, int NW>
+template <typename T, int NW, int SEG>
 cudaError_t launch_n(int dstate, int lanes, const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
     switch (dstate) {
-        case 4: return launch_lanes<T, 4, NW>(lanes, m, p, st);
-        case 8: return launch_lanes<T, 8, NW>(lanes, m, p, st);
-        case 16: return launch_lanes<T, 16, NW>(lanes, m, p, st);
-        case 32: return launch_lanes<T, 32, NW>(lanes, m, p, st);
-        case 64: return launch_lanes<T, 64, NW>(lanes, m, p, st);
-        case 128: return launch_lanes<T, 128, NW>(lanes, m, p, st);
-        case 256: return launch_lanes<T, 256, NW>(lanes, m, p, st);
+        case 4: return launch_lanes<T, 4, NW, SEG>(lanes, m, p, st);
+        case 8: return launch_lanes<T, 8, NW, SEG>(lanes, m, p, st);
+        case 16: return launch_lanes<T, 16, NW, SEG>(lanes, m, p, st);
+        case 32: return launch_lanes<T, 32, NW, SEG>(lanes, m, p, st);
+        case 64: return launch_lanes<T, 64, NW, SEG>(lanes, m, p, st);
+        case 128: return launch_lanes<T, 128, NW, SEG>(lanes, m, p, st);
+        case 256: return launch_lanes<T, 256, NW, SEG>(lanes, m, p, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <typename T>
-int smem_any(int dstate, int lanes, int nw) {
-    switch (nw) {
-        case 2: return smem_n<T, 2>(dstate, lanes);
-        case 4: return smem_n<T, 4>(dstate, lanes);
+int smem_any(int dstate, int lanes, int nw, int seg) {
+    if (nw == 2 && seg == 1) return smem_n<T, 2, 1>(dstate, lanes);
+    if (nw != 4) return 0;
+    switch (seg) {
+        case 1: return smem_n<T, 4, 1>(dstate, lanes);
+        case 2: return smem_n<T, 4, 2>(dstate, lanes);
+        case 4: return smem_n<T, 4, 4>(dstate, lanes);
+        case 8: return smem_n<T, 4, 8>(dstate, lanes);
         default: return 0;
     }
 }
 
 template <typename T>
-cudaError_t launch_any(int dstate, int lanes, int nw, const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
-    switch (nw) {
-        case 2: return launch_n<T, 2>(dstate, lanes, m, p, st);
-        case 4: return launch_n<T, 4>(dstate, lanes, m, p, st);
+cudaError_t launch_any(int dstate, int lanes, int nw, int seg, const WsMaps& m, const WsScanParams& p,
+                       cudaStream_t st) {
+    if (nw == 2 && seg == 1) return launch_n<T, 2, 1>(dstate, lanes, m, p, st);
+    if (nw != 4) return cudaErrorInvalidValue;
+    switch (seg) {
+        case 1: return launch_n<T, 4, 1>(dstate, lanes, m, p, st);
+        case 2: return launch_n<T, 4, 2>(dstate, lanes, m, p, st);
+        case 4: return launch_n<T, 4, 4>(dstate, lanes, m, p, st);
+        case 8: return launch_n<T, 4, 8>(dstate, lanes, m, p, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -19,6 +19,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// The same MUFU.EX2, never merged with an identical earlier one: where a
+// value is deliberately recomputed instead of kept in a register.
+__device__ __forceinline__ float ex2_approx_again(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float lg2_approx(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -63,6 +70,13 @@ __host__ __device__ constexpr float decay_scale() { return ACCURATE ? 1.0f : kLo
 template <bool ACCURATE>
 __device__ __forceinline__ float decay(float x) {
     return ACCURATE ? exp_cody_waite(x) : ex2_approx(x);
+}
+
+// decay() evaluated again for a value computed earlier, without keeping the
+// earlier result live (fp32 I/O: the FMA-pipe exp may still be merged).
+template <bool ACCURATE>
+__device__ __forceinline__ float decay_again(float x) {
+    return ACCURATE ? exp_cody_waite(x) : ex2_approx_again(x);
 }
 
 // softplus(v) = max(v, 0) + log1p(exp(-|v|)).

@@ -330,14 +330,17 @@ struct ScanMaps {
 
 // [batch * ngroups, dim_per_group, seqlen] activation view; box = one tile of
 // kScanRowBytes per row times `rows` channels, swizzled at that row width.
-bool encode_act(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, int dpg, long long bg, int rows) {
+bool encode_act(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, int dpg, long long bg, int rows,
+                int row_bytes = ssm::kScanRowBytes) {
     const cuuint64_t es = io == SSM_F32 ? 4 : 2;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(dpg),
                                 static_cast<cuuint64_t>(bg)};
     const cuuint64_t strides[2] = {seqlen * es, seqlen * es * dpg};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(ssm::kScanRowBytes / es), static_cast<cuuint32_t>(rows), 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(row_bytes / es), static_cast<cuuint32_t>(rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapSwizzle swz = ssm::kScanRowBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    const CUtensorMapSwizzle swz = row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                     : CU_TENSOR_MAP_SWIZZLE_32B;
     return encode_tiled()(m, io == SSM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -345,11 +348,12 @@ bool encode_act(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, int
 }
 
 // [batch * ngroups * dstate, seqlen] view of B or C; box = one tile x dstate rows.
-bool encode_bc(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, long long rows, int dstate) {
+bool encode_bc(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, long long rows, int dstate,
+               int row_bytes = ssm::kScanRowBytes) {
     const cuuint64_t es = io == SSM_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {seqlen * es};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(ssm::kScanRowBytes / es), static_cast<cuuint32_t>(dstate)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes / es), static_cast<cuuint32_t>(dstate)};
     const cuuint32_t estr[2] = {1, 1};
     return encode_tiled()(m, io == SSM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                           const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -513,19 +517,24 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
 // ---------------------------------------------------------------------------
 
 struct WsPlan {
-    int lanes;  // lanes per channel
+    int lanes;  // lanes per channel (the state split)
     int nw;     // consumer warps per CTA
+    int seg;    // time segments per channel inside a warp (1: none)
 };
 
-int ws_smem(ssm_dtype_t io, int dstate, int lanes, int nw) {
-    return io == SSM_F32 ? ssm::ws_smem_bytes_f32(dstate, lanes, nw)
-                         : ssm::ws_smem_bytes_bf16(dstate, lanes, nw);
+// Bytes of a tile row of the warp-specialised pass: 32, or 16 per segment.
+int ws_row_bytes(int seg) { return seg > 1 ? 16 * seg : ssm::kScanRowBytes; }
+
+int ws_smem(ssm_dtype_t io, int dstate, int lanes, int nw, int seg = 1) {
+    return io == SSM_F32 ? ssm::ws_smem_bytes_f32(dstate, lanes, nw, seg)
+                         : ssm::ws_smem_bytes_bf16(dstate, lanes, nw, seg);
 }
 
 // Plans that run one pass over the whole sequence (no time split) take the
 // warp-specialised kernel (scan_ws.cuh): measured 407 us against 455 us for
 // the CTA-synchronous fused pass on bf16 b8 d2048 L4096 (2 lanes), and 1-4%
-// faster at N = 128 and 256.  Chunked plans keep the CTA-synchronous passes,
+// faster at N = 128 (at N = 256 it measured 1.25 ms against 0.93 ms, so that
+// state size keeps the CTA-synchronous pass).  Chunked plans keep the CTA-synchronous passes,
 // which measured faster there (b1 d5120 L65536: 2.20 ms against 2.58 ms for
 // the best chunked plan of the warp-specialised kernel).  Consumer warps per
 // CTA: two when four would leave fewer than two CTAs per SM.
@@ -534,7 +543,7 @@ bool ws_single_pass(int batch, int dim, int dstate, int ngroups, ssm_dtype_t io,
                     WsPlan* out) {
     const char* v = std::getenv("SSM_SCAN_KERNEL");
     if (v && std::strcmp(v, "tma") == 0) return false;
-    if (plan.chunks != 1) return false;
+    if (plan.chunks != 1 || dstate > 128) return false;  // N = 256: the CTA-synchronous pass measured faster
     const int dpg = dim / ngroups;
     auto ctas = [&](int nw) {
         const int ch = nw * 32 / plan.lanes;
@@ -545,17 +554,30 @@ bool ws_single_pass(int batch, int dim, int dstate, int ngroups, ssm_dtype_t io,
     if (fnw == 2 || fnw == 4 || fnw == 8) nw = fnw;
     if (ws_smem(io, dstate, plan.lanes, nw) <= 0) nw = 4;
     if (ws_smem(io, dstate, plan.lanes, nw) <= 0) return false;
-    *out = WsPlan{plan.lanes, nw};
+    *out = WsPlan{plan.lanes, nw, 1};
+    return true;
+}
+
+// SSM_FORCE_SEG=s (with SSM_FORCE_LANES=l) runs the time-segmented variant of
+// the warp-specialised pass -- the whole sequence in one kernel, time split
+// inside each warp by an associative scan -- in place of any other plan.
+bool ws_segmented_forced(ssm_dtype_t io, int dstate, WsPlan* out) {
+    const int seg = env_int("SSM_FORCE_SEG", 0);
+    if (seg <= 1) return false;
+    const int lanes = env_int("SSM_FORCE_LANES", 2);
+    if (ws_smem(io, dstate, lanes, 4, seg) <= 0) return false;
+    *out = WsPlan{lanes, 4, seg};
     return true;
 }
 
 // Encodes the TMA views of one pass whose CTAs hold `ch` channels.
 bool ws_encode(ssm::WsMaps* m, const void* u, const void* delta, const void* z, const void* B, const void* C,
-               ssm_dtype_t io, int seqlen, int dpg, long long bg, int dstate, int ch) {
-    const bool ok = encode_act(&m->u, u, io, seqlen, dpg, bg, ch) && encode_act(&m->d, delta, io, seqlen, dpg, bg, ch) &&
-                    (z ? encode_act(&m->z, z, io, seqlen, dpg, bg, ch) : true) &&
-                    encode_bc(&m->B, B, io, seqlen, bg * dstate, dstate) &&
-                    encode_bc(&m->C, C, io, seqlen, bg * dstate, dstate);
+               ssm_dtype_t io, int seqlen, int dpg, long long bg, int dstate, int ch, int rb) {
+    const bool ok = encode_act(&m->u, u, io, seqlen, dpg, bg, ch, rb) &&
+                    encode_act(&m->d, delta, io, seqlen, dpg, bg, ch, rb) &&
+                    (z ? encode_act(&m->z, z, io, seqlen, dpg, bg, ch, rb) : true) &&
+                    encode_bc(&m->B, B, io, seqlen, bg * dstate, dstate, rb) &&
+                    encode_bc(&m->C, C, io, seqlen, bg * dstate, dstate, rb);
     if (ok && !z) m->z = m->u;  // never read: has_z = 0
     return ok;
 }
@@ -569,18 +591,21 @@ ssm_status_t run_scan_ws(const void* u, const void* delta, const void* z, const 
     if (!encode_tiled()) return cuda_fail(cudaErrorNotSupported);
     const int dpg = dim / ngroups;
     const long long bg = static_cast<long long>(batch) * ngroups;
-    const int ch = plan.nw * 32 / plan.lanes;
+    const int ch = plan.nw * 32 / (plan.lanes * plan.seg);
+    const int rb = ws_row_bytes(plan.seg);
+    const int ts = rb / (io == SSM_F32 ? 4 : 2);
     ssm::WsMaps m;
-    if (!ws_encode(&m, u, delta, z, B, C, io, seqlen, dpg, bg, dstate, ch)) return cuda_fail(cudaErrorInvalidValue);
+    if (!ws_encode(&m, u, delta, z, B, C, io, seqlen, dpg, bg, dstate, ch, rb))
+        return cuda_fail(cudaErrorInvalidValue);
     ssm::WsScanParams p{};
     p.A = A; p.D = Dskip; p.dt_bias = dt_bias; p.h0 = h0; p.h_final = h_final; p.y = y;
     p.status = status;
     p.batch = batch; p.dim = dim; p.seqlen = seqlen; p.ngroups = ngroups; p.dim_per_group = dpg;
     p.blocks_per_group = (dpg + ch - 1) / ch;
-    p.ntiles = (seqlen + tma_steps_per_tile(io) - 1) / tma_steps_per_tile(io);
+    p.ntiles = (seqlen + ts - 1) / ts;
     p.has_z = z != nullptr;
-    const cudaError_t e = io == SSM_F32 ? ssm::ws_launch_f32(dstate, plan.lanes, plan.nw, m, p, st)
-                                        : ssm::ws_launch_bf16(dstate, plan.lanes, plan.nw, m, p, st);
+    const cudaError_t e = io == SSM_F32 ? ssm::ws_launch_f32(dstate, plan.lanes, plan.nw, plan.seg, m, p, st)
+                                        : ssm::ws_launch_bf16(dstate, plan.lanes, plan.nw, plan.seg, m, p, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return SSM_OK;
 }
@@ -725,7 +750,7 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
         unsigned int* status = chunks_ok ? static_cast<unsigned int*>(workspace) : nullptr;
         const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, cap);
         WsPlan wplan{};
-        if (ws_single_pass(batch, dim, dstate, ngroups, io, plan, &wplan))
+        if (ws_segmented_forced(io, dstate, &wplan) || ws_single_pass(batch, dim, dstate, ngroups, io, plan, &wplan))
             return run_scan_ws(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen,
                                ngroups, io, wplan, status, st);
         return run_scan_tma(u, delta, z, A, B, C, Dskip, dt_bias, h0, y, h_final, batch, dim, dstate, seqlen,

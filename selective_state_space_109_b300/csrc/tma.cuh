@@ -167,4 +167,21 @@ __device__ __forceinline__ uint32_t swz32(int r, int c) {
     return static_cast<uint32_t>(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
 }
 
+// The same for 128-byte rows written with CU_TENSOR_MAP_SWIZZLE_128B: address
+// bits [4:6] are XOR-ed with bits [7:9], i.e. with r & 7.  The tile base must
+// be 1024-byte aligned.
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Byte offset of 16-byte chunk c of row r in a tile of RB-byte rows written
+// by TMA with the swizzle of that row width (32, 64 or 128 bytes).
+template <int RB>
+__device__ __forceinline__ uint32_t swz_rows(int r, int c) {
+    static_assert(RB == 32 || RB == 64 || RB == 128, "tile rows are 32, 64 or 128 bytes");
+    if constexpr (RB == 32) return swz32(r, c);
+    else if constexpr (RB == 64) return swz64(r, c);
+    else return swz128(r, c);
+}
+
 }  // namespace ssm
