@@ -18,7 +18,9 @@ variable-length scan and the pooled decode step by
 ``tests/test_oracle_varlen_pins.py`` against the separately pinned scan and
 decode step, the backward pass by ``tests/test_oracle_bwd_pins.py`` against
 central finite differences of the pinned forward scan and a closed form at
-L = 1 -- and
+L = 1, the SSD (Mamba-2) layer by ``tests/test_oracle_ssd_pins.py`` against
+the separately pinned scan with its per-head parameters spread over the
+channels and against the quadratic (matrix-mixer) form -- and
 ``tests/test_oracle_mutants.py`` checks that the pins catch planted slips.
 """
 from __future__ import annotations
@@ -78,6 +80,8 @@ def _set_conv_types(lib):
     lib.oracle_causal_conv1d_update.restype = I
     lib.oracle_scan_bwd.argtypes = [P] * 20 + [I] * 6
     lib.oracle_scan_bwd.restype = I
+    lib.oracle_ssd.argtypes = [P] * 11 + [I] * 7
+    lib.oracle_ssd.restype = I
 
 
 class _use_library:
@@ -332,3 +336,40 @@ def scan_bwd(u, delta, A, B, C, dy, z=None, Dskip=None, dt_bias=None, h0=None, d
     if rc != 0:
         raise ValueError(f"oracle_scan_bwd rejected its arguments (code {rc})")
     return out
+
+
+def ssd(x, delta, A, B, C, z=None, Dskip=None, dt_bias=None, h0=None, *, headdim,
+        return_final_state=False, nthreads=None):
+    """SSD (Mamba-2) layer over whole sequences, in fp64: the recurrence with a
+    scalar decay A[h], step delta[b, h, t] and skip Dskip[h] per head.
+
+    x, z: [batch, nheads * headdim, L]; delta: [batch, nheads, L]; A, Dskip,
+    dt_bias: [nheads]; B, C: [batch, G, N, L]; h0: [batch, nheads * headdim, N].
+    Returns y [batch, nheads * headdim, L] (and h_final when asked).
+    """
+    x = _f64(x)
+    if x.ndim != 3:
+        raise ValueError("x must be [batch, nheads * headdim, L]")
+    batch, dim, L = x.shape
+    if dim % headdim != 0:
+        raise ValueError("the channel count must be a multiple of headdim")
+    nheads = dim // headdim
+    delta = _f64(delta, (batch, nheads, L))
+    z = _f64(z, x.shape)
+    A = _f64(A, (nheads,))
+    B = _f64(B)
+    if B.ndim != 4 or B.shape[0] != batch or B.shape[3] != L:
+        raise ValueError("B must be [batch, G, N, L]")
+    G, N = B.shape[1], B.shape[2]
+    C = _f64(C, B.shape)
+    Dskip = _f64(Dskip, (nheads,))
+    dt_bias = _f64(dt_bias, (nheads,))
+    h0 = _f64(h0, (batch, dim, N))
+    y = np.empty((batch, dim, L), dtype=np.float64)
+    hf = np.empty((batch, dim, N), dtype=np.float64) if return_final_state else None
+    rc = _load().oracle_ssd(_ptr(x), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C), _ptr(Dskip),
+                            _ptr(dt_bias), _ptr(h0), _ptr(y), _ptr(hf),
+                            batch, nheads, headdim, N, L, G, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_ssd rejected its arguments (code {rc})")
+    return (y, hf) if return_final_state else y

@@ -526,3 +526,110 @@ int oracle_scan_bwd(const double *u, const double *delta, const double *z,
     free(jobs); free(tid); free(sums);
     return ok ? ORACLE_OK : ORACLE_BAD_ARG;
 }
+
+/* ------------------------------------------------------------------------
+ * Structured state space duality (SSD, the Mamba-2 layer): the same
+ * recurrence with a scalar decay per head.  eightmm.github.io "Mamba",
+ * Relation to Mamba-2: Mamba-2 computes the causal matrix mixer
+ * y_t = sum_{i<=t} C_t (prod_{j=i+1..t} A_j) B_i x_i with faster block/chunk
+ * algorithms, and intvml.com (engineering paragraph) has it raise the state
+ * size N from 16 to as much as 256.  The reading taken here (the pages give
+ * no formula for the per-head parameters): head h owns headdim channels
+ * d = h * headdim + p that share one scalar A[h], one step
+ *     Delta_t = softplus(delta[b, h, t] + dt_bias[h])
+ * and one skip weight Dskip[h]; B and C are shared by the heads of a group
+ * (g = h / (nheads / ngroups)); per channel d and state n
+ *     H_t[p, n] = exp(Delta_t * A[h]) * H_{t-1}[p, n] + Delta_t * B_t[n] * x_t[p]
+ *     y_t[p]    = (sum_n C_t[n] * H_t[p, n] + Dskip[h] * x_t[p]) * silu(z_t[p])
+ * with the gate dropped when z is NULL.
+ *
+ * Layouts: x, z, y [batch, nheads * headdim, L]; delta [batch, nheads, L];
+ * A, Dskip, dt_bias [nheads]; B, C [batch, ngroups, N, L]; h0, h_final
+ * [batch, nheads * headdim, N].
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    const double *x, *delta, *z, *A, *B, *C, *Dskip, *dt_bias, *h0;
+    double *y, *h_final;
+    int batch, nheads, headdim, dstate, seqlen, ngroups;
+    long first, last; /* range of flattened (b, h) handled by one worker */
+} ssd_job;
+
+static void ssd_head(const ssd_job *J, int b, int h, double *H) {
+    const int P = J->headdim, N = J->dstate, L = J->seqlen;
+    const int dim = J->nheads * P;
+    const int g = h / (J->nheads / J->ngroups);
+    const size_t bc = ((size_t)b * J->ngroups + g) * (size_t)N * (size_t)L;
+    const size_t drow = ((size_t)b * J->nheads + h) * (size_t)L;
+    const double a = J->A[h];
+    const double dskip = J->Dskip ? J->Dskip[h] : 0.0;
+    const double bias = J->dt_bias ? J->dt_bias[h] : 0.0;
+
+    for (int p = 0; p < P; p++)
+        for (int n = 0; n < N; n++)
+            H[(size_t)p * N + n] = J->h0 ? J->h0[((size_t)b * dim + (size_t)h * P + p) * N + n] : 0.0;
+
+    for (int t = 0; t < L; t++) {
+        const double dt = softplus(J->delta[drow + t] + bias);
+        const double abar = exp(dt * a);
+        for (int p = 0; p < P; p++) {
+            const size_t row = ((size_t)b * dim + (size_t)h * P + p) * (size_t)L;
+            const double xt = J->x[row + t];
+            double acc = 0.0;
+            for (int n = 0; n < N; n++) {
+                double *hp = &H[(size_t)p * N + n];
+                *hp = abar * *hp + dt * J->B[bc + (size_t)n * L + t] * xt;
+                acc += J->C[bc + (size_t)n * L + t] * *hp;
+            }
+            double yt = acc + dskip * xt;
+            if (J->z) yt *= silu(J->z[row + t]);
+            J->y[row + t] = yt;
+        }
+    }
+    if (J->h_final)
+        for (int p = 0; p < P; p++)
+            for (int n = 0; n < N; n++)
+                J->h_final[((size_t)b * dim + (size_t)h * P + p) * N + n] = H[(size_t)p * N + n];
+}
+
+static void *ssd_worker(void *arg) {
+    const ssd_job *J = (const ssd_job *)arg;
+    double *H = (double *)malloc(sizeof(double) * (size_t)J->headdim * (size_t)J->dstate);
+    if (!H) return NULL;
+    for (long i = J->first; i < J->last; i++)
+        ssd_head(J, (int)(i / J->nheads), (int)(i % J->nheads), H);
+    free(H);
+    return NULL;
+}
+
+/* SSD layer over whole sequences.  z, Dskip, dt_bias, h0 and h_final may be
+ * NULL.  Returns ORACLE_OK or ORACLE_BAD_ARG. */
+int oracle_ssd(const double *x, const double *delta, const double *z,
+               const double *A, const double *B, const double *C,
+               const double *Dskip, const double *dt_bias, const double *h0,
+               double *y, double *h_final,
+               int batch, int nheads, int headdim, int dstate, int seqlen, int ngroups,
+               int nthreads) {
+    if (batch <= 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || seqlen < 0 || ngroups <= 0) return ORACLE_BAD_ARG;
+    if (nheads % ngroups != 0) return ORACLE_BAD_ARG;
+    if (!x || !delta || !A || !B || !C || !y) return ORACLE_BAD_ARG;
+    const long total = (long)batch * nheads;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > total) nthreads = (int)total;
+    ssd_job *jobs = (ssd_job *)malloc(sizeof(ssd_job) * (size_t)nthreads);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!jobs || !tid) { free(jobs); free(tid); return ORACLE_BAD_ARG; }
+    for (int k = 0; k < nthreads; k++) {
+        ssd_job *J = &jobs[k];
+        J->x = x; J->delta = delta; J->z = z; J->A = A; J->B = B; J->C = C;
+        J->Dskip = Dskip; J->dt_bias = dt_bias; J->h0 = h0; J->y = y; J->h_final = h_final;
+        J->batch = batch; J->nheads = nheads; J->headdim = headdim; J->dstate = dstate;
+        J->seqlen = seqlen; J->ngroups = ngroups;
+        J->first = total * k / nthreads;
+        J->last = total * (k + 1) / nthreads;
+        pthread_create(&tid[k], NULL, ssd_worker, J);
+    }
+    for (int k = 0; k < nthreads; k++) pthread_join(tid[k], NULL);
+    free(jobs);
+    free(tid);
+    return ORACLE_OK;
+}

@@ -1,6 +1,7 @@
 """The pins must be able to fail: each mutant below is the oracle source with
 one plausible slip planted in it (compiled here, on the CPU).  For every
-mutant at least one pin of tests/test_oracle_pins.py has to raise."""
+mutant at least one of the oracle pins (scan, convolution, packed batches,
+backward pass, SSD) has to raise."""
 import os
 import subprocess
 
@@ -11,6 +12,7 @@ import test_oracle_bwd_pins as bwd_pins
 import test_oracle_conv_pins as conv_pins
 import test_oracle_varlen_pins as varlen_pins
 import test_oracle_pins as pins
+import test_oracle_ssd_pins as ssd_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
 
@@ -69,6 +71,14 @@ MUTANTS = {
                                   "J->dA[(size_t)d * N + n] += l * dt * abar * hcur[n];"),
     "bwd_dh_final_ignored": ("lam[n] = J->dhf ? J->dhf[st + n] : 0.0;", "lam[n] = 0.0;"),
     "bwd_worker_sums_overwritten": ("dA[i] += J->dA[i];", "dA[i] = J->dA[i];"),
+    # the SSD (Mamba-2) layer
+    "ssd_head_group_interleaved": ("const int g = h / (J->nheads / J->ngroups);",
+                                   "const int g = h % J->ngroups;"),
+    "ssd_decay_per_channel_index": ("const double a = J->A[h];", "const double a = J->A[0];"),
+    "ssd_input_without_step": ("*hp = abar * *hp + dt * J->B[bc + (size_t)n * L + t] * xt;",
+                               "*hp = abar * *hp + J->B[bc + (size_t)n * L + t] * xt;"),
+    "ssd_readout_uses_B": ("acc += J->C[bc + (size_t)n * L + t] * *hp;", "acc += J->B[bc + (size_t)n * L + t] * *hp;"),
+    "ssd_skip_dropped": ("double yt = acc + dskip * xt;", "double yt = acc;"),
 }
 
 PIN_TESTS = [
@@ -95,6 +105,8 @@ PIN_TESTS = [
     lambda: bwd_pins.test_single_step_closed_form(True),
     lambda: bwd_pins.test_empty_sequence_passes_dh_final_to_h0(),
     lambda: bwd_pins.test_threads_do_not_change_sums(),
+    lambda: ssd_pins.test_ssd_equals_the_scan_with_spread_parameters(2, True),
+    lambda: ssd_pins.test_ssd_equals_the_quadratic_duality_form(2),
 ]
 
 
