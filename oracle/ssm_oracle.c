@@ -581,7 +581,7 @@ static void ssd_head(const ssd_job *J, int b, int h, double *H) {
                 acc += J->C[bc + (size_t)n * L + t] * *hp;
             }
             double yt = acc + dskip * xt;
-            if (J->z) yt *= silu(J->z[row + t]);
+            if (J->z) yt = yt * silu(J->z[row + t]);
             J->y[row + t] = yt;
         }
     }
