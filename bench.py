@@ -527,6 +527,39 @@ def bench_varlen(ssm, I, torch, peaks):
     return res
 
 
+def bench_ssd(ssm, I, torch, peaks, name="ssd_bf16_b2_h64_p64_n128_l2048"):
+    """The SSD (Mamba-2) layer on the tensor cores: device time per launch over
+    rotating inputs (> 3x L2); compulsory bytes per second and the chunked
+    evaluation's dense-contraction FLOPs against the measured bf16 tensor peak."""
+    dev = torch.device("cuda")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    w = I.WORKLOADS[name]
+    args = (w["batch"], w["nheads"], w["headdim"], w["dstate"], w["seqlen"], w["ngroups"])
+    nbytes = I.compulsory_bytes_ssd(*args)
+    flops = I.flops_ssd_chunked(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["seqlen"])
+    nsets = n_rotating_sets(nbytes, l2)
+    xs = [I.make_ssd_inputs(*args, seed=s, device=dev) for s in range(nsets)]
+    ys = [torch.empty_like(x["x"]) for x in xs]
+    hfs = [torch.empty((w["batch"], w["nheads"] * w["headdim"], w["dstate"]), device=dev) for _ in xs]
+
+    def launch(i):
+        x = xs[i]
+        ssm.ssd_fwd(x["x"], x["delta"], x["A"], x["B"], x["C"], z=x["z"], D=x["D"], dt_bias=x["dt_bias"],
+                    headdim=w["headdim"], out=ys[i], h_final=hfs[i])
+
+    ms = bench_graph(torch, launch, nsets, reps=max(3, 60 // nsets))
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops", 1800.0)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del xs, ys, hfs
+    return {name: dict(us_per_launch=round(ms * 1e3, 2), GBps=round(gbs, 1),
+                       frac_of_hbm_measured=round(gbs / peaks["hbm_gbs"], 4), TFLOPs=round(tflops, 1),
+                       roofline={"bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                                 "frac": round(tflops / peak, 4),
+                                 "peak_source": "bf16_tflops of MEASURED_PEAKS.json (cuBLAS bf16 GEMM, burst)"},
+                       kernel="ssd_fwd_kernel (tcgen05.mma, TMEM accumulators, TMA)")}
+
+
 def bench_bwd(ssm, I, torch, peaks, names=("scan_bf16_b2_d1536_l2048", "scan_bf16_b8_d2048_l4096")):
     """Backward pass (every gradient, no final-state gradient) on the scan
     shapes: device time per call over rotating inputs (> 3x L2)."""
@@ -669,6 +702,7 @@ def run_ours(args):
         extra.update(bench_conv(ssm, I, torch, peaks))
         extra.update(bench_varlen(ssm, I, torch, peaks))
         extra.update(bench_bwd(ssm, I, torch, peaks))
+        extra.update(bench_ssd(ssm, I, torch, peaks))
 
     base = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -812,6 +846,17 @@ def run_profile_case(args):
         for _ in range(args.warmup + args.steps):
             ssm.scan_fwd_varlen(x["u"], x["delta"], x["A"], x["B"], x["C"], x["cu_seqlens"], z=x["z"], D=x["D"],
                                 dt_bias=x["dt_bias"], h0=x["h0"], return_final_state=True)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
+        return
+    if args.profile.startswith("ssd_"):
+        w = I.WORKLOADS[args.profile]
+        x = I.make_ssd_inputs(w["batch"], w["nheads"], w["headdim"], w["dstate"], w["seqlen"], w["ngroups"],
+                              device=dev)
+        y = torch.empty_like(x["x"])
+        for _ in range(args.warmup + args.steps):
+            ssm.ssd_fwd(x["x"], x["delta"], x["A"], x["B"], x["C"], z=x["z"], D=x["D"], dt_bias=x["dt_bias"],
+                        headdim=w["headdim"], out=y)
         torch.cuda.synchronize(dev)
         print(json.dumps({"profile_case": args.profile, "launches": args.warmup + args.steps}))
         return

@@ -386,6 +386,37 @@ ssm_status_t ssm_scan_bwd(const void *u, const void *delta, const void *z, const
                           size_t workspace_bytes, void *stream);
 
 /*
+ * ssm_ssd_fwd -- the SSD (structured state space duality, Mamba-2) layer:
+ * the selective recurrence with a scalar decay per head, computed chunk by
+ * chunk as dense contractions on the tensor cores (eightmm.github.io
+ * "Mamba", Relation to Mamba-2: the layer is the causal matrix mixer
+ * y_t = sum_{s<=t} C_t (prod_{j=s+1..t} A_j) B_s x_s, evaluated with block/chunk
+ * algorithms; intvml.com, engineering paragraph: state sizes up to 256).
+ *
+ * Head h owns the headdim channels d = h * headdim + p, which share one scalar
+ * A[h], the step Delta_t = softplus(delta[b, h, t] + dt_bias[h]) and the skip
+ * Dskip[h]; B, C belong to group g = h / (nheads / ngroups).  Per channel and
+ * state n:
+ *   H_t[p, n] = exp(Delta_t A[h]) H_{t-1}[p, n] + Delta_t B_t[n] x_t[p]
+ *   y_t[p]    = (sum_n C_t[n] H_t[p, n] + Dskip[h] x_t[p]) * silu(z_t[p])
+ *   x, z, y    : [batch, nheads * headdim, seqlen] bf16 (z may be NULL: no gate)
+ *   delta      : [batch, nheads, seqlen] bf16
+ *   A          : [nheads] fp32 (required); Dskip, dt_bias : [nheads] fp32 or NULL (0)
+ *   B, C       : [batch, ngroups, dstate, seqlen] bf16
+ *   h0, h_final: [batch, nheads * headdim, dstate] fp32, or NULL (zeros / not wanted)
+ * Supported: io = SSM_BF16, headdim = 64, dstate = 128, seqlen a multiple of
+ * 8 (16-byte rows); anything else returns SSM_ERR_UNSUPPORTED.  All pointers
+ * 16-byte aligned (SSM_ERR_MISALIGNED); outputs must not alias inputs.  The
+ * contractions take bf16 operands (the chunk's decayed mixer and the carried
+ * state are rounded to bf16 for them) and accumulate in fp32; the carried
+ * state itself stays fp32.  Asynchronous on stream; allocates nothing.
+ */
+ssm_status_t ssm_ssd_fwd(const void *x, const void *delta, const void *z, const float *A, const void *B,
+                         const void *C, const float *Dskip, const float *dt_bias, const float *h0, void *y,
+                         float *h_final, int batch, int nheads, int headdim, int dstate, int seqlen,
+                         int ngroups, ssm_dtype_t io, void *stream);
+
+/*
  * ssm_probe_alu_rates -- measurement helper (no counterpart on the source
  * pages): the arithmetic rates that bound the scan on the current device.
  * One state update needs one MUFU.EX2 (the decay exp(Delta A)) and four fp32

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libssmscan.so")
-SOURCES = [os.path.join(CSRC, f) for f in ("ssm_scan.cu", "scan_ws_bf16.cu", "scan_ws_f32.cu", "alu_probe.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("ssm_scan.cu", "scan_ws_bf16.cu", "scan_ws_f32.cu", "alu_probe.cu", "ssd.cu")]
 OBJDIR = os.path.join(HERE, "_build")
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))] + \
     [os.path.join(INCLUDE, "ssm_scan.h")]

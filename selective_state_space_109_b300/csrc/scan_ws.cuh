@@ -183,7 +183,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
         auto widen = [&](int i) {
             const int s = i % STAGES;
             unsigned char* st = stage_ptr(s);
-            if (!mbar_wait(&full_bar[s], static_cast<uint32_t>((i / STAGES) & 1), p.status)) {
+            if (!mbar_wait(&full_bar[s], static_cast<uint32_t>((i / STAGES) & 1), p.status, p.wait_budget_ns)) {
                 ok = false;  // its consumers give up on the ready barrier in turn
                 return;
             }
@@ -206,10 +206,11 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
         };
 #pragma unroll 1
         for (int k = 0; k < nt && ok; ++k) {
+            if (k == p.stop_tile) break;  // failure injection: no load for this tile or any later one
             const int s = k % STAGES;
             if (k >= STAGES) {
                 // Tile k - STAGES's consumers are done with this stage.
-                if (!mbar_wait(&empty_bar[s], static_cast<uint32_t>(((k / STAGES) - 1) & 1), p.status)) {
+                if (!mbar_wait(&empty_bar[s], static_cast<uint32_t>(((k / STAGES) - 1) & 1), p.status, p.wait_budget_ns)) {
                     ok = false;
                     break;
                 }
@@ -233,7 +234,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
         // Loads still in flight (a wait gave up): wait for them before the CTA
         // may exit, so that no copy lands in shared memory it no longer owns.
         for (int i = widened; i < issued; ++i) {
-            mbar_wait(&full_bar[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.status);
+            mbar_wait(&full_bar[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1), p.status, p.wait_budget_ns);
         }
         return;
     }
@@ -290,7 +291,9 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
         for (int i = 0; i < nt; ++i) {
             const int s = i % STAGES;
             const uint32_t par = static_cast<uint32_t>((i / STAGES) & 1);
-            if (!mbar_wait(&full_bar[s], par, p.status) || !mbar_wait(&ready_bar[s], par, p.status)) break;
+            if (!mbar_wait(&full_bar[s], par, p.status, p.wait_budget_ns) ||
+                !mbar_wait(&ready_bar[s], par, p.status, p.wait_budget_ns))
+                break;
             const unsigned char* st = stage_ptr(s);
             const float* bcf = reinterpret_cast<const float*>(st + Lay::BCF_OFFSET);
             const int c = seg;
@@ -478,7 +481,9 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
         for (int i = 0; i < nt; ++i) {
             const int s = i % STAGES;
             const uint32_t par = static_cast<uint32_t>((i / STAGES) & 1);
-            if (!mbar_wait(&full_bar[s], par, p.status) || !mbar_wait(&ready_bar[s], par, p.status)) break;
+            if (!mbar_wait(&full_bar[s], par, p.status, p.wait_budget_ns) ||
+                !mbar_wait(&ready_bar[s], par, p.status, p.wait_budget_ns))
+                break;
             const unsigned char* st = stage_ptr(s);
             const unsigned char* u_t = st;
             const unsigned char* d_t = st + Lay::ACT_BYTES;

@@ -20,6 +20,11 @@ struct WsScanParams {
     int blocks_per_group;  // CTAs along the channels of one group
     int ntiles;            // ceil(seqlen / TS)
     int has_z;
+    // Failure injection for the tests of the bounded waits: the producer
+    // stops issuing loads at this tile (-1: never), and every wait gives up
+    // after wait_budget_ns.
+    int stop_tile;
+    unsigned long long wait_budget_ns;
 };
 
 // TMA descriptors of one call: the [batch * ngroups, dim_per_group, seqlen]

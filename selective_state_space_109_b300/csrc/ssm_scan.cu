@@ -604,6 +604,12 @@ ssm_status_t run_scan_ws(const void* u, const void* delta, const void* z, const 
     p.blocks_per_group = (dpg + ch - 1) / ch;
     p.ntiles = (seqlen + ts - 1) / ts;
     p.has_z = z != nullptr;
+    // Failure injection for the tests of the bounded waits (off unless set):
+    // the producer stops loading at tile SSM_DEBUG_STOP_LOADS_AT_TILE, and the
+    // waits give up after SSM_DEBUG_WAIT_BUDGET_US microseconds.
+    p.stop_tile = env_int("SSM_DEBUG_STOP_LOADS_AT_TILE", -1);
+    const int budget_us = env_int("SSM_DEBUG_WAIT_BUDGET_US", 0);
+    p.wait_budget_ns = budget_us > 0 ? static_cast<unsigned long long>(budget_us) * 1000ull : ssm::kWaitBudgetNs;
     const cudaError_t e = io == SSM_F32 ? ssm::ws_launch_f32(dstate, plan.lanes, plan.nw, plan.seg, m, p, st)
                                         : ssm::ws_launch_bf16(dstate, plan.lanes, plan.nw, plan.seg, m, p, st);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -71,12 +71,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete; bounded by
-// kWaitBudgetNs of wall time.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+// budget_ns of wall time (kWaitBudgetNs unless the caller gives another).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          unsigned long long budget_ns = kWaitBudgetNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long start = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - start > kWaitBudgetNs) {
+        if (global_timer_ns() - start > budget_ns) {
             atomicOr(&g_ssm_device_error, kDeviceErrTimeout);
             if (status) atomicOr(status, kDeviceErrTimeout);
             return false;

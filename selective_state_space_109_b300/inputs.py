@@ -157,6 +157,48 @@ def decode_params(dim, dstate, recipe="scaled", seed=0, device="cpu"):
     return dict(A=a_values(dim, dstate, device), D=D, dt_bias=dt_bias_values(dim, seed, device))
 
 
+def make_ssd_inputs(batch, nheads, headdim, dstate, seqlen, ngroups=1, io="bf16", seed=0, device="cpu",
+                    with_z=True, with_h0=False) -> dict:
+    """Inputs of the SSD (Mamba-2) layer: x, z ~ N(0, 1) [batch, nheads *
+    headdim, L]; delta ~ N(0, 1) [batch, nheads, L]; B, C ~ N(0, 1/N) [batch, G,
+    N, L] (all in the I/O type); per head A = -U(1, 16) (the A = -(n+1) range of
+    the scan workloads as one scalar per head), D ~ N(1, 0.1^2) and dt_bias =
+    softplus^-1(dt) with dt log-uniform on [1e-3, 1e-1] (fp32); h0 ~ N(0, 1)."""
+    dt = io_torch_dtype(io)
+    dim = nheads * headdim
+    act = (batch, dim, seqlen)
+    bc = (batch, ngroups, dstate, seqlen)
+    g = _gen(seed, "A", "cpu", step=11)
+    out = dict(
+        x=_randn(act, seed, "u", "cpu").to(dt),
+        delta=_randn((batch, nheads, seqlen), seed, "delta", "cpu").to(dt),
+        z=_randn(act, seed, "z", "cpu").to(dt) if with_z else None,
+        A=-(1.0 + 15.0 * torch.rand(nheads, generator=g, dtype=torch.float32)),
+        B=(_randn(bc, seed, "B", "cpu") / math.sqrt(dstate)).to(dt),
+        C=(_randn(bc, seed, "C", "cpu") / math.sqrt(dstate)).to(dt),
+        D=1.0 + 0.1 * _randn((nheads,), seed, "D", "cpu"),
+        dt_bias=dt_bias_values(nheads, seed, "cpu"),
+        h0=_randn((batch, dim, dstate), seed, "h0", "cpu") if with_h0 else None,
+    )
+    return {k: (v.contiguous().to(device) if v is not None else None) for k, v in out.items()}
+
+
+def compulsory_bytes_ssd(batch, nheads, headdim, dstate, seqlen, ngroups, io="bf16") -> int:
+    """x, z, y ([batch, nheads * headdim, L] each), delta ([batch, nheads, L])
+    and B, C ([batch, G, N, L] each)."""
+    s = 4 if io == "f32" else 2
+    return (3 * batch * nheads * headdim * seqlen + batch * nheads * seqlen + 2 * batch * ngroups * dstate * seqlen) * s
+
+
+def flops_ssd_chunked(batch, nheads, headdim, dstate, seqlen, chunk=128) -> int:
+    """Dense-contraction FLOPs of the chunked SSD evaluation (2 per multiply-add):
+    per chunk and head C B^T (Q x Q over N), the mixer times x (Q x P over Q),
+    the chunk state (N x P over Q) and the carried-state readout (Q x P over N)."""
+    nch = -(-seqlen // chunk)
+    Q, P, N = chunk, headdim, dstate
+    return 2 * batch * nheads * nch * (Q * Q * N + Q * P * Q + N * P * Q + Q * P * N)
+
+
 # Named workloads: the sizes of the five synthetic workloads this library is
 # checked and measured on.
 def make_conv_inputs(batch, dim, seqlen, width=4, io="bf16", seed=0, device="cpu", with_prev=False):
@@ -222,6 +264,9 @@ WORKLOADS = {
                                           ngroups=1, io="bf16", recipe="scaled"),
     "decode_b256_d5120": dict(kind="decode", batch=256, dim=5120, dstate=16, ngroups=1,
                               io="bf16", recipe="scaled", steps=1024),
+    # SSD (Mamba-2) layer: 64 heads of 64 channels (4096 channels), N 128, L 2048.
+    "ssd_bf16_b2_h64_p64_n128_l2048": dict(kind="ssd", batch=2, nheads=64, headdim=64, dstate=128,
+                                           seqlen=2048, ngroups=1, io="bf16"),
 }
 
 

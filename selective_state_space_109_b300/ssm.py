@@ -75,6 +75,8 @@ def _load() -> ctypes.CDLL:
     L.ssm_scan_bwd_workspace_size.restype = Z
     L.ssm_scan_bwd.argtypes = [P] * 20 + [I] * 6 + [P, Z, P]
     L.ssm_scan_bwd.restype = I
+    L.ssm_ssd_fwd.argtypes = [P] * 11 + [I] * 7 + [P]
+    L.ssm_ssd_fwd.restype = I
     D = ctypes.POINTER(ctypes.c_double)
     L.ssm_probe_alu_rates.argtypes = [P, D, D, P]
     L.ssm_probe_alu_rates.restype = I
@@ -212,6 +214,43 @@ def device_status(clear: bool = False, device=None) -> int:
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return int(lib.ssm_device_status(int(bool(clear)), _stream_handle(dev)))
+
+
+def ssd_fwd(x, delta, A, B, C, z=None, D=None, dt_bias=None, h0=None, *, headdim, out=None, h_final=None,
+            return_final_state=False):
+    """SSD (Mamba-2) layer: x, z [batch, nheads * headdim, L] bf16; delta
+    [batch, nheads, L] bf16; A, D, dt_bias [nheads] fp32; B, C [batch, G, N, L]
+    bf16; h0 [batch, nheads * headdim, N] fp32.  Returns y (and h_final)."""
+    if x.device.type != "cuda" or x.dim() != 3 or B.dim() != 4:
+        raise ValueError("expected CUDA tensors x [batch, dim, L], B [batch, G, N, L]")
+    batch, dim, L = x.shape
+    if dim % headdim != 0:
+        raise ValueError("the channel count must be a multiple of headdim")
+    nheads = dim // headdim
+    G, N = B.shape[1], B.shape[2]
+    dev, io = x.device, x.dtype
+    _check(x, "x", (batch, dim, L), io, dev)
+    _check(delta, "delta", (batch, nheads, L), io, dev)
+    _check(z, "z", (batch, dim, L), io, dev)
+    _check(A, "A", (nheads,), torch.float32, dev)
+    _check(B, "B", (batch, G, N, L), io, dev)
+    _check(C, "C", (batch, G, N, L), io, dev)
+    _check(D, "D", (nheads,), torch.float32, dev)
+    _check(dt_bias, "dt_bias", (nheads,), torch.float32, dev)
+    _check(h0, "h0", (batch, dim, N), torch.float32, dev)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", x.shape, io, dev)
+    hf = h_final
+    if return_final_state and hf is None:
+        hf = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    _check(hf, "h_final", (batch, dim, N), torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib.ssm_ssd_fwd(_ptr(x), _ptr(delta), _ptr(z), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                             _ptr(h0), _ptr(y), _ptr(hf), batch, nheads, headdim, N, L, G, _io_code(io),
+                             _stream_handle(dev))
+    if st != 0:
+        raise SsmError(st, "ssm_ssd_fwd")
+    return (y, hf) if (return_final_state or h_final is not None) else y
 
 
 def probe_alu_rates(device=None) -> dict:

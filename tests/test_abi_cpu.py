@@ -190,3 +190,21 @@ def test_bwd_argument_errors(lib):
     assert lib.ssm_scan_bwd_workspace_size(1, 4, 16, 128, 1, 1) == 0   # one chunk: no workspace
     assert lib.ssm_scan_bwd_workspace_size(2, 4, 64, 129, 1, 1) == 3 * 2 * 4 * 64 * 3 * 4
     assert bwd(batch=0, u=None, dy=None, du=None, dd=None, dA=None, dB=None, dC=None) == 0  # empty problem
+
+
+def ssd(lib, x=P, delta=P, z=None, A=P, B=P, C=P, D=None, bias=None, h0=None, y=P, hf=None,
+        batch=1, nheads=2, P_=64, N=128, L=64, G=1, io=1):
+    return lib.ssm_ssd_fwd(x, delta, z, A, B, C, D, bias, h0, y, hf, batch, nheads, P_, N, L, G, io, None)
+
+
+def test_ssd_argument_checks(lib):
+    assert ssd(lib, io=0) == 2            # fp32 I/O: the tensor-core path is bf16 only
+    assert ssd(lib, P_=32) == 2           # head dimension other than 64
+    assert ssd(lib, N=64) == 2            # state size other than 128
+    assert ssd(lib, L=12) == 2            # rows not whole 16-byte packets
+    assert ssd(lib, nheads=3, G=2) == 1   # heads do not split into the groups
+    assert ssd(lib, nheads=0) == 1
+    assert ssd(lib, y=None) == 1          # missing output
+    assert ssd(lib, A=None) == 1
+    assert ssd(lib, x=MIS) == 3           # misaligned input
+    assert ssd(lib, batch=0) == 0         # nothing to do
