@@ -176,7 +176,7 @@ def measured_peaks():
 # Device sources of the chunked forward call's kernels (summary, carry and
 # fused passes): a DRAM-traffic record stays valid while these and the launch
 # plan are unchanged.
-FWD_SCAN_SOURCES = ("scan_tma.cuh", "scan_ws.cuh", "scan_ws_inst.cuh", "tma.cuh", "ssm_device.cuh")
+FWD_SCAN_SOURCES = ("scan_tma.cuh", "tma.cuh", "ssm_device.cuh")
 
 
 def kernel_source_hash(names=FWD_SCAN_SOURCES):
@@ -190,9 +190,10 @@ def kernel_source_hash(names=FWD_SCAN_SOURCES):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key: str, plan=None):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources and launch plan; else None."""
+def ncu_record(kernel_key: str, plan=None):
+    """The committed ncu record of one call (DRAM bytes and serialised time per
+    kernel), if it was taken on the current kernel sources and launch plan;
+    else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -203,7 +204,7 @@ def ncu_traffic(kernel_key: str, plan=None):
         return None
     if plan is not None and rec.get("plan") != plan:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return rec
 
 
 def n_rotating_sets(bytes_per_set: int, l2_bytes: int) -> int:
@@ -715,7 +716,23 @@ def run_ours(args):
     alu_achieved = r["upd_per_step"] / per_launch_s / 1e9
     upd_per_sm_ns = min(alu["ex2_per_sm_ns"], alu["ffma_per_sm_ns"] / 4.0)
     alu_peak = sms * upd_per_sm_ns  # Gupd/s
-    traffic = ncu_traffic("scan_chunked_call/" + HEADLINE, r["plan"])
+    rec = ncu_record("scan_chunked_call/" + HEADLINE, r["plan"])
+    traffic = rec.get("dram_bytes_per_launch") if rec else None
+    dominant = None
+    if rec and rec.get("kernel_ns"):
+        # The call's dominant kernel: its share of the call from the committed
+        # ncu launch record (serialised, cold), applied to the live call time.
+        tot = sum(rec["kernel_ns"].values())
+        name, ns = max(rec["kernel_ns"].items(), key=lambda kv: kv[1])
+        share = ns / tot
+        t_dom = per_launch_s * share
+        dominant = {"kernel": name, "share_of_call": round(share, 4),
+                    "us_per_launch": round(t_dom * 1e6, 1),
+                    "achieved": round(r["upd_per_step"] / t_dom / 1e9, 1), "unit": "Gupd/s",
+                    "frac": round(r["upd_per_step"] / t_dom / 1e9 / alu_peak, 4),
+                    "traffic": rec["kernels"].get(name),
+                    "basis": "one pass's state updates over the kernel's share of the live call time; share and "
+                             "DRAM bytes from the committed ncu record of the same call (profiles/traffic.json)"}
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -750,9 +767,15 @@ def run_ours(args):
                                     f"{upd_per_sm_ns:.2f} updates per SM per ns x {sms} SMs (nominal: "
                                     f"{NOMINAL_UPDATES_PER_SM_CLK:.0f}/SM/clk x {sm_max:.0f} MHz = "
                                     f"{sms * sm_max * 1e-3 * NOMINAL_UPDATES_PER_SM_CLK:.0f} Gupd/s)"),
+                     "update_mix_ceiling": {"achieved_by_bare_mix": round(alu["mix_updates_per_sm_ns"] * sms, 1),
+                                            "unit": "Gupd/s",
+                                            "frac_of_peak": round(alu["mix_updates_per_sm_ns"] / upd_per_sm_ns, 4),
+                                            "note": "the scan's per-state instruction mix alone (no per-step "
+                                                    "scalars, loads or stores), eight warps per scheduler"},
                      "scope": "the whole chunked call (summary, carry and fused passes) against the "
                               "updates of one pass; the summary pass recomputes the decays of all chunks "
-                              "but the last"},
+                              "but the last",
+                     "dominant_kernel": dominant},
         "hbm_roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "peak_source": peak_src, "traffic": traffic},
@@ -909,23 +932,31 @@ def write_traffic(csv_path, workload):
         rows = [r for r in csv.reader(f) if r]
     hdr = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
     cols = rows[hdr]
-    launches = {}
+    launches, times = {}, {}
     for r in rows[hdr + 1:]:
         if len(r) != len(cols):
             continue
         d = dict(zip(cols, r))
-        if not any(k in d["Kernel Name"] for k in ("scan_tma_kernel", "scan_fwd_kernel", "scan_carry_kernel")):
+        if not any(k in d["Kernel Name"] for k in ("scan_tma_kernel", "scan_fwd_kernel", "scan_carry_kernel",
+                                                    "scan_ws_kernel")):
             continue
         name = d["Kernel Name"].split("(")[0]
         unit = d.get("Metric Unit", "byte")
-        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(unit, 1)
         key = (d["ID"], name)
         launches.setdefault(key, 0.0)
         if d["Metric Name"] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(unit, 1)
             launches[key] += float(d["Metric Value"].replace(",", "")) * scale
-    for (_, name), b in launches.items():
+        elif d["Metric Name"] == "gpu__time_duration.sum":
+            scale = {"ns": 1, "nsecond": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}.get(unit, 1)
+            times[key] = float(d["Metric Value"].replace(",", "")) * scale
+    per_time = {}
+    for (i, name), b in launches.items():
         per_kernel.setdefault(name, []).append(b)
+        if (i, name) in times:
+            per_time.setdefault(name, []).append(times[(i, name)])
     kernels = {k: sum(v) / len(v) for k, v in per_kernel.items()}
+    kernel_ns = {k: sum(v) / len(v) for k, v in per_time.items()}
     from selective_state_space_109_b300 import inputs as I
     from selective_state_space_109_b300 import ssm
     w = I.WORKLOADS[workload]
@@ -939,6 +970,7 @@ def write_traffic(csv_path, workload):
     data["scan_chunked_call/" + workload] = {
         "dram_bytes_per_launch": round(sum(kernels.values())),
         "kernels": {k: round(v) for k, v in kernels.items()},
+        "kernel_ns": {k: round(v) for k, v in kernel_ns.items()},
         "source_hash": kernel_source_hash(),
         "plan": plan,
         "from": os.path.basename(csv_path)}

@@ -425,10 +425,15 @@ ssm_status_t ssm_ssd_fwd(const void *x, const void *delta, const void *z, const 
  * occupied by independent chains of one operation, synchronises, and writes:
  *   *ex2_per_sm_ns  : MUFU.EX2 results per SM per nanosecond
  *   *ffma_per_sm_ns : fp32 FMAs per SM per nanosecond
+ *   *mix_updates_per_sm_ns (may be NULL): state updates per SM per nanosecond
+ *                     of the scan's own per-state instruction mix (B, C from
+ *                     shared memory, eight state pairs per thread, eight warps
+ *                     per scheduler): what that mix can issue at best
  * sink: a device float the kernels may write (they never do in practice).
  * Errors: SSM_ERR_INVALID_ARG (NULL pointer), SSM_ERR_CUDA.
  */
-ssm_status_t ssm_probe_alu_rates(float *sink, double *ex2_per_sm_ns, double *ffma_per_sm_ns, void *stream);
+ssm_status_t ssm_probe_alu_rates(float *sink, double *ex2_per_sm_ns, double *ffma_per_sm_ns,
+                                 double *mix_updates_per_sm_ns, void *stream);
 
 #ifdef __cplusplus
 }

@@ -78,7 +78,7 @@ def _load() -> ctypes.CDLL:
     L.ssm_ssd_fwd.argtypes = [P] * 11 + [I] * 7 + [P]
     L.ssm_ssd_fwd.restype = I
     D = ctypes.POINTER(ctypes.c_double)
-    L.ssm_probe_alu_rates.argtypes = [P, D, D, P]
+    L.ssm_probe_alu_rates.argtypes = [P, D, D, D, P]
     L.ssm_probe_alu_rates.restype = I
     return L
 
@@ -258,12 +258,13 @@ def probe_alu_rates(device=None) -> dict:
     ssm_probe_alu_rates in the C header); synchronises."""
     dev = torch.device("cuda") if device is None else torch.device(device)
     sink = torch.zeros(1, dtype=torch.float32, device=dev)
-    ex2, ffma = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    ex2, ffma, mix = ctypes.c_double(0.0), ctypes.c_double(0.0), ctypes.c_double(0.0)
     with torch.cuda.device(dev):
-        st = lib.ssm_probe_alu_rates(_ptr(sink), ctypes.byref(ex2), ctypes.byref(ffma), _stream_handle(dev))
+        st = lib.ssm_probe_alu_rates(_ptr(sink), ctypes.byref(ex2), ctypes.byref(ffma), ctypes.byref(mix),
+                                     _stream_handle(dev))
     if st != 0:
         raise SsmError(st, "ssm_probe_alu_rates")
-    return dict(ex2_per_sm_ns=ex2.value, ffma_per_sm_ns=ffma.value)
+    return dict(ex2_per_sm_ns=ex2.value, ffma_per_sm_ns=ffma.value, mix_updates_per_sm_ns=mix.value)
 
 
 def state_update(state, u, delta, A, B, C, z=None, D=None, dt_bias=None, *, out=None,
