@@ -224,6 +224,20 @@ ssm_status_t ssm_scan_fwd_chunked_static(const void *u, const void *delta, const
 ssm_status_t ssm_device_status(int clear, void *stream);
 
 /*
+ * Measurement hook.  Registers two CUDA events (cudaEvent_t, created by the
+ * caller, who keeps ownership) that every later forward scan call
+ * (ssm_scan_fwd, ssm_scan_fwd_chunked, ssm_scan_fwd_chunked_static) made from
+ * the calling host thread records on its stream: begin_event immediately
+ * before the launch of the fused pass (the kernel that writes y), end_event
+ * immediately after it.  cudaEventElapsedTime(begin, end) is then that
+ * kernel's device time.  The record between the passes stops the fused pass
+ * from starting early (programmatic dependent launch), so use it for timing
+ * the kernel, not the call.  NULL, NULL clears the hook.
+ * Errors: SSM_ERR_INVALID_ARG when exactly one of the two is NULL.
+ */
+ssm_status_t ssm_set_pass_timer(void *begin_event, void *end_event);
+
+/*
  * ssm_state_update -- one decode step: every sequence of the batch consumes
  * one token (cuishuaiwen.com "Mamba & State-Space Sequence Models", Core
  * mechanics: inference runs the recurrence, O(1) per step, with a state whose

@@ -34,6 +34,17 @@ __device__ unsigned int g_ssm_device_error = 0;
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+// Events that scan calls from this host thread record around the launch of
+// their fused pass (ssm_set_pass_timer); null when unset.
+thread_local cudaEvent_t g_pass_begin = nullptr;
+thread_local cudaEvent_t g_pass_end = nullptr;
+
+void mark_pass_begin(cudaStream_t st) {
+    if (g_pass_begin) cudaEventRecord(g_pass_begin, st);
+}
+void mark_pass_end(cudaStream_t st) {
+    if (g_pass_end) cudaEventRecord(g_pass_end, st);
+}
 
 ssm_status_t cuda_fail(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -506,9 +517,11 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
         e = launch_carry(agg, h0, batch, dim, dstate, plan.chunks, st);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    mark_pass_begin(st);
     e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st)
                       : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st);
     if (e != cudaSuccess) return cuda_fail(e);
+    mark_pass_end(st);
     return SSM_OK;
 }
 
@@ -610,9 +623,11 @@ ssm_status_t run_scan_ws(const void* u, const void* delta, const void* z, const 
     p.stop_tile = env_int("SSM_DEBUG_STOP_LOADS_AT_TILE", -1);
     const int budget_us = env_int("SSM_DEBUG_WAIT_BUDGET_US", 0);
     p.wait_budget_ns = budget_us > 0 ? static_cast<unsigned long long>(budget_us) * 1000ull : ssm::kWaitBudgetNs;
+    mark_pass_begin(st);
     const cudaError_t e = io == SSM_F32 ? ssm::ws_launch_f32(dstate, plan.lanes, plan.nw, plan.seg, m, p, st)
                                         : ssm::ws_launch_bf16(dstate, plan.lanes, plan.nw, plan.seg, m, p, st);
     if (e != cudaSuccess) return cuda_fail(e);
+    mark_pass_end(st);
     return SSM_OK;
 }
 
@@ -1156,6 +1171,13 @@ ssm_status_t ssm_workspace_status(const void* workspace, size_t workspace_bytes,
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e);
     return word == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
+}
+
+ssm_status_t ssm_set_pass_timer(void* begin_event, void* end_event) {
+    if ((begin_event == nullptr) != (end_event == nullptr)) return SSM_ERR_INVALID_ARG;
+    g_pass_begin = static_cast<cudaEvent_t>(begin_event);
+    g_pass_end = static_cast<cudaEvent_t>(end_event);
+    return SSM_OK;
 }
 
 ssm_status_t ssm_device_status(int clear, void* stream) {

@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
     L.ssm_scan_plan.restype = I
     L.ssm_device_status.argtypes = [I, P]
     L.ssm_device_status.restype = I
+    L.ssm_set_pass_timer.argtypes = [P, P]
+    L.ssm_set_pass_timer.restype = I
     L.ssm_state_update.argtypes = [P] * 10 + [I] * 5 + [P]
     L.ssm_state_update.restype = I
     L.ssm_scan_fwd_varlen.argtypes = [P] * 12 + [I] * 6 + [P]
@@ -214,6 +216,17 @@ def device_status(clear: bool = False, device=None) -> int:
     dev = torch.device("cuda") if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return int(lib.ssm_device_status(int(bool(clear)), _stream_handle(dev)))
+
+
+def set_pass_timer(begin=None, end=None) -> None:
+    """Registers two torch.cuda.Event objects (enable_timing=True) that later
+    forward scan calls from this thread record around the launch of their
+    fused pass; set_pass_timer() clears the hook."""
+    b = ctypes.c_void_p(begin.cuda_event) if begin is not None else None
+    e = ctypes.c_void_p(end.cuda_event) if end is not None else None
+    st = lib.ssm_set_pass_timer(b, e)
+    if st != 0:
+        raise SsmError(st, "ssm_set_pass_timer")
 
 
 def ssd_fwd(x, delta, A, B, C, z=None, D=None, dt_bias=None, h0=None, *, headdim, out=None, h_final=None,

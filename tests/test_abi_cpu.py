@@ -208,3 +208,12 @@ def test_ssd_argument_checks(lib):
     assert ssd(lib, A=None) == 1
     assert ssd(lib, x=MIS) == 3           # misaligned input
     assert ssd(lib, batch=0) == 0         # nothing to do
+
+
+def test_pass_timer_arguments(lib):
+    # Both events or neither: one alone is an argument error (checked on the
+    # host; the events are never touched without a GPU).
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.ssm_set_pass_timer(fake, None) == 1
+    assert lib.ssm_set_pass_timer(None, fake) == 1
+    assert lib.ssm_set_pass_timer(None, None) == 0
