@@ -44,10 +44,11 @@
  * - stream is a cudaStream_t (NULL = legacy default stream).  Every call is
  *   asynchronous on that stream; argument errors are returned before anything
  *   is enqueued.
- * - Supported dstate: 4, 8, 16, 32, 64, 128, 256 (others return SSM_ERR_UNSUPPORTED).
- *   dstate 128 and 256 run on the TMA-staged kernels only: the scans take them when
- *   seqlen * element size is a multiple of 16 bytes (SSM_ERR_UNSUPPORTED
- *   otherwise), ssm_scan_fwd_varlen not at all.
+ * - Supported dstate: 4, 8, 16, 32, 64, 128, 256 (others return SSM_ERR_UNSUPPORTED),
+ *   on every scan entry point and any seqlen (rows that are not whole 16-byte
+ *   packets, and the packed sequences of ssm_scan_fwd_varlen, take the
+ *   register-staged kernel, which holds the B/C tile of dstate 128 and 256 in
+ *   dynamic shared memory).
  * - batch == 0 is an empty problem: the call returns SSM_OK without touching
  *   any pointer.  seqlen == 0 is accepted: nothing is read or written except
  *   h_final (which then equals h0, or zeros).

@@ -70,7 +70,7 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_con
     constexpr int STAGES = Lay::STAGES;
     constexpr int P = N / 2;
 
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];  // aligned below at run time
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * Lay::STAGE_BYTES);
 

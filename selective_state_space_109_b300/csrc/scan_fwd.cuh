@@ -65,6 +65,10 @@ struct ScanParams {
     int nseq;
 };
 
+// The generic kernel keeps the widened B/C tile in dynamic shared memory
+// (single-buffered) from N = 128 on.
+__host__ __device__ constexpr bool scan_bc_dynamic(int n) { return n >= 128; }
+
 template <typename T, int LANES>
 struct ScanShape {
     // Steps owned by one lane per block: a 16-byte packet when few lanes share
@@ -88,9 +92,17 @@ scan_fwd_kernel(const ScanParams p) {
     constexpr int VE = Elem<T>::kPer16B;
     constexpr int THREADS = WARPS * 32;
     constexpr int BC_ITEMS = 2 * N * (TT / VE);  // 16-byte B/C packets per tile
-    constexpr int BC_PER_THREAD = (BC_ITEMS + THREADS - 1) / THREADS;
+    // N >= 128: the widened B/C tile (32 or 128 KB) lives in dynamic shared
+    // memory, single-buffered and staged between two barriers at each tile
+    // boundary (no register copy of the next tile).
+    constexpr bool DYN = scan_bc_dynamic(N);
+    constexpr int BUFS = DYN ? 1 : 2;
+    constexpr int BC_PER_THREAD = DYN ? 1 : (BC_ITEMS + THREADS - 1) / THREADS;
 
-    __shared__ __align__(16) float4 bc_s[2][TT][NQ];
+    __shared__ __align__(16) float4 bc_static[DYN ? 1 : 2][DYN ? 1 : TT][DYN ? 1 : NQ];
+    extern __shared__ __align__(16) float4 bc_dynamic[];
+    float4 (*bc_s)[TT][NQ] = DYN ? reinterpret_cast<float4 (*)[TT][NQ]>(bc_dynamic)
+                                 : reinterpret_cast<float4 (*)[TT][NQ]>(&bc_static[0][0][0]);
     // (Delta, Delta*u) per warp channel and step; one float2 of padding per
     // row spreads the rows of a warp over distinct banks.
     __shared__ __align__(16) float2 dd_s[WARPS][CPW][TB + 1];
@@ -164,44 +176,55 @@ scan_fwd_kernel(const ScanParams p) {
 
     // ---- B/C tile staging: global -> registers -> shared (fp32 quads) ----
     Packet<T, VE> bc_reg[BC_PER_THREAD];
+    auto load_item = [&](int item, int t0, Packet<T, VE>& pk) {
+        const int r = item % (2 * N);  // (n, B|C) row, fastest across threads
+        const int tv = item / (2 * N);
+        const int n = r >> 1;
+        const T* src = ((r & 1) ? Cg : Bg) + static_cast<long long>(n) * Lst + t0 + tv * VE;
+        const int valid = L - (t0 + tv * VE);
+        const long long boff = bc_off + static_cast<long long>(n) * Lst + t0 + tv * VE;
+        const long long bhi = boff + ((bc_vec_ok && valid >= VE) ? VE : min(max(valid, 0), VE));
+        if (valid > 0 && !in_range(boff, bhi, bc_size)) pk.zero();
+        else if (bc_vec_ok && valid >= VE) pk.load_cached(src);
+        else if (valid > 0) pk.load_partial(src, valid);
+        else pk.zero();
+    };
+    auto store_item = [&](int item, int buf, const Packet<T, VE>& pk) {
+        float* base = reinterpret_cast<float*>(&bc_s[buf][0][0]);
+        const int r = item % (2 * N);
+        const int tv = item / (2 * N);
+        const int n = r >> 1;
+        const int isC = r & 1;
+        // Pair k of sub-lane j sits at k * LANES + j: the lanes of a
+        // channel read adjacent quads (no bank conflicts).
+        const int q = n >> 1;
+        const int off = ((q % P) * LANES + q / P) * 4 + isC * 2 + (n & 1);
+        float f[VE];
+        pk.to_float(f);
+#pragma unroll
+        for (int k = 0; k < VE; ++k) base[(tv * VE + k) * (2 * N) + off] = f[k];
+    };
     auto load_bc = [&](int t0) {
 #pragma unroll
         for (int i = 0; i < BC_PER_THREAD; ++i) {
             const int item = threadIdx.x + i * THREADS;
-            if (item < BC_ITEMS) {
-                const int r = item % (2 * N);  // (n, B|C) row, fastest across threads
-                const int tv = item / (2 * N);
-                const int n = r >> 1;
-                const T* src = ((r & 1) ? Cg : Bg) + static_cast<long long>(n) * Lst + t0 + tv * VE;
-                const int valid = L - (t0 + tv * VE);
-                const long long boff = bc_off + static_cast<long long>(n) * Lst + t0 + tv * VE;
-                const long long bhi = boff + ((bc_vec_ok && valid >= VE) ? VE : min(max(valid, 0), VE));
-                if (valid > 0 && !in_range(boff, bhi, bc_size)) bc_reg[i].zero();
-                else if (bc_vec_ok && valid >= VE) bc_reg[i].load_cached(src);
-                else if (valid > 0) bc_reg[i].load_partial(src, valid);
-                else bc_reg[i].zero();
-            }
+            if (item < BC_ITEMS) load_item(item, t0, bc_reg[i]);
         }
     };
     auto store_bc = [&](int buf) {
-        float* base = reinterpret_cast<float*>(&bc_s[buf][0][0]);
 #pragma unroll
         for (int i = 0; i < BC_PER_THREAD; ++i) {
             const int item = threadIdx.x + i * THREADS;
-            if (item < BC_ITEMS) {
-                const int r = item % (2 * N);
-                const int tv = item / (2 * N);
-                const int n = r >> 1;
-                const int isC = r & 1;
-                // Pair k of sub-lane j sits at k * LANES + j: the lanes of a
-                // channel read adjacent quads (no bank conflicts).
-                const int q = n >> 1;
-                const int off = ((q % P) * LANES + q / P) * 4 + isC * 2 + (n & 1);
-                float f[VE];
-                bc_reg[i].to_float(f);
-#pragma unroll
-                for (int k = 0; k < VE; ++k) base[(tv * VE + k) * (2 * N) + off] = f[k];
-            }
+            if (item < BC_ITEMS) store_item(item, buf, bc_reg[i]);
+        }
+    };
+    // Single-buffered tiles: load and widen item by item.
+    auto stage_bc = [&](int t0) {
+#pragma unroll 2
+        for (int item = threadIdx.x; item < BC_ITEMS; item += THREADS) {
+            Packet<T, VE> pk;
+            load_item(item, t0, pk);
+            store_item(item, 0, pk);
         }
     };
 
@@ -222,16 +245,22 @@ scan_fwd_kernel(const ScanParams p) {
 
     const int ntiles = (L + TT - 1) / TT;
     if (ntiles > 0) {
-        load_bc(0);
-        store_bc(0);
+        if constexpr (DYN) {
+            stage_bc(0);
+        } else {
+            load_bc(0);
+            store_bc(0);
+        }
         load_act(0, pd_cur, pu_cur, pz_cur);
     }
     __syncthreads();
 
     for (int tile = 0; tile < ntiles; ++tile) {
-        const int buf = tile & 1;
+        const int buf = BUFS == 2 ? (tile & 1) : 0;
         const int t0 = tile * TT;
-        if (tile + 1 < ntiles) load_bc(t0 + TT);
+        if constexpr (!DYN) {
+            if (tile + 1 < ntiles) load_bc(t0 + TT);
+        }
 
 #pragma unroll 1
         for (int blk = 0; blk < TT / TB; ++blk) {
@@ -305,7 +334,14 @@ scan_fwd_kernel(const ScanParams p) {
             __syncwarp();
         }
 
-        if (tile + 1 < ntiles) store_bc(buf ^ 1);
+        if constexpr (DYN) {
+            if (tile + 1 < ntiles) {
+                __syncthreads();  // every lane has read this tile
+                stage_bc(t0 + TT);
+            }
+        } else {
+            if (tile + 1 < ntiles) store_bc(buf ^ 1);
+        }
         __syncthreads();
     }
 

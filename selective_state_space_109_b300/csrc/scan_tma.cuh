@@ -226,7 +226,7 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
     // Align the dynamic shared memory to 1024 bytes by offsetting the shared
     // array itself, so that every access below stays a shared-memory access.
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];  // aligned below at run time
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     float* bcf = reinterpret_cast<float*>(smem + STAGES * Lay::STAGE_BYTES);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFFSET);

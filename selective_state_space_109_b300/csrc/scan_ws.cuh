@@ -131,7 +131,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
     static_assert(S >= 2 && S % 2 == 0, "each lane holds an even number of states");
     static_assert(SEG == 1 || LANES > 1, "the time-segmented variant shares its scalars through the scratch rows");
 
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];  // aligned below at run time
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFFSET);
     uint64_t* ready_bar = full_bar + STAGES;

@@ -77,17 +77,15 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
         return SSM_OK;
     }
     if (!encode_tiled_fn()) return SSM_ERR_CUDA;
-    CUtensorMap mx, mz, my, mb, mc;
+    CUtensorMap mx, mb, mc;
     const bool ok = encode_rows(&mx, x, batch * dim, seqlen, ssm::ssd::P) &&
-                    encode_rows(&my, y, batch * dim, seqlen, ssm::ssd::P) &&
-                    (z ? encode_rows(&mz, z, batch * dim, seqlen, ssm::ssd::P) : true) &&
                     encode_rows(&mb, B, static_cast<long long>(batch) * ngroups * dstate, seqlen, ssm::ssd::N) &&
                     encode_rows(&mc, C, static_cast<long long>(batch) * ngroups * dstate, seqlen, ssm::ssd::N);
     if (!ok) return SSM_ERR_CUDA;
-    if (!z) mz = mx;  // never read: has_z = 0
     ssm::SsdParams p{};
     p.delta = static_cast<const __nv_bfloat16*>(delta);
-    p.A = A; p.D = Dskip; p.dt_bias = dt_bias; p.h0 = h0; p.h_final = h_final; p.status = nullptr;
+    p.A = A; p.D = Dskip; p.dt_bias = dt_bias; p.h0 = h0; p.h_final = h_final;
+    p.y = static_cast<__nv_bfloat16*>(y); p.z = static_cast<const __nv_bfloat16*>(z); p.status = nullptr;
     p.batch = batch; p.nheads = nheads; p.seqlen = seqlen; p.ngroups = ngroups; p.has_z = z != nullptr;
 
     static std::atomic<unsigned long long> done{0};
@@ -102,7 +100,6 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
     }
     const long long grid = static_cast<long long>(batch) * nheads;
     if (grid > 0x7fffffffLL) return SSM_ERR_INVALID_ARG;
-    ssm::ssd_fwd_kernel<<<static_cast<unsigned>(grid), ssm::ssd::THREADS, ssm::ssd::SMEM_BYTES, st>>>(mx, mz, my, mb,
-                                                                                                        mc, p);
+    ssm::ssd_fwd_kernel<<<static_cast<unsigned>(grid), ssm::ssd::THREADS, ssm::ssd::SMEM_BYTES, st>>>(mx, mb, mc, p);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

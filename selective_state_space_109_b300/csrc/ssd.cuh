@@ -16,17 +16,26 @@
 //   y      = (Ydiag + Yoff + Dskip x) * silu(z)
 //
 // One CTA walks one (sequence, head) through its chunks in order, so the state
-// H stays on chip (fp32 in registers, half a state row per thread; a bf16 copy
-// in shared memory feeds the next chunk's Yoff).  Thread 0 issues the TMA
-// loads of each chunk's C, B, x, z tiles (128-byte swizzled rows of 64 steps;
-// x and z one chunk ahead, C and B as soon as the first contractions have read
-// the current ones) and the tcgen05.mma contractions (bf16 operands from shared
-// memory, fp32 accumulators in tensor memory).  The 256 threads -- two
-// warpgroups, each owning the 128 tensor-memory lanes for half of every
-// accumulator row's columns -- build the computed operands (M, w o X, H), read
-// the accumulators back with tcgen05.ld and form y, which leaves by a TMA
-// store.  Operand layouts are the 128-byte-swizzled K-major or MN-major tiles
-// of the UMMA descriptors; every wait is bounded.
+// H stays on chip (fp32 in registers, a 16-channel slice of a state row per
+// thread; a bf16 copy in shared memory feeds the next chunk's Yoff).  A
+// control warp issues the TMA loads of each chunk's C, B and x tiles
+// (128-byte swizzled rows of 64 steps; x two chunks ahead, C and B as soon
+// as the previous chunk's contractions have read them), the
+// tcgen05.mma contractions (bf16 operands from shared memory, fp32
+// accumulators in tensor memory, issued by one thread), and computes the
+// per-step scalars (Delta, the running sum of Delta A, the state weights w)
+// two chunks ahead.  Sixteen compute warps -- four per quarter of the 128
+// tensor-memory lanes, each taking a quarter of every accumulator row's
+// columns -- build the computed operands (M, w o X, H), read the accumulators
+// back with tcgen05.ld, read z and write y straight from and to global memory
+// (per warp and channel, 32 consecutive steps).  The chunks are
+// software-pipelined so that
+// the tensor cores run while the threads compute: Yd(c) = M X runs while the
+// compute warps weight chunk c+1's x, and G, S, Yoff of chunk c+1 run while
+// they form chunk c's output.  Only the lower triangle of M (s <= t) is
+// computed; its upper blocks are written as zeros.  Operand layouts are the
+// 128-byte-swizzled K-major or MN-major tiles of the UMMA descriptors; every
+// wait is bounded.
 #pragma once
 
 #include <cuda.h>
@@ -46,6 +55,8 @@ struct SsdParams {
     const float* dt_bias;        // [nheads] or null
     const float* h0;             // [batch, nheads * P, N] or null
     float* h_final;              // [batch, nheads * P, N] or null
+    const __nv_bfloat16* z;      // [batch, nheads * P, L] or null
+    __nv_bfloat16* y;            // [batch, nheads * P, L]
     unsigned int* status;        // null (device error word only)
     int batch, nheads, seqlen, ngroups;
     int has_z;
@@ -56,36 +67,42 @@ namespace ssd {
 constexpr int Q = 128;   // chunk length (the MMA's M for the per-step rows)
 constexpr int P = 64;    // head dimension
 constexpr int N = 128;   // state size
-constexpr int THREADS = 256;  // two warpgroups: each takes half the columns of every accumulator row
+constexpr int COMPUTE = 512;          // sixteen compute warps: lane quarter = warp % 4, column group = warp / 4
+constexpr int THREADS = COMPUTE + 32; // and one control warp (TMA, MMA issue, per-step scalars)
+constexpr int CTRL = COMPUTE;         // the control warp's first thread
+constexpr int CG = COMPUTE / 128;     // column groups (each a quarter of an accumulator row's columns)
 
 // Shared-memory layout (bytes from a 1024-aligned base).  Tiles of 128-byte
-// rows, two halves of 64 steps along time where a row holds 128 steps.  x and
-// z are double-buffered (the next chunk's tiles load during this chunk); C
-// and B are reloaded as soon as the first contractions have read them.
+// rows, two halves of 64 steps along time where a row holds 128 steps.  x has
+// three buffers (its tile loads two chunks ahead); C and B are reloaded as
+// soon as the contractions of the chunk have read them.  z is read by the
+// output step straight from global memory.
+constexpr int XBUFS = 3;                      // x buffers
 constexpr int CS_OFF = 0;                     // C  [N rows][Q]   (2 halves of N x 128 B)
 constexpr int BS_OFF = CS_OFF + N * 256;      // B  [N rows][Q]
-constexpr int XS_OFF = BS_OFF + N * 256;      // x  [P rows][Q], two buffers
-constexpr int ZS_OFF = XS_OFF + 2 * P * 256;  // z  [P rows][Q], two buffers
-constexpr int XH_OFF = ZS_OFF + 2 * P * 256;  // w o x, bf16 head  [P rows][Q] (B operand of S); y staging
+constexpr int XS_OFF = BS_OFF + N * 256;      // x  [P rows][Q], XBUFS buffers
+constexpr int XH_OFF = XS_OFF + XBUFS * P * 256;  // w o x, bf16 head  [P rows][Q] (B operand of S)
 constexpr int XL_OFF = XH_OFF + P * 256;      // w o x, bf16 tail (the rounding error of the head)
 constexpr int MS_OFF = XL_OFF + P * 256;      // M  [Q rows][Q]     (A operand of Ydiag)
 constexpr int HS_OFF = MS_OFF + Q * 256;      // H  [N rows][P]     (bf16 copy, B operand of Yoff)
-constexpr int F_OFF = HS_OFF + N * 128;       // floats: Delta[Q], cs[Q], w[Q], warp sums[8]
-constexpr int BAR_OFF = F_OFF + (3 * Q + 8) * 4;
-constexpr int SMEM_BYTES = BAR_OFF + 64 + 1024;  // four mbarriers, the TMEM address, alignment slack
-constexpr int XBUF = P * 256;                     // bytes of one x (or z) buffer
+constexpr int F_OFF = HS_OFF + N * 128;       // floats, two buffers of: (cs_t, Delta_t) pairs [Q], w_t [Q]
+constexpr int F_BUF = 3 * Q;                  // floats per buffer
+constexpr int BAR_OFF = F_OFF + 2 * F_BUF * 4;
+constexpr int SMEM_BYTES = BAR_OFF + 64 + 1024;  // six mbarriers, the TMEM address, alignment slack
+constexpr int XBUF = P * 256;                     // bytes of one x buffer
 constexpr int HALF_C = N * 128;                   // byte stride between the time halves of C, B
-constexpr int HALF_X = P * 128;                   // ... of x, z, w o x, y
+constexpr int HALF_X = P * 128;                   // ... of x, w o x
 constexpr int HALF_M = Q * 128;                   // ... of M
 constexpr uint32_t TX_BC = 2u * N * 256u;         // bytes of one chunk's C and B tiles
-constexpr uint32_t TX_X = P * 256u;               // ... of its x (or z) tile
+constexpr uint32_t TX_X = P * 256u;               // ... of its x tile
 static_assert(SMEM_BYTES <= 227 * 1024, "the SSD kernel's shared memory exceeds a CTA's limit");
+static_assert(COMPUTE == 4 * 128 && P == 16 * CG && Q == 32 * CG, "warp roles assume 16 warps, P 64, Q 128");
 
 // Tensor-memory columns (512 allocated; lanes = rows of the accumulators).
 constexpr uint32_t TM_G = 0;      // G      [Q lanes x Q]
-constexpr uint32_t TM_YOFF = 128; // Yoff   [Q lanes x P]
+constexpr uint32_t TM_S = 128;    // S      [N lanes x P]
 constexpr uint32_t TM_YD = 192;   // Ydiag  [Q lanes x P]
-constexpr uint32_t TM_S = 256;    // S      [N lanes x P]
+constexpr uint32_t TM_YOFF = 256; // Yoff   [Q lanes x P], two buffers (chunk parity)
 
 // Byte offset of element c (0..63) of row r in a tile of 128-byte rows written
 // with the 128-byte swizzle (16-byte unit index XOR row % 8).
@@ -155,6 +172,47 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns of this thread's tensor-memory lane (load and
+// wait in one asm statement, as above).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two 16-column loads of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16], float (&b)[16]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[i] = __uint_as_float(r[i]);
+        b[i] = __uint_as_float(r[16 + i]);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&pr);
+}
+
 __device__ __forceinline__ float bf_at(const unsigned char* tile, uint32_t off) {
     return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(tile + off)) << 16);
 }
@@ -168,46 +226,45 @@ __device__ __forceinline__ void bf_put(unsigned char* tile, uint32_t off, float 
 
 // One CTA per (sequence b, head h): blockIdx.x = b * nheads + h.
 __global__ void __launch_bounds__(ssd::THREADS, 1)
-ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
-               const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_B,
-               const __grid_constant__ CUtensorMap tm_C, const SsdParams p) {
+ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
+               const __grid_constant__ CUtensorMap tm_C,
+               const SsdParams p) {
     using namespace ssd;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];  // aligned below at run time
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     unsigned char* Cs = smem + CS_OFF;
     unsigned char* Bs = smem + BS_OFF;
     unsigned char* Xh = smem + XH_OFF;
     unsigned char* Xl = smem + XL_OFF;
-    unsigned char* Ys = Xh;  // y staging reuses the w o x head once the state contraction has read it
     unsigned char* Ms = smem + MS_OFF;
     unsigned char* Hs = smem + HS_OFF;
-    float* dts = reinterpret_cast<float*>(smem + F_OFF);  // Delta_t
-    float* css = dts + Q;                                 // cs_t: running sum of Delta A (log2 units)
-    float* wss = css + Q;                                 // w_s = 2^(cs_end - cs_s) Delta_s
-    float* wsum = wss + Q;                                // per-warp totals of the running sum
+    float* fbase = reinterpret_cast<float*>(smem + F_OFF);  // per buffer: float2 (cs_t, Delta_t) [Q], w_t [Q]
     uint64_t* bc_bar = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // C, B of the current chunk
-    uint64_t* xz_bar = bc_bar + 1;                                   // x, z: one barrier per buffer
-    uint64_t* mma_bar = bc_bar + 3;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 32);
+    uint64_t* x_bar = bc_bar + 1;                                    // x: one barrier per buffer
+    uint64_t* mma1_bar = bc_bar + 1 + XBUFS;                         // G, S, Yoff of a chunk done
+    uint64_t* mma2_bar = mma1_bar + 1;                               // Ydiag of a chunk done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 48);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int r = tid & (Q - 1);  // accumulator row (tensor-memory lane) of this thread
-    const int wg = tid >> 7;      // warpgroup: which half of the row's columns it takes
+    const int qd = warp & 3;      // tensor-memory lane quarter of this warp
+    const int cg = warp >> 2;     // column group of this warp
+    const int r = tid & (Q - 1);  // accumulator row (tensor-memory lane) of this thread: 32 qd + lane
     const int bh = blockIdx.x;
     const int b = bh / p.nheads, h = bh % p.nheads;
     const int g = h / (p.nheads / p.ngroups);
     const int L = p.seqlen;
     const int nch = (L + Q - 1) / Q;
-    const bool has_z = p.has_z != 0;
+    const bool has_z = p.has_z != 0 && p.z != nullptr;
     const float a2 = __ldg(p.A + h) * kLog2e;  // decay exponent per unit of Delta, base 2
     const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
     const float dsk = p.D ? __ldg(p.D + h) : 0.f;
     const long long dim = static_cast<long long>(p.nheads) * P;
-    const int xrow = bh * P;                                 // first row of the head in the x/z/y maps
-    const int bcrow = (b * p.ngroups + g) * N;               // first row of the group in the B/C maps
+    const int xrow = bh * P;                    // first row of the head in the x/z/y maps
+    const int bcrow = (b * p.ngroups + g) * N;  // first row of the group in the B/C maps
+    constexpr int PC = P / CG;                  // channels per column group (16)
 
-    // TMA loads: C and B of chunk c (one phase per chunk), x and z of chunk c
-    // into buffer c % 2 (one phase per use of the buffer).
+    // TMA loads: C and B of chunk c (one phase per chunk), x of chunk c into
+    // buffer c % XBUFS (one phase per use of the buffer).
     auto load_bc = [&](int c) {
         mbar_arrive_expect_tx(bc_bar, TX_BC);
 #pragma unroll
@@ -216,199 +273,242 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tma_load_2d(Bs + half * HALF_C, &tm_B, c * Q + half * 64, bcrow, bc_bar);
         }
     };
-    auto load_xz = [&](int c) {
-        const int buf = c & 1;
-        mbar_arrive_expect_tx(&xz_bar[buf], has_z ? 2 * TX_X : TX_X);
+    auto load_x = [&](int c) {
+        const int buf = c % XBUFS;
+        mbar_arrive_expect_tx(&x_bar[buf], TX_X);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tma_load_2d(smem + XS_OFF + buf * XBUF + half * HALF_X, &tm_x, c * Q + half * 64, xrow, &xz_bar[buf]);
-            if (has_z)
-                tma_load_2d(smem + ZS_OFF + buf * XBUF + half * HALF_X, &tm_z, c * Q + half * 64, xrow,
-                            &xz_bar[buf]);
-        }
+        for (int half = 0; half < 2; ++half)
+            tma_load_2d(smem + XS_OFF + buf * XBUF + half * HALF_X, &tm_x, c * Q + half * 64, xrow, &x_bar[buf]);
     };
-    if (tid == 0) {
+    if (tid == CTRL) {
         mbar_init(bc_bar, 1);
-        mbar_init(&xz_bar[0], 1);
-        mbar_init(&xz_bar[1], 1);
-        mbar_init(mma_bar, 1);
+#pragma unroll
+        for (int i = 0; i < XBUFS; ++i) mbar_init(&x_bar[i], 1);
+        mbar_init(mma1_bar, 1);
+        mbar_init(mma2_bar, 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_C);
-        prefetch_tensormap(&tm_y);
-        if (has_z) prefetch_tensormap(&tm_z);
         load_bc(0);
-        load_xz(0);
-        if (nch > 1) load_xz(1);
+        for (int c = 0; c < XBUFS && c < nch; ++c) load_x(c);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_addr(tslot))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    const bool compute = tid < COMPUTE;
+    uint32_t tmem = 0;  // tensor-memory base (read after the first barrier)
 
-    // The carried state: state row n = r, channels p = 32 wg .. 32 wg + 31 per
-    // thread (fp32), and its bf16 copy in shared memory ([n rows][p], MN-major
-    // operand of Yoff).
-    constexpr int PH = P / 2;
-    float H[PH];
-    {
+    // The carried state (compute threads): state row n = r, channels
+    // PC cg .. PC cg + PC - 1 (fp32), and its bf16 copy in shared memory
+    // ([n rows][p], MN-major operand of Yoff): two 16-byte units of the row.
+    float H[PC];
+    auto store_hs = [&]() {
+        uint32_t w[PC / 2];
+#pragma unroll
+        for (int i = 0; i < PC / 2; ++i) w[i] = pack_bf2(H[2 * i], H[2 * i + 1]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int unit = 2 * cg + u;
+            *reinterpret_cast<uint4*>(Hs + r * 128 + ((unit ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
+    };
+    if (compute) {
         const float* h0 = p.h0 ? p.h0 + (static_cast<long long>(b) * dim + static_cast<long long>(h) * P) * N : nullptr;
 #pragma unroll
-        for (int i = 0; i < PH; ++i) {
-            const int q = wg * PH + i;
-            H[i] = h0 ? __ldg(h0 + static_cast<long long>(q) * N + r) : 0.f;
-            bf_put(Hs, sw128_elem(r, q), H[i]);
-        }
+        for (int i = 0; i < PC; ++i) H[i] = h0 ? __ldg(h0 + static_cast<long long>(cg * PC + i) * N + r) : 0.f;
+        store_hs();
     }
-    // Raw step input of this thread's step (threads 0 .. Q-1), loaded a chunk ahead.
-    const __nv_bfloat16* drow = p.delta + static_cast<long long>(bh) * L;
-    float dnext = (tid < Q && tid < L) ? __bfloat162float(drow[tid]) : 0.f;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
-    uint32_t mma_phase = 0;
-    for (int c = 0; c < nch; ++c) {
-        const int t0 = c * Q;
-        const int buf = c & 1;
-        const unsigned char* Xs = smem + XS_OFF + buf * XBUF;
-        const unsigned char* Zs = smem + ZS_OFF + buf * XBUF;
-        // (1) the previous chunk's y store has read its staging tile (the w o x
-        // head, rewritten below)
-        if (tid == 0) bulk_wait_read<0>();
-        // (2) step sizes and the running sum of Delta A (threads 0 .. Q-1: one step each)
-        {
-            float dt = 0.f, v = 0.f;
-            if (tid < Q) {
-                if (t0 + tid < L) dt = softplus<false>(dnext + bias);
-                // the next chunk's step input, in flight while this chunk runs
-                dnext = (t0 + Q + tid < L) ? __bfloat162float(drow[t0 + Q + tid]) : 0.f;
-                v = dt * a2;
+    // Per-step scalars of chunk c (control warp; lane l owns steps 4l .. 4l+3):
+    // Delta_t, the running sum cs_t of Delta A (base 2) and
+    // w_t = 2^(cs_end - cs_t) Delta_t, into float buffer c % 2.  The raw step
+    // inputs of the next chunk are loaded one chunk ahead.
+    const __nv_bfloat16* drow = p.delta + static_cast<long long>(bh) * L;
+    auto load_raw = [&](int c, float (&raw)[4]) {
+        const int t = c * Q + 4 * lane;
+        if (t + 4 <= L) {
+            const uint2 v = *reinterpret_cast<const uint2*>(drow + t);
+            raw[0] = __uint_as_float(v.x << 16);
+            raw[1] = __uint_as_float(v.x & 0xffff0000u);
+            raw[2] = __uint_as_float(v.y << 16);
+            raw[3] = __uint_as_float(v.y & 0xffff0000u);
+        } else {
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float u = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += u;
-                }
-                if (lane == 31) wsum[warp] = v;
-                dts[tid] = dt;
-            }
-            __syncthreads();
-            if (tid < Q) {
-                for (int w = 0; w < warp; ++w) v += wsum[w];
-                css[tid] = v;
-            }
-            __syncthreads();
-            if (tid < Q) wss[tid] = ex2_approx(css[Q - 1] - v) * dt;
-            __syncthreads();
+            for (int k = 0; k < 4; ++k) raw[k] = t + k < L ? __bfloat162float(drow[t + k]) : 0.f;
         }
-        const float cs_end = css[Q - 1];
-        // (3) the tiles have landed
-        mbar_wait(bc_bar, static_cast<uint32_t>(c & 1), p.status);
-        mbar_wait(&xz_bar[buf], static_cast<uint32_t>((c >> 1) & 1), p.status);
-        // (4) w o x, the B operand of the state contraction (same layout as x),
-        // as a bf16 head plus a bf16 tail holding the head's rounding error, so
-        // that the carried state keeps fp32 accuracy through the contraction
-#pragma unroll 2
-        for (int item = tid; item < P * 16; item += THREADS) {
+    };
+    float rawn[4] = {0.f, 0.f, 0.f, 0.f};
+    auto chunk_scalars = [&](int c) {
+        float* fb = fbase + (c & 1) * F_BUF;
+        float2* cd = reinterpret_cast<float2*>(fb);
+        float* wv = fb + 2 * Q;
+        const int t = c * Q + 4 * lane;
+        float dt[4], cs[4];
+        float run = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            dt[k] = t + k < L ? softplus<false>(rawn[k] + bias) : 0.f;
+            run = fmaf(dt[k], a2, run);
+            cs[k] = run;
+        }
+        if (c + 1 < nch) load_raw(c + 1, rawn);  // in flight until the next call
+        float v = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        const float before = v - run;  // the sum over the lanes before this one
+        const float cs_end = __shfl_sync(0xffffffffu, v, 31);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float c_k = before + cs[k];
+            cd[4 * lane + k] = make_float2(c_k, dt[k]);
+            wv[4 * lane + k] = ex2_approx(cs_end - c_k) * dt[k];
+        }
+    };
+    // w o x of chunk c (compute threads) as a bf16 head and a bf16 tail
+    // holding the head's rounding error, so that the carried state keeps fp32
+    // accuracy through the state contraction.
+    auto weight_x = [&](int c) {
+        const float* wv = fbase + (c & 1) * F_BUF + 2 * Q;
+        mbar_wait(&x_bar[c % XBUFS], static_cast<uint32_t>((c / XBUFS) & 1), p.status);
+        const unsigned char* Xs = smem + XS_OFF + (c % XBUFS) * XBUF;
+#pragma unroll
+        for (int item = tid; item < P * 16; item += COMPUTE) {
             const int row = item >> 4, unit = item & 15;
             const int half = unit >> 3, u8 = unit & 7;
             const uint32_t off = half * HALF_X + static_cast<uint32_t>(row * 128 + ((u8 ^ (row & 7)) << 4));
             const uint4 raw = *reinterpret_cast<const uint4*>(Xs + off);
+            const int s0 = half * 64 + u8 * 8;
+            const float4 wa = *reinterpret_cast<const float4*>(wv + s0);
+            const float4 wb = *reinterpret_cast<const float4*>(wv + s0 + 4);
+            const float ws[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
             const uint32_t w32[4] = {raw.x, raw.y, raw.z, raw.w};
             uint32_t oh[4], ol[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int s = half * 64 + u8 * 8 + 2 * k;
-                const float v0 = __uint_as_float(w32[k] << 16) * wss[s];
-                const float v1 = __uint_as_float(w32[k] & 0xffff0000u) * wss[s + 1];
+                const float v0 = __uint_as_float(w32[k] << 16) * ws[2 * k];
+                const float v1 = __uint_as_float(w32[k] & 0xffff0000u) * ws[2 * k + 1];
                 const __nv_bfloat162 ph = __floats2bfloat162_rn(v0, v1);
                 const float2 fh = __bfloat1622float2(ph);
-                const __nv_bfloat162 pl = __floats2bfloat162_rn(v0 - fh.x, v1 - fh.y);
                 oh[k] = *reinterpret_cast<const uint32_t*>(&ph);
-                ol[k] = *reinterpret_cast<const uint32_t*>(&pl);
+                ol[k] = pack_bf2(v0 - fh.x, v1 - fh.y);
             }
             *reinterpret_cast<uint4*>(Xh + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
             *reinterpret_cast<uint4*>(Xl + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        // (5) G = C B^T, Yoff = C H_prev, S = B^T (w o x)
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t cs_a = smem_addr(Cs), bs_a = smem_addr(Bs), hs_a = smem_addr(Hs);
-            const uint32_t xh_a = smem_addr(Xh), xl_a = smem_addr(Xl);
-            const uint32_t id_g = umma_idesc(Q, Q, true, true);
-            const uint32_t id_off = umma_idesc(Q, P, true, true);
-            const uint32_t id_s = umma_idesc(N, P, false, false);
-#pragma unroll
-            for (int ks = 0; ks < N / 16; ++ks) {  // K = the N states, 16 rows per step
-                const uint64_t ca = umma_desc(cs_a + ks * 2048, HALF_C, 1024);
-                umma_f16(tmem + TM_G, ca, umma_desc(bs_a + ks * 2048, HALF_C, 1024), id_g, ks > 0);
-                umma_f16(tmem + TM_YOFF, ca, umma_desc(hs_a + ks * 2048, HALF_C, 1024), id_off, ks > 0);
-            }
-#pragma unroll
-            for (int ks = 0; ks < Q / 16; ++ks) {  // K = the chunk's steps
-                const uint32_t koff = (ks & 3) * 32;  // 16 steps = 32 bytes into the 128-byte row
-                const uint64_t ba = umma_desc(bs_a + (ks >> 2) * HALF_C + koff, 16, 1024);
-                umma_f16(tmem + TM_S, ba, umma_desc(xh_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_s, ks > 0);
-                umma_f16(tmem + TM_S, ba, umma_desc(xl_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_s, 1);
-            }
-            umma_commit(mma_bar);
-        }
-        mbar_wait(mma_bar, mma_phase & 1, p.status);
-        ++mma_phase;
+    };
+    // G = C B^T, Yoff = C H_prev (into buffer c % 2), S = B^T (w o x) of
+    // chunk c, by the control thread once C and B have landed.
+    auto issue_mma1 = [&](int c) {
+        mbar_wait(bc_bar, static_cast<uint32_t>(c & 1), p.status);
         tc_fence_after();
-        // C and B of this chunk are read: the next chunk's tiles load meanwhile.
-        if (tid == 0 && c + 1 < nch) load_bc(c + 1);
-        // (6) M = G o 2^(cs_t - cs_s) Delta_s (s <= t), row t = r, columns
-        // s = 64 wg .. 64 wg + 63
-        const float cs_t = css[r];
-#pragma unroll 1
-        for (int j = 2 * wg; j < 2 * wg + 2; ++j) {
-            float gv[32];
-            tmem_ld32(tmem + lane_base + TM_G + j * 32, gv);
-            const int half = j >> 1;
+        const uint32_t cs_a = smem_addr(Cs), bs_a = smem_addr(Bs), hs_a = smem_addr(Hs);
+        const uint32_t xh_a = smem_addr(Xh), xl_a = smem_addr(Xl);
+        const uint32_t id_g = umma_idesc(Q, Q, true, true);
+        const uint32_t id_off = umma_idesc(Q, P, true, true);
+        const uint32_t id_s = umma_idesc(N, P, false, false);
+        const uint32_t tm_off = tmem + TM_YOFF + static_cast<uint32_t>((c & 1) * P);
 #pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) {  // four 16-byte units of 8 steps
-                uint32_t o32[4];
+        for (int ks = 0; ks < N / 16; ++ks) {  // K = the N states, 16 rows per step
+            const uint64_t ca = umma_desc(cs_a + ks * 2048, HALF_C, 1024);
+            umma_f16(tmem + TM_G, ca, umma_desc(bs_a + ks * 2048, HALF_C, 1024), id_g, ks > 0);
+            umma_f16(tm_off, ca, umma_desc(hs_a + ks * 2048, HALF_C, 1024), id_off, ks > 0);
+        }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int i0 = u4 * 8 + 2 * k;
-                    const int s0 = j * 32 + i0;
-                    const float m0 = s0 <= r ? gv[i0] * ex2_approx(cs_t - css[s0]) * dts[s0] : 0.f;
-                    const float m1 = s0 + 1 <= r ? gv[i0 + 1] * ex2_approx(cs_t - css[s0 + 1]) * dts[s0 + 1] : 0.f;
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(m0, m1);
-                    o32[k] = *reinterpret_cast<const uint32_t*>(&pr);
+        for (int ks = 0; ks < Q / 16; ++ks) {  // K = the chunk's steps
+            const uint32_t koff = (ks & 3) * 32;  // 16 steps = 32 bytes into the 128-byte row
+            const uint64_t ba = umma_desc(bs_a + (ks >> 2) * HALF_C + koff, 16, 1024);
+            umma_f16(tmem + TM_S, ba, umma_desc(xh_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_s, ks > 0);
+            umma_f16(tmem + TM_S, ba, umma_desc(xl_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_s, 1);
+        }
+        umma_commit(mma1_bar);
+    };
+
+    if (!compute) {
+        load_raw(0, rawn);
+        chunk_scalars(0);
+        if (nch > 1) chunk_scalars(1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem = *tslot;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;  // this warp's TMEM lanes
+    if (compute) weight_x(0);
+    __syncthreads();
+    if (tid == CTRL) issue_mma1(0);
+
+    for (int c = 0; c < nch; ++c) {
+        const int t0 = c * Q;
+        const int buf = c & 1;
+        const float2* cd = reinterpret_cast<const float2*>(fbase + buf * F_BUF);
+        const unsigned char* Xs = smem + XS_OFF + (c % XBUFS) * XBUF;
+        // (B) G, S, Yoff of chunk c have landed; C and B are read, so the
+        // next chunk's tiles load meanwhile.
+        mbar_wait(mma1_bar, static_cast<uint32_t>(c & 1), p.status);
+        tc_fence_after();
+        float cs_t = 0.f;
+        if (tid == CTRL && c + 1 < nch) load_bc(c + 1);
+        if (compute) {
+            cs_t = cd[r].x;
+            // M = G o 2^(cs_t - cs_s) Delta_s (s <= t): rows t = r, columns
+            // s = 32 cg .. 32 cg + 31 (a block above the diagonal is all zero)
+            const int half = cg >> 1;
+            const uint32_t rowoff = half * HALF_M + static_cast<uint32_t>(r * 128);
+            if (cg > qd) {
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const int unit = (cg & 1) * 4 + u4;
+                    *reinterpret_cast<uint4*>(Ms + rowoff + ((unit ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
-                const int unit = ((j & 1) * 4 + u4);  // 16-byte unit within the 128-byte row of this half
-                const uint32_t off = half * HALF_M + static_cast<uint32_t>(r * 128 + ((unit ^ (r & 7)) << 4));
-                *reinterpret_cast<uint4*>(Ms + off) = make_uint4(o32[0], o32[1], o32[2], o32[3]);
-            }
-        }
-        // (7) H = 2^cs_end H + S, state row n = r, channels 32 wg .. 32 wg + 31,
-        // and its bf16 copy (pairs of channels per 4-byte store)
-        {
-            const float decay_all = ex2_approx(cs_end);
-            float sv[32];
-            tmem_ld32(tmem + lane_base + TM_S + wg * PH, sv);
+            } else {
+                float gv[32];
+                tmem_ld32(tmem + lane_base + TM_G + cg * 32, gv);
+                const bool diag = cg == qd;
 #pragma unroll
-            for (int i = 0; i < PH; i += 2) {
-                H[i] = fmaf(decay_all, H[i], sv[i]);
-                H[i + 1] = fmaf(decay_all, H[i + 1], sv[i + 1]);
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(H[i], H[i + 1]);
-                *reinterpret_cast<__nv_bfloat162*>(Hs + sw128_elem(r, wg * PH + i)) = pr;
+                for (int u4 = 0; u4 < 4; ++u4) {  // four 16-byte units of 8 steps
+                    uint32_t o32[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int i0 = u4 * 8 + 2 * k;
+                        const int s0 = cg * 32 + i0;
+                        const float4 cp = *reinterpret_cast<const float4*>(cd + s0);  // cs, Delta of s0, s0 + 1
+                        float m0 = gv[i0] * ex2_approx(cs_t - cp.x) * cp.y;
+                        float m1 = gv[i0 + 1] * ex2_approx(cs_t - cp.z) * cp.w;
+                        if (diag) {
+                            m0 = s0 <= r ? m0 : 0.f;
+                            m1 = s0 + 1 <= r ? m1 : 0.f;
+                        }
+                        o32[k] = pack_bf2(m0, m1);
+                    }
+                    const int unit = (cg & 1) * 4 + u4;
+                    *reinterpret_cast<uint4*>(Ms + rowoff + ((unit ^ (r & 7)) << 4)) =
+                        make_uint4(o32[0], o32[1], o32[2], o32[3]);
+                }
             }
+            // H = 2^cs_end H + S, state row n = r, channels PC cg .. PC cg + PC - 1,
+            // and its bf16 copy
+            const float decay_all = ex2_approx(cd[Q - 1].x);
+            float sv[PC];
+            tmem_ld16(tmem + lane_base + TM_S + cg * PC, sv);
+#pragma unroll
+            for (int i = 0; i < PC; ++i) H[i] = fmaf(decay_all, H[i], sv[i]);
+            store_hs();
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // (8) Ydiag = M x
-        if (tid == 0) {
+        // Ydiag = M x, by the control thread; meanwhile the compute threads
+        // weight the next chunk's x
+        if (tid == CTRL) {
             tc_fence_after();
             const uint32_t ms_a = smem_addr(Ms), xs_a = smem_addr(Xs);
             const uint32_t id_d = umma_idesc(Q, P, false, false);
@@ -418,48 +518,62 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 umma_f16(tmem + TM_YD, umma_desc(ms_a + (ks >> 2) * HALF_M + koff, 16, 1024),
                          umma_desc(xs_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_d, ks > 0);
             }
-            umma_commit(mma_bar);
+            umma_commit(mma2_bar);
         }
-        mbar_wait(mma_bar, mma_phase & 1, p.status);
-        ++mma_phase;
-        tc_fence_after();
-        // (9) y = (Ydiag + 2^cs_t Yoff + D x) * silu(z), row t = r, channels
-        // 32 wg .. 32 wg + 31, staged as [p rows][t]
-        {
-            const float e_t = ex2_approx(cs_t);
-            const int half = r >> 6, tc = r & 63;
-            float yd[32], yo[32];
-            tmem_ld32(tmem + lane_base + TM_YD + wg * PH, yd);
-            tmem_ld32(tmem + lane_base + TM_YOFF + wg * PH, yo);
+        if (c + 1 < nch) {
+            if (compute) weight_x(c + 1);
+            __syncthreads();
+        }
+        if (!compute) {
+            // G, S, Yoff of the next chunk (from the H just written) while the
+            // compute threads form this chunk's output; then the step scalars
+            // of the chunk after it
+            if (tid == CTRL && c + 1 < nch) issue_mma1(c + 1);
+            if (c + 2 < nch) chunk_scalars(c + 2);
+        } else {
+            // (C) y = (Ydiag + 2^cs_t Yoff + D x) * silu(z), row t = r, channels
+            // PC cg .. PC cg + PC - 1: z read from global memory (per warp and
+            // channel, 32 consecutive steps) while Ydiag finishes, y written
+            // straight back the same way
+            const bool row_ok = t0 + r < L;
+            const long long rbase = (static_cast<long long>(xrow) + cg * PC) * L + t0 + r;
+            float zv[PC];
+            if (has_z && row_ok) {
 #pragma unroll
-            for (int i = 0; i < PH; ++i) {
-                const int q = wg * PH + i;
-                const uint32_t off = half * HALF_X + sw128_elem(q, tc);
-                const float xv = bf_at(Xs, off);
-                float yv = fmaf(dsk, xv, fmaf(e_t, yo[i], yd[i]));
-                if (has_z) yv *= silu<false>(bf_at(Zs, off));
-                bf_put(Ys, off, yv);
+                for (int i = 0; i < PC; ++i)
+                    zv[i] = __bfloat162float(__ldcs(p.z + rbase + static_cast<long long>(i) * L));
+            }
+            const int half = r >> 6, tc = r & 63;
+            float xv[PC];
+#pragma unroll
+            for (int i = 0; i < PC; ++i) xv[i] = bf_at(Xs, half * HALF_X + sw128_elem(cg * PC + i, tc));
+            const float e_t = ex2_approx(cs_t);
+            mbar_wait(mma2_bar, static_cast<uint32_t>(c & 1), p.status);
+            tc_fence_after();
+            float yd[PC], yo[PC];
+            tmem_ld16x2(tmem + lane_base + TM_YD + cg * PC,
+                        tmem + lane_base + TM_YOFF + static_cast<uint32_t>(buf * P + cg * PC), yd, yo);
+            if (row_ok) {
+                __nv_bfloat16* yrow = p.y + rbase;
+#pragma unroll
+                for (int i = 0; i < PC; ++i) {
+                    float yv = fmaf(dsk, xv[i], fmaf(e_t, yo[i], yd[i]));
+                    if (has_z) yv *= silu<false>(zv[i]);
+                    yrow[static_cast<long long>(i) * L] = __float2bfloat16_rn(yv);
+                }
             }
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) tma_store_2d(&tm_y, t0 + half * 64, xrow, Ys + half * HALF_X);
-            bulk_commit();
-            // x and z of this buffer are read: chunk c + 2 loads into it.
-            if (c + 2 < nch) load_xz(c + 2);
-        }
+        // x of this buffer is read (Ydiag is done, and so is the output step):
+        // chunk c + XBUFS loads into it.
+        if (tid == CTRL && c + XBUFS < nch) load_x(c + XBUFS);
     }
-    if (tid == 0) bulk_wait<0>();
-    if (p.h_final) {
+    if (p.h_final && compute) {
         float* hf = p.h_final + (static_cast<long long>(b) * dim + static_cast<long long>(h) * P) * N;
 #pragma unroll
-        for (int i = 0; i < PH; ++i) hf[static_cast<long long>(wg * PH + i) * N + r] = H[i];
+        for (int i = 0; i < PC; ++i) hf[static_cast<long long>(cg * PC + i) * N + r] = H[i];
     }
-    tc_fence_before();
-    __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");

@@ -55,9 +55,6 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool supported_dstate(int n) { return n == 4 || n == 8 || n == 16 || n == 32 || n == 64 || n == 128 || n == 256; }
 
-// N = 128 and 256 run on the TMA-staged kernel only (8 or 16 lanes of 16
-// states): rows must be whole 16-byte packets.
-bool dstate_needs_tma(int n) { return n > 64; }
 
 // Lanes that may share one channel's N states: each lane keeps an even number
 // of them, at most 16 (the register budget of the update loop).
@@ -79,8 +76,6 @@ ssm_status_t check_scan_args(const void* u, const void* delta, const void* z, co
     if (dim % ngroups != 0) return SSM_ERR_INVALID_ARG;
     if (io != SSM_F32 && io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
     if (!supported_dstate(dstate)) return SSM_ERR_UNSUPPORTED;
-    if (dstate_needs_tma(dstate) && (static_cast<long long>(seqlen) * (io == SSM_F32 ? 4 : 2)) % 16 != 0)
-        return SSM_ERR_UNSUPPORTED;
     if (batch == 0) return SSM_OK;
     if (!A) return SSM_ERR_INVALID_ARG;
     if (seqlen > 0 && (!u || !delta || !B || !C || !y)) return SSM_ERR_INVALID_ARG;
@@ -115,11 +110,26 @@ int device_sm_count() {
     return cached_sms;
 }
 
+// Opts a kernel into its dynamic shared memory once per device.
+template <typename K>
+cudaError_t ensure_smem(K kern, int bytes, unsigned long long* done_mask) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
+    return e;
+}
+
 constexpr int kScanWarps = 4;
-// Steps per staged B/C tile of the generic kernel: 64, or 32 for N = 64 (its
-// fp32 B/C quads of 64 steps would not fit the 48 KB of static shared memory).
+// Steps per staged B/C tile of the generic kernel: 64, or 32 for N = 64 and
+// 128 (fp32 B/C quads of 64 steps would not fit), 64 again at N = 256 (16
+// lanes of 4 steps: one warp block).  From N = 128 on the tile is held in
+// dynamic shared memory, single-buffered (32 KB at N = 128, 128 KB at 256).
 template <int N>
-constexpr int scan_tile() { return N >= 64 ? 32 : 64; }
+constexpr int scan_tile() { return N >= 256 ? 64 : (N >= 64 ? 32 : 64); }
 
 template <typename T, int N, int LANES>
 cudaError_t launch_scan_variant(ssm::ScanParams p, cudaStream_t st) {
@@ -132,18 +142,27 @@ cudaError_t launch_scan_variant(ssm::ScanParams p, cudaStream_t st) {
     const long long blocks = static_cast<long long>(p.blocks_per_group) * p.ngroups * p.batch;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     constexpr bool kAccurate = sizeof(T) == 4;
-    ssm::scan_fwd_kernel<T, N, LANES, kScanWarps, scan_tile<N>(), kAccurate>
-        <<<static_cast<unsigned>(blocks), kScanWarps * 32, 0, st>>>(p);
+    auto kern = ssm::scan_fwd_kernel<T, N, LANES, kScanWarps, scan_tile<N>(), kAccurate>;
+    int dyn = 0;
+    if constexpr (ssm::scan_bc_dynamic(N)) {
+        dyn = scan_tile<N>() * (N / 2) * 16;
+        static unsigned long long done = 0;
+        const cudaError_t e = ensure_smem(kern, dyn, &done);
+        if (e != cudaSuccess) return e;
+    }
+    kern<<<static_cast<unsigned>(blocks), kScanWarps * 32, dyn, st>>>(p);
     return cudaGetLastError();
 }
 
+// Lanes per channel of the generic kernel: 2 to 16 states each.
 template <typename T, int N>
 cudaError_t launch_scan_n(const ssm::ScanParams& p, int lanes, cudaStream_t st) {
     switch (lanes) {
         case 1: if constexpr (N <= 16) return launch_scan_variant<T, N, 1>(p, st); break;
         case 2: if constexpr (N <= 32) return launch_scan_variant<T, N, 2>(p, st); break;
-        case 4: if constexpr (N >= 8) return launch_scan_variant<T, N, 4>(p, st); break;
-        case 8: if constexpr (N >= 16) return launch_scan_variant<T, N, 8>(p, st); break;
+        case 4: if constexpr (N >= 8 && N <= 64) return launch_scan_variant<T, N, 4>(p, st); break;
+        case 8: if constexpr (N >= 16 && N <= 128) return launch_scan_variant<T, N, 8>(p, st); break;
+        case 16: if constexpr (N == 256) return launch_scan_variant<T, N, 16>(p, st); break;
         default: break;
     }
     return cudaErrorInvalidValue;
@@ -157,6 +176,8 @@ cudaError_t launch_scan_t(const ssm::ScanParams& p, int dstate, int lanes, cudaS
         case 16: return launch_scan_n<T, 16>(p, lanes, st);
         case 32: return launch_scan_n<T, 32>(p, lanes, st);
         case 64: return launch_scan_n<T, 64>(p, lanes, st);
+        case 128: return launch_scan_n<T, 128>(p, lanes, st);
+        case 256: return launch_scan_n<T, 256>(p, lanes, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -372,18 +393,6 @@ bool encode_bc(CUtensorMap* m, const void* ptr, ssm_dtype_t io, int seqlen, long
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Opts a kernel into its dynamic shared memory once per device.
-template <typename K>
-cudaError_t ensure_smem(K kern, int bytes, unsigned long long* done_mask) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
-    return e;
-}
 
 template <typename T, int N, int LANES, ssm::ScanMode MODE>
 cudaError_t launch_tma(const ScanMaps& m, const ssm::TmaScanParams& p, int grid_y, cudaStream_t st) {
@@ -764,7 +773,7 @@ ssm_status_t run_scan(const void* u, const void* delta, const void* z, const flo
         }
         return SSM_OK;
     }
-    if (tma_eligible(seqlen, io) && (!force_generic() || dstate_needs_tma(dstate))) {
+    if (tma_eligible(seqlen, io) && !force_generic()) {
         const bool chunks_ok = workspace != nullptr;
         const int cap = chunks_ok ? chunks_fitting(workspace_bytes, batch, dim, dstate) : 1;
         float* agg = chunks_ok ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kWorkspaceHeader) : nullptr;
@@ -1069,8 +1078,7 @@ ssm_status_t ssm_scan_plan(int batch, int dim, int dstate, int seqlen, int ngrou
         *kernels = (batch > 0 && chunked) ? 1 : 0;  // h_final copy for an empty sequence
         return SSM_OK;
     }
-    if (dstate_needs_tma(dstate) && !tma_eligible(seqlen, io)) return SSM_ERR_UNSUPPORTED;
-    if (tma_eligible(seqlen, io) && (!force_generic() || dstate_needs_tma(dstate))) {
+    if (tma_eligible(seqlen, io) && !force_generic()) {
         const ScanPlan plan = plan_scan(batch, dim, dstate, seqlen, ngroups, io, chunked != 0 ? kMaxChunks : 1);
         *lanes = plan.lanes; *chunks = plan.chunks; *kernels = plan.chunks > 1 ? 3 : 1; *staged = 1;
     } else {
@@ -1271,7 +1279,6 @@ ssm_status_t ssm_scan_fwd_varlen(const void* u, const void* delta, const void* z
                                  const void* C, const float* Dskip, const float* dt_bias, const float* h0,
                                  const int* cu_seqlens, void* y, float* h_final, int dim, int dstate, int total,
                                  int ngroups, int nseq, ssm_dtype_t io, void* stream) {
-    if (dstate_needs_tma(dstate)) return SSM_ERR_UNSUPPORTED;  // the packed scan runs on the generic kernel
     const ssm_status_t s = check_scan_args(u, delta, z, A, B, C, Dskip, dt_bias, y, h0, h_final, 1, dim, dstate,
                                            total, ngroups, io);
     if (s != SSM_OK) return s;

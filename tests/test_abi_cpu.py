@@ -70,7 +70,8 @@ def test_scan_argument_errors(lib):
     assert scan(lib, dim=6, G=4) == 1          # dim % ngroups
     assert scan(lib, N=12) == 2                # unsupported state size
     assert scan(lib, N=512) == 2               # N up to 256
-    assert scan(lib, N=128, L=9) == 2          # N = 128 needs rows of whole 16-byte packets
+    assert scan(lib, N=128, L=9, B=MIS) == 3   # N = 128 and 256 pass the checks on unaligned rows too
+    assert scan(lib, N=256, L=9, B=MIS) == 3
     assert scan(lib, io=7) == 2
     assert scan(lib, B=MIS) == 3               # misaligned
     assert scan(lib, z=MIS) == 3
@@ -148,7 +149,8 @@ def test_varlen_and_pooled_argument_errors(lib):
     assert varlen(cu=None) == 1
     assert varlen(cu=MIS) == 3
     assert varlen(N=12) == 2
-    assert varlen(N=128) == 2                 # the packed scan stops at N = 64
+    assert varlen(N=128, cu=MIS) == 3         # the packed scan takes N = 128 and 256
+    assert varlen(N=256, cu=MIS) == 3
     assert varlen(dim=6, G=4) == 1
 
     def pooled(idx=None, nslots=2, batch=2):

@@ -2,8 +2,8 @@
 128 and 256, several lanes sharing one channel's states) against the fp64
 oracle: the TMA-staged path single pass and time-chunked, the generic path,
 the packed variable-length scan and the decode step.  N = 128 and 256 (8 or 16
-lanes of 16 states, more lanes than the steps of a 16-byte chunk) run on the
-staged path only."""
+lanes of 16 states) run on every path: on the generic one and in the packed
+scan with the widened B/C tile in dynamic shared memory, single-buffered."""
 import numpy as np
 import pytest
 import torch
@@ -41,7 +41,7 @@ def test_staged_large_state(ssm, monkeypatch, io, N, chunks):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N,lanes", [(32, 2), (32, 4), (32, 8), (64, 4), (64, 8)])
+@pytest.mark.parametrize("N,lanes", [(32, 2), (32, 4), (32, 8), (64, 4), (64, 8), (128, 8), (256, 16)])
 def test_generic_large_state(ssm, monkeypatch, io, N, lanes):
     monkeypatch.setenv("SSM_FORCE_PATH", "generic")
     monkeypatch.setenv("SSM_FORCE_LANES", str(lanes))
@@ -53,7 +53,22 @@ def test_generic_large_state(ssm, monkeypatch, io, N, lanes):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [32, 64])
+@pytest.mark.parametrize("N,L", [(128, 203), (256, 131)])
+def test_unaligned_rows_large_state(ssm, io, N, L):
+    """Rows that are not whole 16-byte packets (no TMA description): N = 128
+    and 256 on the generic kernel, with an initial and a final state."""
+    x = I.make_scan_inputs(2, 48, N, L, 2, io=io, recipe="scaled", seed=70 + N, device="cuda", with_h0=True)
+    y, hf = chunked(ssm, x, h0=x.h0)
+    torch.cuda.synchronize()
+    assert not ssm.scan_plan(2, 48, N, L, 2, x.u.dtype)["staged"]
+    ref_y, ref_h = oracle_scan(x, h0=x.h0, final_state=True)
+    assert_close(to_np(y), ref_y, io, f"unaligned N={N} L={L} io={io}")
+    assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
+    assert ssm.device_status() == 0
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [32, 64, 128, 256])
 def test_varlen_large_state(ssm, io, N):
     x = I.make_varlen_inputs(64, N, [37, 0, 90, 8], io=io, seed=95 + N, device="cuda", with_h0=True)
     y, hf = ssm.scan_fwd_varlen(x["u"], x["delta"], x["A"], x["B"], x["C"], x["cu_seqlens"], z=x["z"], D=x["D"],
@@ -97,18 +112,25 @@ def test_n64_full_size_bf16_b2_d1536_l2048(ssm):
     print(f"N=64 full-size rel_l2 = {e:.3e}")
 
 
-def test_n128_single_pass_and_unsupported_forms(ssm):
-    """N = 128 through the entry point without a workspace (one pass), and the
-    forms it does not take: rows that are not whole 16-byte packets, and the
-    packed scan."""
+def test_n128_single_pass_and_other_forms(ssm):
+    """N = 128 through the entry point without a workspace (one pass), on a
+    row that is not whole 16-byte packets (the generic kernel), and in the
+    packed scan, each against the oracle."""
     x = I.make_scan_inputs(2, 48, 128, 96, 1, io="bf16", recipe="scaled", seed=7, device="cuda")
     y = ssm.scan_fwd(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias)
     torch.cuda.synchronize()
     assert_close(to_np(y), oracle_scan(x), "bf16", "N=128 single pass")
     odd = I.make_scan_inputs(1, 16, 128, 37, 1, io="bf16", recipe="scaled", seed=8, device="cuda")
-    with pytest.raises(ssm.SsmError):
-        ssm.scan_fwd(odd.u, odd.delta, odd.A, odd.B, odd.C, z=odd.z, D=odd.D, dt_bias=odd.dt_bias)
+    yo = ssm.scan_fwd(odd.u, odd.delta, odd.A, odd.B, odd.C, z=odd.z, D=odd.D, dt_bias=odd.dt_bias)
+    torch.cuda.synchronize()
+    assert_close(to_np(yo), oracle_scan(odd), "bf16", "N=128 unaligned row")
     v = I.make_varlen_inputs(16, 128, [5, 11], io="bf16", seed=9, device="cuda", row_multiple=8)
-    with pytest.raises(ssm.SsmError):
-        ssm.scan_fwd_varlen(v["u"], v["delta"], v["A"], v["B"], v["C"], v["cu_seqlens"], z=v["z"], D=v["D"],
-                            dt_bias=v["dt_bias"])
+    yv = ssm.scan_fwd_varlen(v["u"], v["delta"], v["A"], v["B"], v["C"], v["cu_seqlens"], z=v["z"], D=v["D"],
+                             dt_bias=v["dt_bias"])
+    torch.cuda.synchronize()
+    f = lambda t: to_np(t)
+    ry = oracle.scan_varlen(f(v["u"]), f(v["delta"]), f(v["A"]), f(v["B"]), f(v["C"]), v["cu_seqlens"].cpu().numpy(),
+                            z=f(v["z"]), Dskip=f(v["D"]), dt_bias=f(v["dt_bias"]))
+    n = int(v["cu_seqlens"][-1])  # the row's padding past the last sequence is not written
+    assert_close(to_np(yv)[:, :n], ry[:, :n], "bf16", "N=128 packed")
+    assert ssm.device_status() == 0
