@@ -10,6 +10,9 @@
 #include "../../include/ssm_scan.h"
 #include "ssd.cuh"
 
+// Records a CUDA error for ssm_last_cuda_error (ssm_scan.cu).
+ssm_status_t ssm_note_cuda_error(cudaError_t e);
+
 namespace {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -72,7 +75,8 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
         if (h_final) {
             const long long n = static_cast<long long>(batch) * dim * dstate;
             ssd_copy_state_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(h0, h_final, n);
-            if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return ssm_note_cuda_error(e);
         }
         return SSM_OK;
     }
@@ -93,13 +97,14 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
     if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(ssm::ssd_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ssm::ssd::SMEM_BYTES) != cudaSuccess)
-            return SSM_ERR_CUDA;
+        const cudaError_t e = cudaFuncSetAttribute(ssm::ssd_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   ssm::ssd::SMEM_BYTES);
+        if (e != cudaSuccess) return ssm_note_cuda_error(e);
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
     const long long grid = static_cast<long long>(batch) * nheads;
     if (grid > 0x7fffffffLL) return SSM_ERR_INVALID_ARG;
     ssm::ssd_fwd_kernel<<<static_cast<unsigned>(grid), ssm::ssd::THREADS, ssm::ssd::SMEM_BYTES, st>>>(mx, mb, mc, p);
-    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SSM_OK : ssm_note_cuda_error(e);
 }

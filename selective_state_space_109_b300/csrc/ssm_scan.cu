@@ -31,6 +31,10 @@ namespace ssm {
 __device__ unsigned int g_ssm_device_error = 0;
 }
 
+// Records a CUDA error for ssm_last_cuda_error (also used by the SSD
+// translation unit) and returns the matching status.
+ssm_status_t ssm_note_cuda_error(cudaError_t e);
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -986,6 +990,8 @@ __global__ void copy_or_zero_kernel(const float* __restrict__ src, float* __rest
 }
 
 }  // namespace
+
+ssm_status_t ssm_note_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
 extern "C" {
 
