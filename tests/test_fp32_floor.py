@@ -1,8 +1,8 @@
-"""Pins the reading of the benchmark spec's fp32 max-rel tolerance, on the CPU.
+"""Pins the reading of the fp32 max-rel tolerance, on the CPU.
 
-The build specification asks fp32 I/O to meet rel-L2 <= 1e-5 and max
-relative error <= 1e-4 against the fp64 oracle, but does not say what an
-element near zero is measured relative to.  The tests read it as
+The fp32 I/O tolerance is rel-L2 <= 1e-5 and max relative error <= 1e-4
+against the fp64 oracle; it does not say what an element near zero is
+measured relative to.  The tests read it as
 max_i |y_i - r_i| / max(|r_i|, 1e-2 * rms(r)).  These tests show why the
 guard cannot be tighter: a correctly rounded fp32 evaluation of the
 recurrence (``tests/fp32_model.py``: each operation rounded once, exp and
