@@ -653,6 +653,16 @@ bool decode_tma_eligible(int batch, int dim, int dstate, int ngroups, ssm_dtype_
            (ngroups == 1 || dpg % 128 == 0);
 }
 
+// The bulk-staged decode runs the warp-specialised kernel (decode_ws_kernel):
+// measured 31.5-31.8 us against 32.8-33.0 us for the CTA-synchronous one on
+// batch 256 x 5120 channels with the state cold in HBM (82% against 79% of
+// the measured copy); with the state resident in L2 it is slower (27.2
+// against 24.8 us).  SSM_DECODE_KERNEL=tma selects the CTA-synchronous kernel.
+bool decode_ws_enabled() {
+    const char* v = std::getenv("SSM_DECODE_KERNEL");
+    return !(v && std::strcmp(v, "tma") == 0);
+}
+
 template <typename T, int CH, int STAGES>
 cudaError_t launch_decode_tma_v(float* state, const int* slots, int nslots, const void* u, const void* delta,
                                 const void* z, const float* A, const void* B, const void* C, const float* Dskip,
@@ -703,6 +713,29 @@ cudaError_t launch_decode_tma_v(float* state, const int* slots, int nslots, cons
     p.slots = slots;
     p.nslots = nslots;
 
+    if (decode_ws_enabled()) {
+        // Warp-specialised kernel: the state block also leaves by 32-row boxes.
+        using WLay = ssm::DecodeWsLayout<T, CH, STAGES>;
+        CUtensorMap mso;
+        const cuuint64_t dims[3] = {N, static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(nslots)};
+        const cuuint64_t str[2] = {N * 4, static_cast<cuuint64_t>(dim) * N * 4};
+        const cuuint32_t box[3] = {N, 32, 1};
+        if (encode_tiled()(&mso, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, state, dims, str, box, e1,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        auto kern = ssm::decode_ws_kernel<T, CH, STAGES, sizeof(T) == 4>;
+        static unsigned long long done_ws = 0;
+        cudaError_t e = ensure_smem(kern, WLay::SMEM_BYTES, &done_ws);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CH + 32, WLay::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        const long long grid =
+            std::min<long long>(p.ntiles, static_cast<long long>(device_sm_count()) * std::max(1, per_sm));
+        kern<<<static_cast<unsigned>(grid), CH + 32, WLay::SMEM_BYTES, st>>>(ms, mso, mu, md, mz, mB, mC, p);
+        return cudaGetLastError();
+    }
     auto kern = ssm::decode_tma_kernel<T, CH, STAGES, sizeof(T) == 4>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem(kern, Lay::SMEM_BYTES, &done);
@@ -722,8 +755,10 @@ template <typename T>
 cudaError_t launch_decode_tma(float* state, const int* slots, int nslots, const void* u, const void* delta,
                               const void* z, const float* A, const void* B, const void* C, const float* Dskip,
                               const float* dt_bias, void* y, int batch, int dim, int ngroups, cudaStream_t st) {
-    // 128 channels x 3 stages measured fastest on B300 (32 us for batch 256 x
-    // 5120 channels; 128x4, 64x4, 64x6 within 4%, 32x8 30% slower).
+    // 128 channels x 3 stages measured fastest on B300 for both kernels
+    // (CTA-synchronous: 128x4, 64x4, 64x6 within 6%, 32x8 30% slower;
+    // warp-specialised: 128x4 and 64x4 5% slower, 256x3 3%, 128x2 and 256x2
+    // 30-40%).
     int ch = 128, stages = 3;
     if (const char* v = std::getenv("SSM_DECODE_TILE")) std::sscanf(v, "%dx%d", &ch, &stages);
 #define SSM_DECODE_V(C_, S_) \
@@ -731,6 +766,9 @@ cudaError_t launch_decode_tma(float* state, const int* slots, int nslots, const 
         return launch_decode_tma_v<T, C_, S_>(state, slots, nslots, u, delta, z, A, B, C, Dskip, dt_bias, y, batch, \
                                               dim, ngroups, st);
     SSM_DECODE_V(128, 4)
+    SSM_DECODE_V(128, 2)
+    SSM_DECODE_V(256, 2)
+    SSM_DECODE_V(256, 3)
     SSM_DECODE_V(64, 4)
     SSM_DECODE_V(64, 6)
     SSM_DECODE_V(32, 8)

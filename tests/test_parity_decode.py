@@ -23,17 +23,20 @@ def run_step(ssm, state, tok, prm, **kw):
 
 @pytest.fixture
 def path(request, monkeypatch):
-    if request.param is not None:
-        monkeypatch.setenv("SSM_FORCE_PATH", request.param)
+    if request.param == "generic":
+        monkeypatch.setenv("SSM_FORCE_PATH", "generic")
+    elif request.param == "tma":  # the CTA-synchronous bulk-staged kernel
+        monkeypatch.setenv("SSM_DECODE_KERNEL", "tma")
     return request.param
 
 
-@pytest.mark.parametrize("path", [None, "generic"], indirect=True)
+@pytest.mark.parametrize("path", [None, "tma", "generic"], indirect=True)
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("N", [4, 8, 16])
 @pytest.mark.parametrize("G", [1, 2])
 def test_small_steps_whole_tensor(ssm, io, N, G, path):
-    """Both decode kernels: bulk-staged (default) and register-staged."""
+    """The three decode kernels: bulk-staged warp-specialised (default),
+    bulk-staged CTA-synchronous, and register-staged."""
     batch, dim = 11, 70  # 70 channels: a partial channel block; 11 sequences: a partial batch chunk
     prm = I.decode_params(dim, N, recipe="scaled", seed=1, device="cuda")
     state = I.make_decode_state(batch, dim, N, seed=1, device="cuda")
