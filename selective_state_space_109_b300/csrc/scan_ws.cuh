@@ -146,7 +146,10 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
     const int b = bg / p.ngroups;
     const int dloc0 = cb * Lay::CH;
 
-    const int nt = p.ntiles;
+    // This CTA's time chunk: tiles [tb, tb + nt).
+    const int chunk = blockIdx.y;
+    const int tb = static_cast<int>(static_cast<long long>(chunk) * p.ntiles / p.nchunks);
+    const int nt = static_cast<int>(static_cast<long long>(chunk + 1) * p.ntiles / p.nchunks) - tb;
     const bool has_z = p.has_z;
 
     if (threadIdx.x == 0) {
@@ -217,7 +220,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
             }
             if (lane == 0) {
                 unsigned char* st = stage_ptr(s);
-                const int x = k * TS;
+                const int x = (tb + k) * TS;
                 mbar_arrive_expect_tx(&full_bar[s], stage_tx);
                 tma_load_3d(st, &tm_u, x, dloc0, bg, &full_bar[s]);
                 tma_load_3d(st + Lay::ACT_BYTES, &tm_d, x, dloc0, bg, &full_bar[s]);
@@ -467,7 +470,18 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
                 a2[k] = make_float2(av.x * decay_scale<ACCURATE>(), av.y * decay_scale<ACCURATE>());
                 h[k] = make_float2(0.f, 0.f);
             }
-            if (p.h0 && active) {
+            if (chunk > 0) {
+                // The carry pass wrote the state entering this chunk; this
+                // kernel may have started before it finished.
+                grid_dep_wait();
+                if (active) {
+                    const long long BD = static_cast<long long>(p.batch) * p.dim;
+                    const float2* cv = reinterpret_cast<const float2*>(
+                        p.carry + (static_cast<long long>(chunk - 1) * BD + bd) * (2 * N) + N + j * S);
+#pragma unroll
+                    for (int k = 0; k < P; ++k) h[k] = __ldcg(cv + k);
+                }
+            } else if (p.h0 && active) {
                 const float2* h0v = reinterpret_cast<const float2*>(p.h0 + bd * N + j * S);
 #pragma unroll
                 for (int k = 0; k < P; ++k) h[k] = __ldg(h0v + k);
@@ -489,7 +503,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
             const unsigned char* d_t = st + Lay::ACT_BYTES;
             const unsigned char* z_t = st + 2 * Lay::ACT_BYTES;
             const float* bcf = reinterpret_cast<const float*>(st + Lay::BCF_OFFSET);
-            const int t0 = i * TS;
+            const int t0 = (tb + i) * TS;
 
             // One 16-byte chunk (VPC steps) of this lane's channel row.  MASKED:
             // the tile runs past the sequence end, so steps beyond it get Delta = 0
@@ -621,7 +635,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
         }
 
         if (!active) return;
-        if (p.h_final) {
+        if (p.h_final && chunk == p.nchunks - 1) {
             float2* hf = reinterpret_cast<float2*>(p.h_final + bd * N + j * S);
 #pragma unroll
             for (int k = 0; k < P; ++k) hf[k] = h[k];

@@ -25,6 +25,12 @@ struct WsScanParams {
     // after wait_budget_ns.
     int stop_tile;
     unsigned long long wait_budget_ns;
+    // Time chunks (grid y; 1: the whole sequence).  Chunk c > 0 starts from
+    // the state carried into it, at carry[((c - 1) * batch * dim + b * dim +
+    // d) * 2 * dstate + dstate ...] (the summary layout after the carry pass),
+    // read once the previous kernel in the stream has completed.
+    const float* carry;
+    int nchunks;
 };
 
 // TMA descriptors of one call: the [batch * ngroups, dim_per_group, seqlen]
@@ -41,7 +47,8 @@ struct WsMaps {
 int ws_smem_bytes_bf16(int dstate, int lanes, int nw, int seg);
 int ws_smem_bytes_f32(int dstate, int lanes, int nw, int seg);
 
-// Enqueues the pass (grid: blocks_per_group * ngroups * batch CTAs).
+// Enqueues the pass (grid: blocks_per_group * ngroups * batch CTAs, times
+// nchunks; a chunked pass is launched to overlap the previous kernel's tail).
 // cudaErrorInvalidValue if the variant is not built.
 cudaError_t ws_launch_bf16(int dstate, int lanes, int nw, int seg, const WsMaps& m, const WsScanParams& p,
                            cudaStream_t st);

@@ -69,9 +69,19 @@ cudaError_t launch(const WsMaps& m, const WsScanParams& p, cudaStream_t st) {
             done.fetch_or(bit, std::memory_order_acq_rel);
         }
         const long long gx = static_cast<long long>(p.blocks_per_group) * p.ngroups * p.batch;
-        if (gx > 0x7fffffffLL || gx <= 0) return cudaErrorInvalidConfiguration;
-        kern<<<static_cast<unsigned>(gx), Lay::THREADS, Lay::SMEM_BYTES, st>>>(m.u, m.d, m.z, m.B, m.C, p);
-        return cudaGetLastError();
+        if (gx > 0x7fffffffLL || gx <= 0 || p.nchunks < 1 || p.nchunks > 65535) return cudaErrorInvalidConfiguration;
+        if (SEG > 1 && p.nchunks != 1) return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p.nchunks));
+        cfg.blockDim = dim3(Lay::THREADS);
+        cfg.dynamicSmemBytes = Lay::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = p.nchunks > 1 ? &attr : nullptr;
+        cfg.numAttrs = p.nchunks > 1 ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, kern, m.u, m.d, m.z, m.B, m.C, p);
     } else {
         (void)m; (void)p; (void)st;
         return cudaErrorInvalidValue;

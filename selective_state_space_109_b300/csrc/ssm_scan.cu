@@ -481,6 +481,17 @@ cudaError_t launch_carry(float* agg, const float* h0, int batch, int dim, int ds
     }
 }
 
+int ws_smem(ssm_dtype_t io, int dstate, int lanes, int nw, int seg = 1);
+bool ws_encode(ssm::WsMaps* m, const void* u, const void* delta, const void* z, const void* B, const void* C,
+               ssm_dtype_t io, int seqlen, int dpg, long long bg, int dstate, int ch, int rb);
+
+// SSM_FUSED_KERNEL=ws runs the fused pass of chunked plans on the
+// warp-specialised kernel.
+bool fused_ws_enabled() {
+    const char* v = std::getenv("SSM_FUSED_KERNEL");
+    return v && std::strcmp(v, "ws") == 0;
+}
+
 // Enqueues the staged scan: with plan.chunks > 1 the summary pass over all
 // chunks but the last, then the full pass over every chunk.
 ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const float* A, const void* B,
@@ -530,6 +541,30 @@ ssm_status_t run_scan_tma(const void* u, const void* delta, const void* z, const
         e = launch_carry(agg, h0, batch, dim, dstate, plan.chunks, st);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    if (plan.chunks > 1 && fused_ws_enabled() && ws_smem(io, dstate, plan.lanes, 4) > 0) {
+        // The fused pass of the chunked call on the warp-specialised kernel.
+        ssm::WsMaps wm;
+        const int wch = 4 * 32 / plan.lanes;
+        if (!ws_encode(&wm, u, delta, z, B, C, io, seqlen, dpg, bg, dstate, wch, ssm::kScanRowBytes))
+            return cuda_fail(cudaErrorInvalidValue);
+        ssm::WsScanParams wp{};
+        wp.A = A; wp.D = Dskip; wp.dt_bias = dt_bias; wp.h0 = h0; wp.h_final = h_final; wp.y = y;
+        wp.status = status;
+        wp.batch = batch; wp.dim = dim; wp.seqlen = seqlen; wp.ngroups = ngroups; wp.dim_per_group = dpg;
+        wp.blocks_per_group = (dpg + wch - 1) / wch;
+        wp.ntiles = p.ntiles;
+        wp.has_z = z != nullptr;
+        wp.stop_tile = -1;
+        wp.wait_budget_ns = ssm::kWaitBudgetNs;
+        wp.carry = agg;
+        wp.nchunks = plan.chunks;
+        mark_pass_begin(st);
+        e = io == SSM_F32 ? ssm::ws_launch_f32(dstate, plan.lanes, 4, 1, wm, wp, st)
+                          : ssm::ws_launch_bf16(dstate, plan.lanes, 4, 1, wm, wp, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        mark_pass_end(st);
+        return SSM_OK;
+    }
     mark_pass_begin(st);
     e = io == SSM_F32 ? launch_tma_n<float, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st)
                       : launch_tma_n<__nv_bfloat16, ssm::ScanMode::Full>(m, p, dstate, plan.lanes, plan.chunks, st);
@@ -551,7 +586,7 @@ struct WsPlan {
 // Bytes of a tile row of the warp-specialised pass: 32, or 16 per segment.
 int ws_row_bytes(int seg) { return seg > 1 ? 16 * seg : ssm::kScanRowBytes; }
 
-int ws_smem(ssm_dtype_t io, int dstate, int lanes, int nw, int seg = 1) {
+int ws_smem(ssm_dtype_t io, int dstate, int lanes, int nw, int seg) {
     return io == SSM_F32 ? ssm::ws_smem_bytes_f32(dstate, lanes, nw, seg)
                          : ssm::ws_smem_bytes_bf16(dstate, lanes, nw, seg);
 }
@@ -636,6 +671,8 @@ ssm_status_t run_scan_ws(const void* u, const void* delta, const void* z, const 
     p.stop_tile = env_int("SSM_DEBUG_STOP_LOADS_AT_TILE", -1);
     const int budget_us = env_int("SSM_DEBUG_WAIT_BUDGET_US", 0);
     p.wait_budget_ns = budget_us > 0 ? static_cast<unsigned long long>(budget_us) * 1000ull : ssm::kWaitBudgetNs;
+    p.carry = nullptr;
+    p.nchunks = 1;
     mark_pass_begin(st);
     const cudaError_t e = io == SSM_F32 ? ssm::ws_launch_f32(dstate, plan.lanes, plan.nw, plan.seg, m, p, st)
                                         : ssm::ws_launch_bf16(dstate, plan.lanes, plan.nw, plan.seg, m, p, st);

@@ -53,3 +53,20 @@ def test_segmented_no_gate_no_skip(ssm, monkeypatch, lanes, seg):
     ref_y, ref_h = oracle_scan(x, final_state=True)
     assert_close(to_np(y), ref_y, "bf16", "no gate")
     assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_warp_specialised_fused_pass_of_a_chunked_plan(ssm, monkeypatch, io):
+    """SSM_FUSED_KERNEL=ws runs the fused pass of a chunked plan on the
+    warp-specialised kernel (each CTA a time chunk, starting from the carried
+    state): y and the final state against the oracle, with an initial state."""
+    monkeypatch.setenv("SSM_FUSED_KERNEL", "ws")
+    monkeypatch.setenv("SSM_FORCE_CHUNKS", "5")
+    x = I.make_scan_inputs(2, 192, 16, 1000, 2, io=io, recipe="scaled", seed=47, device="cuda", with_h0=True)
+    assert ssm.scan_plan(2, 192, 16, 1000, 2, x.u.dtype)["chunks"] == 5
+    y, hf = ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias, h0=x.h0)
+    torch.cuda.synchronize()
+    ref_y, ref_h = oracle_scan(x, h0=x.h0, final_state=True)
+    assert_close(to_np(y), ref_y, io, f"ws fused pass, 5 chunks, io={io}")
+    assert rel_l2(to_np(hf), ref_h) <= STATE_REL_L2
+    assert ssm.device_status() == 0
