@@ -191,3 +191,36 @@ def test_autograd_function_matches_scan_bwd(ssm):
         got = leaves[k].grad
         assert got is not None and got.dtype == leaves[k].dtype, k
         assert rel_l2(to_np(got), to_np(ref[r].to(got.dtype))) <= 1e-6, k
+
+
+def test_backward_writes_exactly_its_gradients(ssm):
+    """Canary: every gradient is a view into a larger buffer filled with a
+    sentinel (ragged L = 300 over three chunks, 70 channels, two groups, bf16);
+    the kernels must write exactly the gradients' elements, and the values
+    must match the oracle."""
+    x = I.make_scan_inputs(1, 70 * 2, 16, 300, 2, io="bf16", recipe="scaled", seed=77, device="cuda", with_h0=True)
+    dy = I.make_scan_inputs(1, 70 * 2, 16, 300, 2, io="bf16", recipe="scaled", seed=78, device="cuda").u
+    batch, dim, L = x.u.shape
+    N, G = x.A.shape[1], x.B.shape[1]
+    shapes = dict(du=((batch, dim, L), torch.bfloat16), ddelta=((batch, dim, L), torch.bfloat16),
+                  dz=((batch, dim, L), torch.bfloat16), dA=((dim, N), torch.float32),
+                  dB=((batch, G, N, L), torch.float32), dC=((batch, G, N, L), torch.float32),
+                  dD=((dim,), torch.float32), ddt_bias=((dim,), torch.float32), dh0=((batch, dim, N), torch.float32))
+    pad = 2048
+    bigs, out = {}, {}
+    for k, (shape, dt) in shapes.items():
+        n = int(np.prod(shape))
+        bigs[k] = torch.full((n + 2 * pad,), 7.0, dtype=dt, device="cuda")
+        out[k] = bigs[k][pad:pad + n].view(shape)
+    gr = ssm.scan_bwd(x.u, x.delta, x.A, x.B, x.C, dy, z=x.z, D=x.D, dt_bias=x.dt_bias, h0=x.h0, out=out)
+    torch.cuda.synchronize()
+    for k, (shape, dt) in shapes.items():
+        n = int(np.prod(shape))
+        assert torch.all(bigs[k][:pad] == 7.0) and torch.all(bigs[k][pad + n:] == 7.0), k
+    f = x.as_f64()
+    ref = oracle.scan_bwd(f["u"], f["delta"], f["A"], f["B"], f["C"], to_np(dy), z=f["z"], Dskip=f["Dskip"],
+                          dt_bias=f["dt_bias"], h0=f["h0"])
+    for k in ("du", "ddelta", "dz"):
+        assert rel_l2(to_np(gr[k]), ref[k]) <= 5e-3, k
+    for k in ("dA", "dB", "dC", "dD", "ddt_bias", "dh0"):
+        assert rel_l2(to_np(gr[k]), ref[k]) <= 1e-3, k

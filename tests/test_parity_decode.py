@@ -130,3 +130,32 @@ def test_staged_decode_steps(ssm, io, dim, G):
         assert_close(to_np(y), ref_y, io, f"step {step}")
         assert rel_l2(to_np(state), ref_state) <= STATE_REL_L2
     assert ssm.device_status() == 0
+
+
+@pytest.mark.parametrize("path", [None, "tma"], indirect=True)
+def test_decode_writes_exactly_its_state_and_y(ssm, path):
+    """Canary: the state and y are views into larger buffers filled with a
+    sentinel; 200 channels (a partial 128-channel block, and a partial 32-row
+    box for the warp-specialised kernel's per-warp state stores), 3 steps."""
+    batch, dim, N = 5, 200, 16
+    prm = I.decode_params(dim, N, recipe="scaled", seed=2, device="cuda")
+    s0 = I.make_decode_state(batch, dim, N, seed=2, device="cuda")
+    n = s0.numel()
+    big = torch.full((n + 8192,), 7.0, dtype=torch.float32, device="cuda")
+    state = big[4096:4096 + n].view_as(s0)
+    state.copy_(s0)
+    ref_state = to_np(s0)
+    f = {k: to_np(v) for k, v in prm.items()}
+    big_y = torch.full((batch * dim + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = big_y[2048:2048 + batch * dim].view(batch, dim)
+    for step in range(3):
+        tok = I.make_decode_token(batch, dim, N, step, io="bf16", seed=2, device="cuda")
+        run_step(ssm, state, tok, prm, out=y)
+        torch.cuda.synchronize()
+        t = {k: to_np(v) for k, v in tok.items()}
+        ref_state, ref_y = oracle.state_update(ref_state, t["u"], t["delta"], f["A"], t["B"], t["C"],
+                                               z=t["z"], Dskip=f["D"], dt_bias=f["dt_bias"])
+        assert_close(to_np(y), ref_y, "bf16", f"step {step}")
+        assert rel_l2(to_np(state), ref_state) <= STATE_REL_L2
+    assert torch.all(big[:4096] == 7.0) and torch.all(big[4096 + n:] == 7.0)
+    assert torch.all(big_y[:2048] == 7.0) and torch.all(big_y[2048 + batch * dim:] == 7.0)

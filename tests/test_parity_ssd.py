@@ -88,3 +88,22 @@ def test_ssd_full_workload_sampled_heads(ssm):
             eh = rel_l2(to_np(hf[b:b + 1, h * P:(h + 1) * P]), rh)
             assert e <= BF16_REL_L2, f"b={b} h={h}: y rel_l2 {e:.3e}"
             assert eh <= STATE_REL_L2, f"b={b} h={h}: h_final rel_l2 {eh:.3e}"
+
+
+def test_ssd_writes_exactly_its_outputs(ssm):
+    """Canary: y and the final state are views into larger buffers filled with
+    a sentinel (a ragged last chunk, two groups); the kernel must write exactly
+    their elements."""
+    x = I.make_ssd_inputs(1, 4, 64, 128, 200, 2, seed=93, device="cuda", with_h0=True)
+    n, m = x["x"].numel(), x["h0"].numel()
+    big_y = torch.full((n + 8192,), 7.0, dtype=torch.bfloat16, device="cuda")
+    big_h = torch.full((m + 8192,), 7.0, dtype=torch.float32, device="cuda")
+    y = big_y[4096:4096 + n].view_as(x["x"])
+    hf = big_h[4096:4096 + m].view_as(x["h0"])
+    run(ssm, x, out=y, h_final=hf)
+    torch.cuda.synchronize()
+    assert torch.all(big_y[:4096] == 7.0) and torch.all(big_y[4096 + n:] == 7.0)
+    assert torch.all(big_h[:4096] == 7.0) and torch.all(big_h[4096 + m:] == 7.0)
+    ry, rh = ref(x)
+    assert rel_l2(to_np(y), ry) <= BF16_REL_L2
+    assert rel_l2(to_np(hf), rh) <= STATE_REL_L2
