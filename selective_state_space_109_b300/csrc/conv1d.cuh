@@ -57,8 +57,12 @@ __device__ __forceinline__ void conv_st(T* p, long long i, float v) {
 // Vector path: L * sizeof(T) is a multiple of 16 and x, out are 16-byte aligned.
 // A warp takes U groups of 32 consecutive chunks per iteration and issues all
 // U loads before it computes, so that every lane has U x 16 bytes in flight.
+// Five resident CTAs per SM (48 registers, a few spilled): measured 303.7 us
+// against 323.5 us at four (60 registers) on b1 d5120 L65536 bf16, and 65.6
+// against 67.9 us on b8 d2048 L4096; six (40 registers) and loading the next
+// iteration's packets ahead (84 registers) were slower.
 template <typename T, int W, typename Idx>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 5)
 conv1d_vec_kernel(const ConvParams p) {
     constexpr int VPC = 16 / static_cast<int>(sizeof(T));
     constexpr int H = W - 1;  // history length
