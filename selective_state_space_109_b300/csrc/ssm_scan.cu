@@ -332,6 +332,12 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
             }
         }
     }
+    // At N <= 16 the summary pass runs with the fewest lanes the states allow:
+    // measured best on both chunked N = 16 plans (b2 d1536 L2048: 66.1 us
+    // against 68.3 and 71.8 at 2 and 4 lanes; b1 d5120 L65536: 2226 us
+    // against 2407 and 2618), where the cost model above preferred 2 lanes
+    // for the first.
+    if (best.chunks > 1 && dstate <= 16) best.agg_lanes = lmin;
     const int fl = env_int("SSM_FORCE_LANES", 0);
     if ((fl == 1 || fl == 2 || fl == 4) && fl <= lmax && fl >= lmin) best.lanes = fl;
     const int fk = env_int("SSM_FORCE_CHUNKS", 0);
