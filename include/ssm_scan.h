@@ -52,6 +52,18 @@
  * - batch == 0 is an empty problem: the call returns SSM_OK without touching
  *   any pointer.  seqlen == 0 is accepted: nothing is read or written except
  *   h_final (which then equals h0, or zeros).
+ * - Environment variables read at each call, for tests and tuning only (the
+ *   defaults are the measured best; results differ at most in fp32 rounding
+ *   order): SSM_FORCE_PATH=generic (register-staged scan and decode kernels),
+ *   SSM_FORCE_LANES, SSM_FORCE_CHUNKS, SSM_FORCE_AGG_LANES (the launch plan),
+ *   SSM_FORCE_NW (consumer warps of the warp-specialised pass),
+ *   SSM_FORCE_SEG (its time-segmented variant), SSM_SCAN_KERNEL=tma (the
+ *   CTA-synchronous pass for single-pass plans), SSM_FUSED_KERNEL=ws (the
+ *   warp-specialised fused pass for chunked plans), SSM_DECODE_KERNEL=tma and
+ *   SSM_DECODE_TILE=<channels>x<stages> (the bulk-staged decode); and, to
+ *   test the bounded waits, SSM_DEBUG_STOP_LOADS_AT_TILE and
+ *   SSM_DEBUG_WAIT_BUDGET_US (the warp-specialised pass stops loading at that
+ *   tile, and its waits give up after that many microseconds).
  */
 #ifndef SSM_SCAN_H
 #define SSM_SCAN_H
