@@ -36,8 +36,9 @@
 // butterfly-reduced over the LN lanes; dB and dC sum over the channels of the group: a
 // reduce-scatter over the channels of a warp, a sum over the CTA's warps in
 // shared memory, then one atomic add per (state, step) per CTA into fp32
-// buffers.  dA, dD and ddt_bias collect in registers and are added atomically
-// once per CTA.
+// buffers (vector adds of four steps when the rows keep 16-byte alignment).
+// dA, dD and ddt_bias collect in registers and are added atomically once per
+// CTA.
 #pragma once
 
 #include "ssm_device.cuh"
@@ -703,16 +704,37 @@ scan_bwd_kernel(const BwdParams p) {
         }
         __syncthreads();
 
-        // dB, dC of the tile: sum over warps, one atomic add per CTA.
-        for (int e = threadIdx.x; e < 2 * N * TT; e += THREADS) {
-            const int t = e % TT;
-            const int k = e / TT;  // tensor * N + n
-            if (t0 + t < L) {
-                float v = 0.f;
+        // dB, dC of the tile: sum over warps, one atomic add per CTA -- four
+        // steps per vector add when the rows keep 16-byte alignment.
+        if (L % 4 == 0) {
+            for (int e = threadIdx.x; e < 2 * N * (TT / 4); e += THREADS) {
+                const int t = (e % (TT / 4)) * 4;
+                const int k = e / (TT / 4);  // tensor * N + n
+                if (t0 + t < L) {
+                    float v[4];
 #pragma unroll
-                for (int w = 0; w < kBwdWarps; ++w) v += red[w][t][k];
-                float* dst = (k / N) ? p.dC : p.dB;
-                atomicAdd(dst + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + t, v);
+                    for (int q = 0; q < 4; ++q) {
+                        v[q] = 0.f;
+#pragma unroll
+                        for (int w = 0; w < kBwdWarps; ++w) v[q] += red[w][t + q][k];
+                    }
+                    float* dst = ((k / N) ? p.dC : p.dB) + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + t;
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v[0]), "f"(v[1]),
+                                 "f"(v[2]), "f"(v[3])
+                                 : "memory");
+                }
+            }
+        } else {
+            for (int e = threadIdx.x; e < 2 * N * TT; e += THREADS) {
+                const int t = e % TT;
+                const int k = e / TT;  // tensor * N + n
+                if (t0 + t < L) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kBwdWarps; ++w) v += red[w][t][k];
+                    float* dst = (k / N) ? p.dC : p.dB;
+                    atomicAdd(dst + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + t, v);
+                }
             }
         }
         // du, ddelta, dz rows of the tile.
