@@ -763,10 +763,14 @@ scan_bwd_kernel(const BwdParams p) {
             *reinterpret_cast<float2*>(p.dh0 + l.bd * N + l.j * S + 2 * k) = mu[k];
     }
     if (l.active) {
+        // dA of this lane's S states (16-byte aligned: S is 4 or 8 floats), four per vector add.
+        static_assert(S % 4 == 0, "vector adds of dA take whole groups of four states");
 #pragma unroll
-        for (int k = 0; k < P2; ++k) {
-            atomicAdd(p.dA + static_cast<long long>(l.d) * N + l.j * S + 2 * k, dA_acc[k].x);
-            atomicAdd(p.dA + static_cast<long long>(l.d) * N + l.j * S + 2 * k + 1, dA_acc[k].y);
+        for (int k = 0; k < P2; k += 2) {
+            float* da = p.dA + static_cast<long long>(l.d) * N + l.j * S + 2 * k;
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(da), "f"(dA_acc[k].x),
+                         "f"(dA_acc[k].y), "f"(dA_acc[k + 1].x), "f"(dA_acc[k + 1].y)
+                         : "memory");
         }
         if (l.j == 0) {
             if (p.dD) atomicAdd(p.dD + l.d, dD_acc);
