@@ -16,7 +16,7 @@
 //   dA[n] += lam_t[n] Delta_t Abar_t[n] h_{t-1}[n],  dD += g_t u_t,
 //   ddt_bias += ddelta_t,  dh0[n] = Abar_0[n] lam_0[n].
 //
-// Structure.  Time is cut into chunks of bwd_chunk_steps(N) steps; a CTA owns
+// Structure.  Time is cut into chunks of p.chunk_steps steps; a CTA owns
 // CH channels of one (sequence, group) and one chunk.  Both recurrences run
 // across chunks through summaries, as in the forward pass:
 //   1. summary pass: per chunk, from a zero state, the decay product P and
@@ -53,10 +53,10 @@ constexpr int kBwdWarps = 4;
 __host__ __device__ constexpr int bwd_states_per_lane(int n) { return n > 128 ? 8 : 4; }
 
 // Tiles per time chunk: their start states are held in shared memory (16 KB
-// per 8 tiles at 4 states a lane); fewer from N = 64 on, whose dB/dC staging
-// is larger.
-__host__ __device__ constexpr int bwd_chunk_tiles(int n) { return n >= 64 ? 8 : 16; }
-__host__ __device__ constexpr int bwd_chunk_steps(int n) { return kBwdTT * bwd_chunk_tiles(n); }
+// per 8 tiles at 4 states a lane).  The chunk length is chosen per call (see
+// bwd_chunk_tiles_for in the host code) up to bwd_chunk_tiles_max tiles: 20,
+// or 8 from N = 64 on, whose dB/dC staging is larger.
+__host__ __device__ constexpr int bwd_chunk_tiles_max(int n) { return n >= 64 ? 8 : 20; }
 
 struct BwdParams {
     const void *u, *delta, *z, *dy, *B, *C;
@@ -66,6 +66,7 @@ struct BwdParams {
     float* fagg;  // [nchunks][batch*dim][2][N]: P, then E (replaced by the state entering chunk c+1)
     float* bagg;  // [nchunks][batch*dim][N]: M (replaced by the adjoint entering chunk c-1 from the right)
     int batch, dim, seqlen, ngroups, dim_per_group, blocks_per_group, nchunks;
+    int chunk_steps;  // steps per time chunk: a multiple of kBwdTT, at most kBwdTT * bwd_chunk_tiles_max(N)
     int vec_ok;   // every row may be read and written as aligned 16-byte packets
 };
 
@@ -291,8 +292,8 @@ scan_bwd_summary_kernel(const BwdParams p) {
     const int d = g * p.dim_per_group + (active ? dloc0 + r : 0);
     const long long bd = static_cast<long long>(b) * p.dim + d;
     const int L = p.seqlen;
-    const int s0 = c * bwd_chunk_steps(N);
-    const int s1 = min(L, s0 + bwd_chunk_steps(N));
+    const int s0 = c * p.chunk_steps;
+    const int s1 = min(L, s0 + p.chunk_steps);
     const int ntile = (s1 - s0 + TT - 1) / TT;
     const long long BD = static_cast<long long>(p.batch) * p.dim;
     const bool vec = p.vec_ok != 0;
@@ -462,7 +463,7 @@ struct BwdLayout {
     static constexpr int TT = kBwdTT;
     static constexpr int THREADS = kBwdWarps * 32;
     static constexpr int CKPT = 0;                                                  // float4 [tiles * S/4][THREADS]
-    static constexpr int ACT = CKPT + bwd_chunk_tiles(N) * (Sh::S / 4) * THREADS * 16;  // T [2][4][CH][TT]
+    static constexpr int ACT = CKPT + bwd_chunk_tiles_max(N) * (Sh::S / 4) * THREADS * 16;  // T [2][4][CH][TT]
     static constexpr int BC = ACT + 2 * 4 * Sh::CH * TT * static_cast<int>(sizeof(T));  // T [2][2][N][TT]
     static constexpr int SC = BC + 2 * 2 * N * TT * static_cast<int>(sizeof(T));   // float4 [TT][CH]
     static constexpr int SC2 = SC + TT * Sh::CH * 16;                               // float2 [TT][CH]
@@ -498,8 +499,8 @@ scan_bwd_kernel(const BwdParams p) {
     const BwdLane l = bwd_lane<N>(p);
     const int c = blockIdx.y;
     const int L = p.seqlen;
-    const int s0 = c * bwd_chunk_steps(N);
-    const int s1 = min(L, s0 + bwd_chunk_steps(N));
+    const int s0 = c * p.chunk_steps;
+    const int s1 = min(L, s0 + p.chunk_steps);
     const int ntile = (s1 - s0 + TT - 1) / TT;
     const long long BD = static_cast<long long>(p.batch) * p.dim;
     const bool vec = p.vec_ok != 0;

@@ -999,15 +999,44 @@ cudaError_t launch_conv_update_t(void* state, const void* x, const float* w, con
 // Backward pass
 // ---------------------------------------------------------------------------
 
-int bwd_chunk_steps_for(int dstate) { return ssm::bwd_chunk_steps(dstate); }
+// Tiles per time chunk of the backward pass.  The main pass runs three CTAs
+// per SM, each owning one (channel block, chunk); the length is chosen among
+// 16..20 tiles (8 from N = 64 on) so that its CTAs fill whole waves on 148
+// SMs: minimum of ceil(CTAs / 444) x tiles, the shorter chunk on a tie.  b2
+// d1536 L2048: 20 tiles (13 chunks, 2.81 waves) in place of 16 (16 chunks,
+// 3.46 waves).  A function of the arguments only, so that the workspace size
+// needs no device.
+int bwd_chunk_tiles_for(int batch, int dim, int dstate, int seqlen, int ngroups) {
+    const int tmax = ssm::bwd_chunk_tiles_max(dstate);
+    if (dstate >= 64) return tmax;
+    const int ch = ssm::kBwdWarps * 32 / (dstate / ssm::bwd_states_per_lane(dstate));
+    const long long blocks = static_cast<long long>((dim / ngroups + ch - 1) / ch) * ngroups * batch;
+    const long long slots = 148LL * 3;
+    int best = 16;
+    long long best_cost = -1;
+    for (int t = 16; t <= tmax; ++t) {
+        const long long steps = static_cast<long long>(ssm::kBwdTT) * t;
+        const long long k = std::max(1LL, (seqlen + steps - 1) / steps);
+        const long long cost = ((blocks * k + slots - 1) / slots) * t;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = t;
+        }
+    }
+    return best;
+}
 
-int bwd_nchunks(int seqlen, int dstate) {
-    const int cs = bwd_chunk_steps_for(dstate);
+int bwd_chunk_steps_for(int batch, int dim, int dstate, int seqlen, int ngroups) {
+    return ssm::kBwdTT * bwd_chunk_tiles_for(batch, dim, dstate, seqlen, ngroups);
+}
+
+int bwd_nchunks(int batch, int dim, int dstate, int seqlen, int ngroups) {
+    const int cs = bwd_chunk_steps_for(batch, dim, dstate, seqlen, ngroups);
     return std::max(1, (seqlen + cs - 1) / cs);
 }
 
-size_t bwd_workspace_bytes(int batch, int dim, int dstate, int seqlen) {
-    const int k = bwd_nchunks(seqlen, dstate);
+size_t bwd_workspace_bytes(int batch, int dim, int dstate, int seqlen, int ngroups) {
+    const int k = bwd_nchunks(batch, dim, dstate, seqlen, ngroups);
     if (k <= 1 || batch <= 0) return 0;
     // fagg [k][BD][2][N] and bagg [k][BD][N], fp32
     return static_cast<size_t>(k) * static_cast<size_t>(batch) * static_cast<size_t>(dim) *
@@ -1077,10 +1106,10 @@ ssm_status_t ssm_note_cuda_error(cudaError_t e) { return cuda_fail(e); }
 extern "C" {
 
 size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_dtype_t io) {
-    (void)ngroups;
     (void)io;
-    if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0) return 0;
-    return bwd_workspace_bytes(batch, dim, dstate, seqlen);
+    if (batch <= 0 || dim <= 0 || dstate <= 0 || seqlen <= 0 || ngroups <= 0 || dim % ngroups != 0) return 0;
+    if (!supported_dstate(dstate)) return 0;
+    return bwd_workspace_bytes(batch, dim, dstate, seqlen, ngroups);
 }
 
 ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const void* z, const float* A, const void* B,
@@ -1138,7 +1167,8 @@ ssm_status_t ssm_scan_bwd(const void* u, const void* delta, const void* z, const
     p.dim_per_group = dim / ngroups;
     const int ch = ssm::kBwdWarps * 32 / (dstate / ssm::bwd_states_per_lane(dstate));
     p.blocks_per_group = (p.dim_per_group + ch - 1) / ch;
-    p.nchunks = bwd_nchunks(seqlen, dstate);
+    p.chunk_steps = bwd_chunk_steps_for(batch, dim, dstate, seqlen, ngroups);
+    p.nchunks = bwd_nchunks(batch, dim, dstate, seqlen, ngroups);
     p.vec_ok = (static_cast<long long>(seqlen) * es) % 16 == 0;
     if (p.nchunks > 1) {
         const size_t BDN = static_cast<size_t>(batch) * dim * dstate;

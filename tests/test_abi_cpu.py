@@ -191,6 +191,11 @@ def test_bwd_argument_errors(lib):
     assert bwd(L=300, ws=Q + 0x900, ws_bytes=need - 16) == 4
     assert lib.ssm_scan_bwd_workspace_size(1, 4, 16, 128, 1, 1) == 0   # one chunk: no workspace
     assert lib.ssm_scan_bwd_workspace_size(2, 4, 64, 129, 1, 1) == 3 * 2 * 4 * 64 * 3 * 4
+    # The chunk length fills whole waves of three CTAs on each of 148 SMs: b2
+    # d1536 L2048 takes 20 tiles of 8 steps (13 chunks, 96 x 13 CTAs) where
+    # 16 tiles would leave a partial fourth wave; b8 d2048 L4096 keeps 16.
+    assert lib.ssm_scan_bwd_workspace_size(2, 1536, 16, 2048, 1, 1) == 13 * 2 * 1536 * 16 * 3 * 4
+    assert lib.ssm_scan_bwd_workspace_size(8, 2048, 16, 4096, 1, 1) == 32 * 8 * 2048 * 16 * 3 * 4
     assert bwd(batch=0, u=None, dy=None, du=None, dd=None, dA=None, dB=None, dC=None) == 0  # empty problem
 
 
