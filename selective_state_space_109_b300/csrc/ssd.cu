@@ -81,8 +81,11 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
         return SSM_OK;
     }
     if (!encode_tiled_fn()) return SSM_ERR_CUDA;
-    CUtensorMap mx, mb, mc;
+    CUtensorMap mx, mb, mc, mz, my;
+    // z's map is encoded on x when there is no z (the kernel then never uses it).
     const bool ok = encode_rows(&mx, x, batch * dim, seqlen, ssm::ssd::P) &&
+                    encode_rows(&mz, z ? z : x, batch * dim, seqlen, ssm::ssd::P) &&
+                    encode_rows(&my, y, batch * dim, seqlen, ssm::ssd::P) &&
                     encode_rows(&mb, B, static_cast<long long>(batch) * ngroups * dstate, seqlen, ssm::ssd::N) &&
                     encode_rows(&mc, C, static_cast<long long>(batch) * ngroups * dstate, seqlen, ssm::ssd::N);
     if (!ok) return SSM_ERR_CUDA;
@@ -104,7 +107,7 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
     }
     const long long grid = static_cast<long long>(batch) * nheads;
     if (grid > 0x7fffffffLL) return SSM_ERR_INVALID_ARG;
-    ssm::ssd_fwd_kernel<<<static_cast<unsigned>(grid), ssm::ssd::THREADS, ssm::ssd::SMEM_BYTES, st>>>(mx, mb, mc, p);
+    ssm::ssd_fwd_kernel<<<static_cast<unsigned>(grid), ssm::ssd::THREADS, ssm::ssd::SMEM_BYTES, st>>>(mx, mb, mc, mz, my, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SSM_OK : ssm_note_cuda_error(e);
 }

@@ -27,9 +27,10 @@
 // two chunks ahead.  Sixteen compute warps -- four per quarter of the 128
 // tensor-memory lanes, each taking a quarter of every accumulator row's
 // columns -- build the computed operands (M, w o X, H), read the accumulators
-// back with tcgen05.ld, read z and write y straight from and to global memory
-// (per warp and channel, 32 consecutive steps).  The chunks are
-// software-pipelined so that
+// back with tcgen05.ld and form y in a shared-memory tile: z arrives there
+// by TMA while the chunk's operands are built, each thread overwrites its own
+// z elements with y, and the control warp stores the tile by TMA.  The chunks
+// are software-pipelined so that
 // the tensor cores run while the threads compute: Yd(c) = M X runs while the
 // compute warps weight chunk c+1's x, and G, S, Yoff of chunk c+1 run while
 // they form chunk c's output.  Only the lower triangle of M (s <= t) is
@@ -75,8 +76,9 @@ constexpr int CG = COMPUTE / 128;     // column groups (each a quarter of an acc
 // Shared-memory layout (bytes from a 1024-aligned base).  Tiles of 128-byte
 // rows, two halves of 64 steps along time where a row holds 128 steps.  x has
 // three buffers (its tile loads two chunks ahead); C and B are reloaded as
-// soon as the contractions of the chunk have read them.  z is read by the
-// output step straight from global memory.
+// soon as the contractions of the chunk have read them.  One z tile: loaded
+// once the previous chunk's y (formed in the same tile) has been read out by
+// its TMA store.
 constexpr int XBUFS = 3;                      // x buffers
 constexpr int CS_OFF = 0;                     // C  [N rows][Q]   (2 halves of N x 128 B)
 constexpr int BS_OFF = CS_OFF + N * 256;      // B  [N rows][Q]
@@ -85,10 +87,11 @@ constexpr int XH_OFF = XS_OFF + XBUFS * P * 256;  // w o x, bf16 head  [P rows][
 constexpr int XL_OFF = XH_OFF + P * 256;      // w o x, bf16 tail (the rounding error of the head)
 constexpr int MS_OFF = XL_OFF + P * 256;      // M  [Q rows][Q]     (A operand of Ydiag)
 constexpr int HS_OFF = MS_OFF + Q * 256;      // H  [N rows][P]     (bf16 copy, B operand of Yoff)
-constexpr int F_OFF = HS_OFF + N * 128;       // floats, two buffers of: (cs_t, Delta_t) pairs [Q], w_t [Q]
+constexpr int ZS_OFF = HS_OFF + N * 128;      // z, then y in place  [P rows][Q]
+constexpr int F_OFF = ZS_OFF + P * 256;       // floats, two buffers of: (cs_t, Delta_t) pairs [Q], w_t [Q]
 constexpr int F_BUF = 3 * Q;                  // floats per buffer
 constexpr int BAR_OFF = F_OFF + 2 * F_BUF * 4;
-constexpr int SMEM_BYTES = BAR_OFF + 64 + 1024;  // six mbarriers, the TMEM address, alignment slack
+constexpr int SMEM_BYTES = BAR_OFF + 64 + 1024;  // seven mbarriers, the TMEM address, alignment slack
 constexpr int XBUF = P * 256;                     // bytes of one x buffer
 constexpr int HALF_C = N * 128;                   // byte stride between the time halves of C, B
 constexpr int HALF_X = P * 128;                   // ... of x, w o x
@@ -227,8 +230,8 @@ __device__ __forceinline__ void bf_put(unsigned char* tile, uint32_t off, float 
 // One CTA per (sequence b, head h): blockIdx.x = b * nheads + h.
 __global__ void __launch_bounds__(ssd::THREADS, 1)
 ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_B,
-               const __grid_constant__ CUtensorMap tm_C,
-               const SsdParams p) {
+               const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_z,
+               const __grid_constant__ CUtensorMap tm_y, const SsdParams p) {
     using namespace ssd;
     extern __shared__ __align__(16) unsigned char smem_raw[];  // aligned below at run time
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -238,12 +241,14 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     unsigned char* Xl = smem + XL_OFF;
     unsigned char* Ms = smem + MS_OFF;
     unsigned char* Hs = smem + HS_OFF;
+    unsigned char* Zs = smem + ZS_OFF;
     float* fbase = reinterpret_cast<float*>(smem + F_OFF);  // per buffer: float2 (cs_t, Delta_t) [Q], w_t [Q]
     uint64_t* bc_bar = reinterpret_cast<uint64_t*>(smem + BAR_OFF);  // C, B of the current chunk
     uint64_t* x_bar = bc_bar + 1;                                    // x: one barrier per buffer
     uint64_t* mma1_bar = bc_bar + 1 + XBUFS;                         // G, S, Yoff of a chunk done
     uint64_t* mma2_bar = mma1_bar + 1;                               // Ydiag of a chunk done
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 48);
+    uint64_t* z_bar = bc_bar + 7;                                    // z of the current chunk
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3;      // tensor-memory lane quarter of this warp
@@ -280,17 +285,28 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         for (int half = 0; half < 2; ++half)
             tma_load_2d(smem + XS_OFF + buf * XBUF + half * HALF_X, &tm_x, c * Q + half * 64, xrow, &x_bar[buf]);
     };
+    auto load_z = [&](int c) {
+        mbar_arrive_expect_tx(z_bar, TX_X);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) tma_load_2d(Zs + half * HALF_X, &tm_z, c * Q + half * 64, xrow, z_bar);
+    };
     if (tid == CTRL) {
         mbar_init(bc_bar, 1);
 #pragma unroll
         for (int i = 0; i < XBUFS; ++i) mbar_init(&x_bar[i], 1);
         mbar_init(mma1_bar, 1);
         mbar_init(mma2_bar, 1);
+        mbar_init(z_bar, 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_x);
         prefetch_tensormap(&tm_B);
         prefetch_tensormap(&tm_C);
+        prefetch_tensormap(&tm_y);
         load_bc(0);
+        if (has_z) {
+            prefetch_tensormap(&tm_z);
+            load_z(0);
+        }
         for (int c = 0; c < XBUFS && c < nch; ++c) load_x(c);
     }
     if (warp == 0) {
@@ -405,16 +421,14 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         fence_proxy_async_smem();
         tc_fence_before();
     };
-    // G = C B^T, Yoff = C H_prev (into buffer c % 2), S = B^T (w o x) of
-    // chunk c, by the control thread once C and B have landed.
-    auto issue_mma1 = [&](int c) {
+    // G = C B^T and Yoff = C H_prev (into buffer c % 2) of chunk c, by the
+    // control thread once C and B have landed (H_prev's bf16 copy written).
+    auto issue_g_off = [&](int c) {
         mbar_wait(bc_bar, static_cast<uint32_t>(c & 1), p.status);
         tc_fence_after();
         const uint32_t cs_a = smem_addr(Cs), bs_a = smem_addr(Bs), hs_a = smem_addr(Hs);
-        const uint32_t xh_a = smem_addr(Xh), xl_a = smem_addr(Xl);
         const uint32_t id_g = umma_idesc(Q, Q, true, true);
         const uint32_t id_off = umma_idesc(Q, P, true, true);
-        const uint32_t id_s = umma_idesc(N, P, false, false);
         const uint32_t tm_off = tmem + TM_YOFF + static_cast<uint32_t>((c & 1) * P);
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {  // K = the N states, 16 rows per step
@@ -422,6 +436,15 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             umma_f16(tmem + TM_G, ca, umma_desc(bs_a + ks * 2048, HALF_C, 1024), id_g, ks > 0);
             umma_f16(tm_off, ca, umma_desc(hs_a + ks * 2048, HALF_C, 1024), id_off, ks > 0);
         }
+    };
+    // S = B^T (w o x) of chunk c once its weighted x is written; the commit
+    // covers every contraction of the chunk issued before it (G, Yoff, S).
+    auto issue_s = [&](int c) {
+        (void)c;
+        tc_fence_after();
+        const uint32_t bs_a = smem_addr(Bs);
+        const uint32_t xh_a = smem_addr(Xh), xl_a = smem_addr(Xl);
+        const uint32_t id_s = umma_idesc(N, P, false, false);
 #pragma unroll
         for (int ks = 0; ks < Q / 16; ++ks) {  // K = the chunk's steps
             const uint32_t koff = (ks & 3) * 32;  // 16 steps = 32 bytes into the 128-byte row
@@ -444,7 +467,10 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;  // this warp's TMEM lanes
     if (compute) weight_x(0);
     __syncthreads();
-    if (tid == CTRL) issue_mma1(0);
+    if (tid == CTRL) {
+        issue_g_off(0);
+        issue_s(0);
+    }
 
     for (int c = 0; c < nch; ++c) {
         const int t0 = c * Q;
@@ -456,7 +482,15 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         mbar_wait(mma1_bar, static_cast<uint32_t>(c & 1), p.status);
         tc_fence_after();
         float cs_t = 0.f;
-        if (tid == CTRL && c + 1 < nch) load_bc(c + 1);
+        if (tid == CTRL) {
+            if (c + 1 < nch) load_bc(c + 1);
+            // The previous chunk's y has been read out of the z tile: this
+            // chunk's z loads into it while the operands are built.
+            if (c > 0) {
+                bulk_wait_read<0>();
+                if (has_z) load_z(c);
+            }
+        }
         if (compute) {
             cs_t = cd[r].x;
             // M = G o 2^(cs_t - cs_s) Delta_s (s <= t): rows t = r, columns
@@ -506,7 +540,9 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         tc_fence_before();
         __syncthreads();
-        // Ydiag = M x, by the control thread; meanwhile the compute threads
+        // Ydiag = M x, then G and Yoff of the next chunk (G is read, H written),
+        // by the control thread, and the step scalars of the chunk after it
+        // (this chunk's scalars are read); meanwhile the compute threads
         // weight the next chunk's x
         if (tid == CTRL) {
             tc_fence_after();
@@ -519,30 +555,23 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                          umma_desc(xs_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_d, ks > 0);
             }
             umma_commit(mma2_bar);
+            if (c + 1 < nch) issue_g_off(c + 1);
         }
         if (c + 1 < nch) {
             if (compute) weight_x(c + 1);
             __syncthreads();
         }
         if (!compute) {
-            // G, S, Yoff of the next chunk (from the H just written) while the
-            // compute threads form this chunk's output; then the step scalars
-            // of the chunk after it
-            if (tid == CTRL && c + 1 < nch) issue_mma1(c + 1);
+            // S of the next chunk while the compute threads form this chunk's
+            // output; then the step scalars of the chunk after it
+            if (tid == CTRL && c + 1 < nch) issue_s(c + 1);
             if (c + 2 < nch) chunk_scalars(c + 2);
         } else {
             // (C) y = (Ydiag + 2^cs_t Yoff + D x) * silu(z), row t = r, channels
-            // PC cg .. PC cg + PC - 1: z read from global memory (per warp and
-            // channel, 32 consecutive steps) while Ydiag finishes, y written
-            // straight back the same way
-            const bool row_ok = t0 + r < L;
-            const long long rbase = (static_cast<long long>(xrow) + cg * PC) * L + t0 + r;
-            float zv[PC];
-            if (has_z && row_ok) {
-#pragma unroll
-                for (int i = 0; i < PC; ++i)
-                    zv[i] = __bfloat162float(__ldcs(p.z + rbase + static_cast<long long>(i) * L));
-            }
+            // PC cg .. PC cg + PC - 1, formed in the z tile in place (each
+            // element is read and written by this thread only); steps past
+            // the sequence's end are computed but not stored (the TMA store
+            // clips them)
             const int half = r >> 6, tc = r & 63;
             float xv[PC];
 #pragma unroll
@@ -553,22 +582,31 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             float yd[PC], yo[PC];
             tmem_ld16x2(tmem + lane_base + TM_YD + cg * PC,
                         tmem + lane_base + TM_YOFF + static_cast<uint32_t>(buf * P + cg * PC), yd, yo);
-            if (row_ok) {
-                __nv_bfloat16* yrow = p.y + rbase;
+            if (has_z) mbar_wait(z_bar, static_cast<uint32_t>(c & 1), p.status);
 #pragma unroll
-                for (int i = 0; i < PC; ++i) {
-                    float yv = fmaf(dsk, xv[i], fmaf(e_t, yo[i], yd[i]));
-                    if (has_z) yv *= silu<false>(zv[i]);
-                    yrow[static_cast<long long>(i) * L] = __float2bfloat16_rn(yv);
-                }
+            for (int i = 0; i < PC; ++i) {
+                const uint32_t off = half * HALF_X + sw128_elem(cg * PC + i, tc);
+                float yv = fmaf(dsk, xv[i], fmaf(e_t, yo[i], yd[i]));
+                if (has_z) yv *= silu<false>(bf_at(Zs, off));
+                bf_put(Zs, off, yv);
             }
+            fence_proxy_async_smem();
         }
         tc_fence_before();
         __syncthreads();
-        // x of this buffer is read (Ydiag is done, and so is the output step):
-        // chunk c + XBUFS loads into it.
-        if (tid == CTRL && c + XBUFS < nch) load_x(c + XBUFS);
+        if (tid == CTRL) {
+            // y of this chunk out of the z tile (the halves that start before
+            // the sequence's end)
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                if (t0 + half * 64 < L) tma_store_2d(&tm_y, t0 + half * 64, xrow, Zs + half * HALF_X);
+            bulk_commit();
+            // x of this buffer is read (Ydiag is done, and so is the output
+            // step): chunk c + XBUFS loads into it.
+            if (c + XBUFS < nch) load_x(c + XBUFS);
+        }
     }
+    if (tid == CTRL) bulk_wait<0>();
     if (p.h_final && compute) {
         float* hf = p.h_final + (static_cast<long long>(b) * dim + static_cast<long long>(h) * P) * N;
 #pragma unroll
