@@ -31,9 +31,9 @@
 // by TMA while the chunk's operands are built, each thread overwrites its own
 // z elements with y, and the control warp stores the tile by TMA.  The chunks
 // are software-pipelined so that
-// the tensor cores run while the threads compute: Yd(c) = M X runs while the
-// compute warps weight chunk c+1's x, and G, S, Yoff of chunk c+1 run while
-// they form chunk c's output.  Only the lower triangle of M (s <= t) is
+// the tensor cores run while the threads compute: Yd(c) = M X and G, Yoff
+// of chunk c+1 run while the compute warps weight chunk c+1's x, and S of
+// chunk c+1 while they form chunk c's output.  Only the lower triangle of M (s <= t) is
 // computed; its upper blocks are written as zeros.  Operand layouts are the
 // 128-byte-swizzled K-major or MN-major tiles of the UMMA descriptors; every
 // wait is bounded.
@@ -83,9 +83,9 @@ constexpr int XBUFS = 3;                      // x buffers
 constexpr int CS_OFF = 0;                     // C  [N rows][Q]   (2 halves of N x 128 B)
 constexpr int BS_OFF = CS_OFF + N * 256;      // B  [N rows][Q]
 constexpr int XS_OFF = BS_OFF + N * 256;      // x  [P rows][Q], XBUFS buffers
-constexpr int XH_OFF = XS_OFF + XBUFS * P * 256;  // w o x, bf16 head  [P rows][Q] (B operand of S)
-constexpr int XL_OFF = XH_OFF + P * 256;      // w o x, bf16 tail (the rounding error of the head)
-constexpr int MS_OFF = XL_OFF + P * 256;      // M  [Q rows][Q]     (A operand of Ydiag)
+constexpr int XW_OFF = XS_OFF + XBUFS * P * 256;  // w o x [2P rows][Q]: P rows of the bf16 head, then
+                                              // P rows of its tail (the head's rounding error); B operand of S
+constexpr int MS_OFF = XW_OFF + 2 * P * 256;  // M  [Q rows][Q]     (A operand of Ydiag)
 constexpr int HS_OFF = MS_OFF + Q * 256;      // H  [N rows][P]     (bf16 copy, B operand of Yoff)
 constexpr int ZS_OFF = HS_OFF + N * 128;      // z, then y in place  [P rows][Q]
 constexpr int F_OFF = ZS_OFF + P * 256;       // floats, two buffers of: (cs_t, Delta_t) pairs [Q], w_t [Q]
@@ -94,7 +94,8 @@ constexpr int BAR_OFF = F_OFF + 2 * F_BUF * 4;
 constexpr int SMEM_BYTES = BAR_OFF + 64 + 1024;  // seven mbarriers, the TMEM address, alignment slack
 constexpr int XBUF = P * 256;                     // bytes of one x buffer
 constexpr int HALF_C = N * 128;                   // byte stride between the time halves of C, B
-constexpr int HALF_X = P * 128;                   // ... of x, w o x
+constexpr int HALF_X = P * 128;                   // ... of x
+constexpr int HALF_W = 2 * P * 128;               // ... of w o x (head and tail rows)
 constexpr int HALF_M = Q * 128;                   // ... of M
 constexpr uint32_t TX_BC = 2u * N * 256u;         // bytes of one chunk's C and B tiles
 constexpr uint32_t TX_X = P * 256u;               // ... of its x tile
@@ -103,9 +104,9 @@ static_assert(COMPUTE == 4 * 128 && P == 16 * CG && Q == 32 * CG, "warp roles as
 
 // Tensor-memory columns (512 allocated; lanes = rows of the accumulators).
 constexpr uint32_t TM_G = 0;      // G      [Q lanes x Q]
-constexpr uint32_t TM_S = 128;    // S      [N lanes x P]
-constexpr uint32_t TM_YD = 192;   // Ydiag  [Q lanes x P]
-constexpr uint32_t TM_YOFF = 256; // Yoff   [Q lanes x P], two buffers (chunk parity)
+constexpr uint32_t TM_S = 128;    // S      [N lanes x 2P]: B^T (head of w o x), then B^T (its tail)
+constexpr uint32_t TM_YD = 256;   // Ydiag  [Q lanes x P]
+constexpr uint32_t TM_YOFF = 320; // Yoff   [Q lanes x P], two buffers (chunk parity)
 
 // Byte offset of element c (0..63) of row r in a tile of 128-byte rows written
 // with the 128-byte swizzle (16-byte unit index XOR row % 8).
@@ -237,8 +238,7 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     unsigned char* Cs = smem + CS_OFF;
     unsigned char* Bs = smem + BS_OFF;
-    unsigned char* Xh = smem + XH_OFF;
-    unsigned char* Xl = smem + XL_OFF;
+    unsigned char* Xw = smem + XW_OFF;
     unsigned char* Ms = smem + MS_OFF;
     unsigned char* Hs = smem + HS_OFF;
     unsigned char* Zs = smem + ZS_OFF;
@@ -415,8 +415,9 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 oh[k] = *reinterpret_cast<const uint32_t*>(&ph);
                 ol[k] = pack_bf2(v0 - fh.x, v1 - fh.y);
             }
-            *reinterpret_cast<uint4*>(Xh + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-            *reinterpret_cast<uint4*>(Xl + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+            const uint32_t woff = half * HALF_W + static_cast<uint32_t>(row * 128 + ((u8 ^ (row & 7)) << 4));
+            *reinterpret_cast<uint4*>(Xw + woff) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+            *reinterpret_cast<uint4*>(Xw + woff + P * 128) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -443,14 +444,13 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         (void)c;
         tc_fence_after();
         const uint32_t bs_a = smem_addr(Bs);
-        const uint32_t xh_a = smem_addr(Xh), xl_a = smem_addr(Xl);
-        const uint32_t id_s = umma_idesc(N, P, false, false);
+        const uint32_t xw_a = smem_addr(Xw);
+        const uint32_t id_s = umma_idesc(N, 2 * P, false, false);  // head and tail columns in one pass
 #pragma unroll
         for (int ks = 0; ks < Q / 16; ++ks) {  // K = the chunk's steps
             const uint32_t koff = (ks & 3) * 32;  // 16 steps = 32 bytes into the 128-byte row
             const uint64_t ba = umma_desc(bs_a + (ks >> 2) * HALF_C + koff, 16, 1024);
-            umma_f16(tmem + TM_S, ba, umma_desc(xh_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_s, ks > 0);
-            umma_f16(tmem + TM_S, ba, umma_desc(xl_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_s, 1);
+            umma_f16(tmem + TM_S, ba, umma_desc(xw_a + (ks >> 2) * HALF_W + koff, 16, 1024), id_s, ks > 0);
         }
         umma_commit(mma1_bar);
     };
@@ -531,10 +531,10 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             // H = 2^cs_end H + S, state row n = r, channels PC cg .. PC cg + PC - 1,
             // and its bf16 copy
             const float decay_all = ex2_approx(cd[Q - 1].x);
-            float sv[PC];
-            tmem_ld16(tmem + lane_base + TM_S + cg * PC, sv);
+            float sh[PC], sl[PC];
+            tmem_ld16x2(tmem + lane_base + TM_S + cg * PC, tmem + lane_base + TM_S + P + cg * PC, sh, sl);
 #pragma unroll
-            for (int i = 0; i < PC; ++i) H[i] = fmaf(decay_all, H[i], sv[i]);
+            for (int i = 0; i < PC; ++i) H[i] = fmaf(decay_all, H[i], sh[i] + sl[i]);
             store_hs();
             fence_proxy_async_smem();
         }
