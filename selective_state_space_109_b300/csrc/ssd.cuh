@@ -85,8 +85,7 @@ constexpr int BS_OFF = CS_OFF + N * 256;      // B  [N rows][Q]
 constexpr int XS_OFF = BS_OFF + N * 256;      // x  [P rows][Q], XBUFS buffers
 constexpr int XW_OFF = XS_OFF + XBUFS * P * 256;  // w o x [2P rows][Q]: P rows of the bf16 head, then
                                               // P rows of its tail (the head's rounding error); B operand of S
-constexpr int MS_OFF = XW_OFF + 2 * P * 256;  // M  [Q rows][Q]     (A operand of Ydiag)
-constexpr int HS_OFF = MS_OFF + Q * 256;      // H  [N rows][P]     (bf16 copy, B operand of Yoff)
+constexpr int HS_OFF = XW_OFF + 2 * P * 256;  // H  [N rows][P]     (bf16 copy, B operand of Yoff)
 constexpr int ZS_OFF = HS_OFF + N * 128;      // z, then y in place  [P rows][Q]
 constexpr int F_OFF = ZS_OFF + P * 256;       // floats, two buffers of: (cs_t, Delta_t) pairs [Q], w_t [Q]
 constexpr int F_BUF = 3 * Q;                  // floats per buffer
@@ -96,7 +95,6 @@ constexpr int XBUF = P * 256;                     // bytes of one x buffer
 constexpr int HALF_C = N * 128;                   // byte stride between the time halves of C, B
 constexpr int HALF_X = P * 128;                   // ... of x
 constexpr int HALF_W = 2 * P * 128;               // ... of w o x (head and tail rows)
-constexpr int HALF_M = Q * 128;                   // ... of M
 constexpr uint32_t TX_BC = 2u * N * 256u;         // bytes of one chunk's C and B tiles
 constexpr uint32_t TX_X = P * 256u;               // ... of its x tile
 static_assert(SMEM_BYTES <= 227 * 1024, "the SSD kernel's shared memory exceeds a CTA's limit");
@@ -107,6 +105,7 @@ constexpr uint32_t TM_G = 0;      // G      [Q lanes x Q]
 constexpr uint32_t TM_S = 128;    // S      [N lanes x 2P]: B^T (head of w o x), then B^T (its tail)
 constexpr uint32_t TM_YD = 256;   // Ydiag  [Q lanes x P]
 constexpr uint32_t TM_YOFF = 320; // Yoff   [Q lanes x P], two buffers (chunk parity)
+constexpr uint32_t TM_M = 448;    // M      [Q lanes x Q] bf16, two steps a column (A operand of Ydiag)
 
 // Byte offset of element c (0..63) of row r in a tile of 128-byte rows written
 // with the 128-byte swizzle (16-byte unit index XOR row % 8).
@@ -143,6 +142,17 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same contraction with the A operand in tensor memory: M rows in lanes,
+// two bf16 K elements a 32-bit column (the lower K index in the low half).
+__device__ __forceinline__ void umma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -212,6 +222,18 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)
     }
 }
 
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane, stored
+// and waited for in one asm statement.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&pr);
@@ -239,7 +261,6 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     unsigned char* Cs = smem + CS_OFF;
     unsigned char* Bs = smem + BS_OFF;
     unsigned char* Xw = smem + XW_OFF;
-    unsigned char* Ms = smem + MS_OFF;
     unsigned char* Hs = smem + HS_OFF;
     unsigned char* Zs = smem + ZS_OFF;
     float* fbase = reinterpret_cast<float*>(smem + F_OFF);  // per buffer: float2 (cs_t, Delta_t) [Q], w_t [Q]
@@ -494,22 +515,18 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         if (compute) {
             cs_t = cd[r].x;
             // M = G o 2^(cs_t - cs_s) Delta_s (s <= t): rows t = r, columns
-            // s = 32 cg .. 32 cg + 31 (a block above the diagonal is all zero)
-            const int half = cg >> 1;
-            const uint32_t rowoff = half * HALF_M + static_cast<uint32_t>(r * 128);
+            // s = 32 cg .. 32 cg + 31 (a block above the diagonal is all
+            // zero), into tensor-memory columns 16 cg .. 16 cg + 15 of M
+            uint32_t m32[16];
             if (cg > qd) {
 #pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const int unit = (cg & 1) * 4 + u4;
-                    *reinterpret_cast<uint4*>(Ms + rowoff + ((unit ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                }
+                for (int i = 0; i < 16; ++i) m32[i] = 0u;
             } else {
                 float gv[32];
                 tmem_ld32(tmem + lane_base + TM_G + cg * 32, gv);
                 const bool diag = cg == qd;
 #pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {  // four 16-byte units of 8 steps
-                    uint32_t o32[4];
+                for (int u4 = 0; u4 < 4; ++u4) {  // four groups of 8 steps
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int i0 = u4 * 8 + 2 * k;
@@ -521,13 +538,11 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             m0 = s0 <= r ? m0 : 0.f;
                             m1 = s0 + 1 <= r ? m1 : 0.f;
                         }
-                        o32[k] = pack_bf2(m0, m1);
+                        m32[u4 * 4 + k] = pack_bf2(m0, m1);
                     }
-                    const int unit = (cg & 1) * 4 + u4;
-                    *reinterpret_cast<uint4*>(Ms + rowoff + ((unit ^ (r & 7)) << 4)) =
-                        make_uint4(o32[0], o32[1], o32[2], o32[3]);
                 }
             }
+            tmem_st16(tmem + lane_base + TM_M + cg * 16, m32);
             // H = 2^cs_end H + S, state row n = r, channels PC cg .. PC cg + PC - 1,
             // and its bf16 copy
             const float decay_all = ex2_approx(cd[Q - 1].x);
@@ -546,13 +561,13 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         // weight the next chunk's x
         if (tid == CTRL) {
             tc_fence_after();
-            const uint32_t ms_a = smem_addr(Ms), xs_a = smem_addr(Xs);
+            const uint32_t xs_a = smem_addr(Xs);
             const uint32_t id_d = umma_idesc(Q, P, false, false);
 #pragma unroll
-            for (int ks = 0; ks < Q / 16; ++ks) {
+            for (int ks = 0; ks < Q / 16; ++ks) {  // M from tensor memory: 16 steps = 8 columns
                 const uint32_t koff = (ks & 3) * 32;
-                umma_f16(tmem + TM_YD, umma_desc(ms_a + (ks >> 2) * HALF_M + koff, 16, 1024),
-                         umma_desc(xs_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_d, ks > 0);
+                umma_f16_ta(tmem + TM_YD, tmem + TM_M + static_cast<uint32_t>(ks * 8),
+                            umma_desc(xs_a + (ks >> 2) * HALF_X + koff, 16, 1024), id_d, ks > 0);
             }
             umma_commit(mma2_bar);
             if (c + 1 < nch) issue_g_off(c + 1);
