@@ -604,7 +604,8 @@ int ws_smem(ssm_dtype_t io, int dstate, int lanes, int nw, int seg) {
 // state size keeps the CTA-synchronous pass).  Chunked plans keep the CTA-synchronous passes,
 // which measured faster there (b1 d5120 L65536: 2.20 ms against 2.58 ms for
 // the best chunked plan of the warp-specialised kernel).  Consumer warps per
-// CTA: two when four would leave fewer than two CTAs per SM.
+// CTA: two when four would leave SMs without a CTA (four measured 399 us
+// against 407 us for two on b8 d2048 L4096, 256 CTAs of four).
 // SSM_SCAN_KERNEL=tma forces the CTA-synchronous kernel (for comparisons).
 bool ws_single_pass(int batch, int dim, int dstate, int ngroups, ssm_dtype_t io, const ScanPlan& plan,
                     WsPlan* out) {
@@ -616,7 +617,7 @@ bool ws_single_pass(int batch, int dim, int dstate, int ngroups, ssm_dtype_t io,
         const int ch = nw * 32 / plan.lanes;
         return static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
     };
-    int nw = ctas(4) < 2LL * kPlanSms ? 2 : 4;
+    int nw = ctas(4) < kPlanSms ? 2 : 4;
     const int fnw = env_int("SSM_FORCE_NW", 0);
     if (fnw == 2 || fnw == 4 || fnw == 8) nw = fnw;
     if (ws_smem(io, dstate, plan.lanes, nw) <= 0) nw = 4;
