@@ -21,20 +21,21 @@
 // control warp issues the TMA loads of each chunk's C, B and x tiles
 // (128-byte swizzled rows of 64 steps; x two chunks ahead, C and B as soon
 // as the previous chunk's contractions have read them), the
-// tcgen05.mma contractions (bf16 operands from shared memory, fp32
-// accumulators in tensor memory, issued by one thread), and computes the
-// per-step scalars (Delta, the running sum of Delta A, the state weights w)
-// two chunks ahead.  Sixteen compute warps -- four per quarter of the 128
-// tensor-memory lanes, each taking a quarter of every accumulator row's
-// columns -- build the computed operands (M, w o X, H), read the accumulators
-// back with tcgen05.ld and form y in a shared-memory tile: z arrives there
-// by TMA while the chunk's operands are built, each thread overwrites its own
-// z elements with y, and the control warp stores the tile by TMA.  The chunks
-// are software-pipelined so that
-// the tensor cores run while the threads compute: Yd(c) = M X and G, Yoff
-// of chunk c+1 run while the compute warps weight chunk c+1's x, and S of
-// chunk c+1 while they form chunk c's output.  Only the lower triangle of M (s <= t) is
-// computed; its upper blocks are written as zeros.  Operand layouts are the
+// tcgen05.mma contractions (bf16 operands from shared memory, except M,
+// which Ydiag reads from tensor memory; fp32 accumulators in tensor memory;
+// issued by one thread), and computes the per-step scalars (Delta, the
+// running sum of Delta A, the state weights w) two chunks ahead.  Sixteen
+// compute warps -- four per quarter of the 128 tensor-memory lanes, each
+// taking a quarter of every accumulator row's columns -- build the computed
+// operands (M with tcgen05.st, w o X and H in shared memory), read the
+// accumulators back with tcgen05.ld and form y in a shared-memory tile: z
+// arrives there by TMA while the chunk's operands are built, each thread
+// overwrites its own z elements with y, and the control warp stores the tile
+// by TMA.  The chunks are software-pipelined so that the tensor cores run
+// while the threads compute: Yd(c) = M X and G, Yoff of chunk c+1 run while
+// the compute warps weight chunk c+1's x, and S of chunk c+1 while they form
+// chunk c's output.  Only the lower triangle of M (s <= t) is computed; its
+// upper blocks are written as zeros.  Shared-memory operands are the
 // 128-byte-swizzled K-major or MN-major tiles of the UMMA descriptors; every
 // wait is bounded.
 #pragma once
