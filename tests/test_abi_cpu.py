@@ -196,6 +196,7 @@ def test_bwd_argument_errors(lib):
     # 16 tiles would leave a partial fourth wave; b8 d2048 L4096 keeps 16.
     assert lib.ssm_scan_bwd_workspace_size(2, 1536, 16, 2048, 1, 1) == 13 * 2 * 1536 * 16 * 3 * 4
     assert lib.ssm_scan_bwd_workspace_size(8, 2048, 16, 4096, 1, 1) == 32 * 8 * 2048 * 16 * 3 * 4
+    assert lib.ssm_scan_bwd_workspace_size(2, 1440, 16, 520, 1, 1) == 4 * 2 * 1440 * 16 * 3 * 4  # 17 tiles
     assert bwd(batch=0, u=None, dy=None, du=None, dd=None, dA=None, dB=None, dC=None) == 0  # empty problem
 
 

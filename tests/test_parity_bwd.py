@@ -1,7 +1,7 @@
 """GPU parity of the backward pass (ssm_scan_bwd) against the fp64 oracle's
 backward, on the same seeded inputs (bf16 inputs are widened exactly).
 
-Sizes span several time chunks (128 steps, 64 at N = 64) with a ragged last
+Sizes span several time chunks (128 to 160 steps, 64 at N = 64) with a ragged last
 tile, channel blocks that end inside a group, two groups, and every optional
 input present or absent; the benchmark's b2 d1536 N16 L2048 bf16 shape is
 compared in full.
@@ -111,6 +111,18 @@ def test_bwd_full_size_bf16_b2_d1536_l2048(ssm):
                         with_h0=False, with_dhf=False, recipe=w["recipe"])
     errs = check(got, ref, "bf16", "b2 d1536 L2048")
     print("full-size bwd rel_l2:", {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_chunk_length_between_the_defaults(ssm, io):
+    """The chunk length is chosen per shape to fill whole waves of the main
+    pass: b2 d1440 N16 L520 takes 17 tiles of 8 steps (four chunks of 136,
+    136, 136 and 112 steps), a length the other cases never meet."""
+    need = ssm.bwd_workspace_size(2, 1440, 16, 520, 1, torch.bfloat16 if io == "bf16" else torch.float32)
+    assert need == 4 * 2 * 1440 * 16 * 3 * 4
+    got, ref = run_case(ssm, 2, 1440, 16, 520, 1, io, seed=23)
+    errs = check(got, ref, io, f"b2 d1440 L520 {io}")
+    print("chunk-length case rel_l2:", {k: f"{v:.2e}" for k, v in errs.items()})
 
 
 def test_bwd_matches_finite_difference_of_the_kernel(ssm):
