@@ -395,8 +395,9 @@ ssm_status_t ssm_causal_conv1d_update(void *conv_state, const void *x, const flo
  *   ddt_bias   : [dim] fp32; required when dt_bias is given, may be NULL otherwise
  *   dh0        : [batch, dim, dstate] fp32, or NULL (not wanted)
  * workspace: device memory of at least ssm_scan_bwd_workspace_size() bytes
- *   (the chunk summaries; 12 * dstate bytes per channel and chunk of 128 steps,
- *   64 at dstate 64); may be NULL when that size is 0.
+ *   (the chunk summaries; 12 * dstate bytes per channel and time chunk: 128 to
+ *   160 steps, chosen from the arguments, or 64 from dstate 64 on); may be NULL
+ *   when that size is 0.
  * The sums over channels and time are accumulated with fp32 atomic adds, so
  * dA, dB, dC, dDskip and ddt_bias may differ in the last bits between runs.
  * Errors: SSM_ERR_INVALID_ARG (bad size, missing required pointer, an output
@@ -431,8 +432,10 @@ ssm_status_t ssm_scan_bwd(const void *u, const void *delta, const void *z, const
  *   A          : [nheads] fp32 (required); Dskip, dt_bias : [nheads] fp32 or NULL (0)
  *   B, C       : [batch, ngroups, dstate, seqlen] bf16
  *   h0, h_final: [batch, nheads * headdim, dstate] fp32, or NULL (zeros / not wanted)
- * Supported: io = SSM_BF16, headdim = 64, dstate = 128, seqlen a multiple of
- * 8 (16-byte rows); anything else returns SSM_ERR_UNSUPPORTED.  All pointers
+ * Supported: io = SSM_BF16, headdim = 64, dstate = 16, 32, 64 or 128 (the
+ * smaller sizes run on the 128-state tiles with zero rows: the same time as
+ * 128), seqlen a multiple of 8 (16-byte rows); anything else returns
+ * SSM_ERR_UNSUPPORTED.  All pointers
  * 16-byte aligned (SSM_ERR_MISALIGNED); outputs must not alias inputs.  The
  * contractions take bf16 operands (the chunk's decayed mixer and the carried
  * state are rounded to bf16 for them) and accumulate in fp32; the carried

@@ -44,6 +44,20 @@ bool encode_rows(CUtensorMap* m, const void* ptr, long long rows, int seqlen, in
                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [planes, dstate, L] bf16 view of B or C, box = 64 steps x the tile's N rows
+// x 1 plane, 128-byte swizzle: rows past dstate are filled with zeros.
+bool encode_bc_planes(CUtensorMap* m, const void* ptr, long long planes, int dstate, int seqlen) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(seqlen), static_cast<cuuint64_t>(dstate),
+                                static_cast<cuuint64_t>(planes)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(seqlen) * 2,
+                                   static_cast<cuuint64_t>(seqlen) * 2 * static_cast<cuuint64_t>(dstate)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(ssm::ssd::N), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode_tiled_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 __global__ void ssd_copy_state_kernel(const float* h0, float* h_final, long long n) {
@@ -61,7 +75,8 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
         return SSM_ERR_INVALID_ARG;
     if (nheads % ngroups != 0) return SSM_ERR_INVALID_ARG;
     if (io != SSM_BF16) return SSM_ERR_UNSUPPORTED;
-    if (headdim != ssm::ssd::P || dstate != ssm::ssd::N) return SSM_ERR_UNSUPPORTED;
+    if (headdim != ssm::ssd::P) return SSM_ERR_UNSUPPORTED;
+    if (dstate != 16 && dstate != 32 && dstate != 64 && dstate != ssm::ssd::N) return SSM_ERR_UNSUPPORTED;
     if ((static_cast<long long>(seqlen) * 2) % 16 != 0) return SSM_ERR_UNSUPPORTED;
     if (batch == 0) return SSM_OK;
     if (!A) return SSM_ERR_INVALID_ARG;
@@ -86,14 +101,15 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
     const bool ok = encode_rows(&mx, x, batch * dim, seqlen, ssm::ssd::P) &&
                     encode_rows(&mz, z ? z : x, batch * dim, seqlen, ssm::ssd::P) &&
                     encode_rows(&my, y, batch * dim, seqlen, ssm::ssd::P) &&
-                    encode_rows(&mb, B, static_cast<long long>(batch) * ngroups * dstate, seqlen, ssm::ssd::N) &&
-                    encode_rows(&mc, C, static_cast<long long>(batch) * ngroups * dstate, seqlen, ssm::ssd::N);
+                    encode_bc_planes(&mb, B, static_cast<long long>(batch) * ngroups, dstate, seqlen) &&
+                    encode_bc_planes(&mc, C, static_cast<long long>(batch) * ngroups, dstate, seqlen);
     if (!ok) return SSM_ERR_CUDA;
     ssm::SsdParams p{};
     p.delta = static_cast<const __nv_bfloat16*>(delta);
     p.A = A; p.D = Dskip; p.dt_bias = dt_bias; p.h0 = h0; p.h_final = h_final;
     p.y = static_cast<__nv_bfloat16*>(y); p.z = static_cast<const __nv_bfloat16*>(z); p.status = nullptr;
-    p.batch = batch; p.nheads = nheads; p.seqlen = seqlen; p.ngroups = ngroups; p.has_z = z != nullptr;
+    p.batch = batch; p.nheads = nheads; p.seqlen = seqlen; p.ngroups = ngroups; p.dstate = dstate;
+    p.has_z = z != nullptr;
 
     static std::atomic<unsigned long long> done{0};
     int dev = 0;

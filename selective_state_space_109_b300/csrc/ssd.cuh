@@ -15,6 +15,11 @@
 //   H      = exp(cs_end) H_prev + S                  the state carried out
 //   y      = (Ydiag + Yoff + Dskip x) * silu(z)
 //
+// State sizes below N = 128 run on the same tiles: the B and C tiles load
+// through 3-D maps whose rows past the caller's state size are filled with
+// zeros, so G, Yoff and S gain only zero terms and the padded state rows stay
+// zero (h0 and h_final touch only the caller's rows).
+//
 // One CTA walks one (sequence, head) through its chunks in order, so the state
 // H stays on chip (fp32 in registers, a 16-channel slice of a state row per
 // thread; a bf16 copy in shared memory feeds the next chunk's Yoff).  A
@@ -55,12 +60,13 @@ struct SsdParams {
     const float* A;              // [nheads]
     const float* D;              // [nheads] or null
     const float* dt_bias;        // [nheads] or null
-    const float* h0;             // [batch, nheads * P, N] or null
-    float* h_final;              // [batch, nheads * P, N] or null
+    const float* h0;             // [batch, nheads * P, dstate] or null
+    float* h_final;              // [batch, nheads * P, dstate] or null
     const __nv_bfloat16* z;      // [batch, nheads * P, L] or null
     __nv_bfloat16* y;            // [batch, nheads * P, L]
     unsigned int* status;        // null (device error word only)
     int batch, nheads, seqlen, ngroups;
+    int dstate;                  // the caller's state size, at most N: the tiles' rows past it load as zeros
     int has_z;
 };
 
@@ -287,7 +293,8 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const float dsk = p.D ? __ldg(p.D + h) : 0.f;
     const long long dim = static_cast<long long>(p.nheads) * P;
     const int xrow = bh * P;                    // first row of the head in the x/z/y maps
-    const int bcrow = (b * p.ngroups + g) * N;  // first row of the group in the B/C maps
+    const int bcg = b * p.ngroups + g;          // the (sequence, group) plane of the B/C maps
+    const int NS = p.dstate;                    // state rows in memory (rows NS..N-1 of the tiles are zero)
     constexpr int PC = P / CG;                  // channels per column group (16)
 
     // TMA loads: C and B of chunk c (one phase per chunk), x of chunk c into
@@ -296,8 +303,8 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         mbar_arrive_expect_tx(bc_bar, TX_BC);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            tma_load_2d(Cs + half * HALF_C, &tm_C, c * Q + half * 64, bcrow, bc_bar);
-            tma_load_2d(Bs + half * HALF_C, &tm_B, c * Q + half * 64, bcrow, bc_bar);
+            tma_load_3d(Cs + half * HALF_C, &tm_C, c * Q + half * 64, 0, bcg, bc_bar);
+            tma_load_3d(Bs + half * HALF_C, &tm_B, c * Q + half * 64, 0, bcg, bc_bar);
         }
     };
     auto load_x = [&](int c) {
@@ -355,9 +362,9 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
     };
     if (compute) {
-        const float* h0 = p.h0 ? p.h0 + (static_cast<long long>(b) * dim + static_cast<long long>(h) * P) * N : nullptr;
+        const float* h0 = p.h0 ? p.h0 + (static_cast<long long>(b) * dim + static_cast<long long>(h) * P) * NS : nullptr;
 #pragma unroll
-        for (int i = 0; i < PC; ++i) H[i] = h0 ? __ldg(h0 + static_cast<long long>(cg * PC + i) * N + r) : 0.f;
+        for (int i = 0; i < PC; ++i) H[i] = h0 && r < NS ? __ldg(h0 + static_cast<long long>(cg * PC + i) * NS + r) : 0.f;
         store_hs();
     }
 
@@ -623,10 +630,10 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
     }
     if (tid == CTRL) bulk_wait<0>();
-    if (p.h_final && compute) {
-        float* hf = p.h_final + (static_cast<long long>(b) * dim + static_cast<long long>(h) * P) * N;
+    if (p.h_final && compute && r < NS) {
+        float* hf = p.h_final + (static_cast<long long>(b) * dim + static_cast<long long>(h) * P) * NS;
 #pragma unroll
-        for (int i = 0; i < PC; ++i) hf[static_cast<long long>(cg * PC + i) * N + r] = H[i];
+        for (int i = 0; i < PC; ++i) hf[static_cast<long long>(cg * PC + i) * NS + r] = H[i];
     }
     if (warp == 0) {
         tc_fence_after();

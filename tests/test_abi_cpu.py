@@ -208,7 +208,8 @@ def ssd(lib, x=P, delta=P, z=None, A=P, B=P, C=P, D=None, bias=None, h0=None, y=
 def test_ssd_argument_checks(lib):
     assert ssd(lib, io=0) == 2            # fp32 I/O: the tensor-core path is bf16 only
     assert ssd(lib, P_=32) == 2           # head dimension other than 64
-    assert ssd(lib, N=64) == 2            # state size other than 128
+    assert ssd(lib, N=256) == 2           # state size above the 128-state tiles
+    assert ssd(lib, N=48) == 2            # state size other than 16, 32, 64, 128
     assert ssd(lib, L=12) == 2            # rows not whole 16-byte packets
     assert ssd(lib, nheads=3, G=2) == 1   # heads do not split into the groups
     assert ssd(lib, nheads=0) == 1

@@ -52,6 +52,22 @@ def test_ssd_matches_oracle(ssm, batch, nheads, L, G, with_z, with_h0):
     assert ssm.device_status() == 0
 
 
+@pytest.mark.parametrize("N", [16, 32, 64])
+def test_ssd_smaller_state_sizes(ssm, N):
+    """State sizes below 128 run on the 128-state tiles, the rows past N
+    loaded as zeros: several chunks, a ragged last one, two groups, an
+    initial state and its final state."""
+    x = I.make_ssd_inputs(2, 4, 64, N, 392, 2, seed=70 + N, device="cuda", with_h0=True)
+    y, hf = run(ssm, x)
+    torch.cuda.synchronize()
+    ry, rh = ref(x)
+    e, eh = rel_l2(to_np(y), ry), rel_l2(to_np(hf), rh)
+    print(f"N={N}: y rel_l2 {e:.2e}, h_final rel_l2 {eh:.2e}")
+    assert e <= BF16_REL_L2, f"y rel_l2 {e:.3e}"
+    assert eh <= STATE_REL_L2, f"h_final rel_l2 {eh:.3e}"
+    assert ssm.device_status() == 0
+
+
 def test_ssd_empty_sequence_copies_h0(ssm):
     x = I.make_ssd_inputs(1, 2, 64, 128, 0, seed=90, device="cuda", with_h0=True)
     y, hf = run(ssm, x)
