@@ -1,0 +1,86 @@
+"""Tensors past 2^31 elements on the GPU: every offset into them must be
+64-bit.  The chunked scan runs on activations of 2^31 + 2^21 elements (bf16,
+4.3 GB each) and the decode step on a state of 2^31 + 2^20 fp32 elements
+(8.6 GB); sampled channels -- at the start, in the middle and at the end,
+whose elements lie beyond 2^31 -- are compared with the oracle.  The oracle
+sees only the sampled rows (sliced on the device, then widened exactly), so
+host memory stays small."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import rel_l2, to_np
+from selective_state_space_109_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+BF16_REL_L2 = 5e-3
+STATE_REL_L2 = 1e-4
+
+
+@pytest.fixture(scope="module")
+def ssm():
+    from selective_state_space_109_b300 import ssm as m
+    return m
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float32).double().numpy()
+
+
+def test_scan_past_2_31_elements(ssm, monkeypatch):
+    """The plan the library picks for this shape (one pass), then a forced
+    split into four time chunks (summary, carry and fused passes)."""
+    batch, dim, N, L = 1, 16400, 16, 131072
+    assert batch * dim * L > 2 ** 31
+    x = I.make_scan_inputs(batch, dim, N, L, 1, io="bf16", recipe="scaled", seed=41, device="cuda")
+    channels = [0, dim // 2, dim - 17, dim - 1]
+    assert (dim - 1) * L > 2 ** 31  # the last channel's first element
+    B, C = f64(x.B), f64(x.C)
+    A, D, bias = f64(x.A), f64(x.D), f64(x.dt_bias)
+    refs = {}
+    for d in channels:
+        sl = slice(d, d + 1)
+        refs[d] = oracle.scan(f64(x.u[:, sl]), f64(x.delta[:, sl]), A[sl], B, C, z=f64(x.z[:, sl]),
+                              Dskip=D[sl], dt_bias=bias[sl], return_final_state=True)
+    for chunks in (None, 4):
+        if chunks is not None:
+            monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
+            assert ssm.scan_plan(batch, dim, N, L, 1, torch.bfloat16)["chunks"] == chunks
+        y, hf = ssm.scan_fwd_chunked(x.u, x.delta, x.A, x.B, x.C, z=x.z, D=x.D, dt_bias=x.dt_bias)
+        torch.cuda.synchronize()
+        assert ssm.device_status() == 0
+        for d in channels:
+            sl = slice(d, d + 1)
+            ry, rh = refs[d]
+            e = rel_l2(f64(y[:, sl]), ry)
+            eh = rel_l2(f64(hf[:, sl]), rh)
+            assert e <= BF16_REL_L2, f"chunks={chunks} channel {d}: y rel_l2 {e:.3e}"
+            assert eh <= STATE_REL_L2, f"chunks={chunks} channel {d}: h_final rel_l2 {eh:.3e}"
+        del y, hf
+
+
+def test_decode_step_past_2_31_state_elements(ssm):
+    batch, dim, N = 2049, 65536, 16
+    assert batch * dim * N > 2 ** 31
+    state = I.make_decode_state(batch, dim, N, seed=43, device="cuda")
+    tok = I.make_decode_token(batch, dim, N, step=0, io="bf16", recipe="scaled", seed=43, device="cuda")
+    prm = I.decode_params(dim, N, recipe="scaled", seed=43, device="cuda")
+    A, D, bias = prm["A"], prm["D"], prm["dt_bias"]
+    rows = [(0, 0), (batch // 2, dim // 2), (batch - 1, dim - 3), (batch - 1, dim - 1)]
+    before = {r: f64(state[r[0], r[1]]) for r in rows}
+    y = ssm.state_update(state, tok["u"], tok["delta"], A, tok["B"], tok["C"], z=tok["z"], D=D, dt_bias=bias)
+    torch.cuda.synchronize()
+    assert ssm.device_status() == 0
+    An, Dn, bn = f64(A), f64(D), f64(bias)
+    for b, d in rows:
+        st = before[(b, d)].reshape(1, 1, N)
+        rs, ry = oracle.state_update(st, f64(tok["u"][b:b + 1, d:d + 1]), f64(tok["delta"][b:b + 1, d:d + 1]),
+                                     An[d:d + 1], f64(tok["B"][b:b + 1]), f64(tok["C"][b:b + 1]),
+                                     z=f64(tok["z"][b:b + 1, d:d + 1]), Dskip=Dn[d:d + 1],
+                                     dt_bias=bn[d:d + 1])
+        es = rel_l2(f64(state[b, d]).reshape(1, 1, N), rs)
+        assert es <= STATE_REL_L2, f"row {(b, d)}: state rel_l2 {es:.3e}"
+        gy, ryv = float(f64(y[b, d])), float(ry[0, 0])
+        assert abs(gy - ryv) <= 1e-2 * max(abs(ryv), 1e-2), f"row {(b, d)}: y {gy} against {ryv}"
