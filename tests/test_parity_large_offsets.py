@@ -1,8 +1,10 @@
 """Tensors past 2^31 elements on the GPU: every offset into them must be
-64-bit.  The chunked scan runs on activations of 2^31 + 2^21 elements (bf16,
-4.3 GB each) and the decode step on a state of 2^31 + 2^20 fp32 elements
-(8.6 GB); sampled channels -- at the start, in the middle and at the end,
-whose elements lie beyond 2^31 -- are compared with the oracle.  The oracle
+64-bit.  The scan and the backward pass run on activations of 2^31 + 2^21
+elements (bf16, 4.3 GB each) and the decode step on a state of 2^31 + 2^20
+fp32 elements (8.6 GB); sampled channels -- at the start, in the middle and
+at the end, whose elements lie beyond 2^31 -- are compared with the oracle
+(for the backward pass, every per-channel gradient; dB and dC sum over all
+channels and are checked on the smaller shapes of the backward tests).  The oracle
 sees only the sampled rows (sliced on the device, then widened exactly), so
 host memory stays small."""
 import numpy as np
@@ -84,3 +86,25 @@ def test_decode_step_past_2_31_state_elements(ssm):
         assert es <= STATE_REL_L2, f"row {(b, d)}: state rel_l2 {es:.3e}"
         gy, ryv = float(f64(y[b, d])), float(ry[0, 0])
         assert abs(gy - ryv) <= 1e-2 * max(abs(ryv), 1e-2), f"row {(b, d)}: y {gy} against {ryv}"
+
+
+def test_backward_past_2_31_elements(ssm):
+    batch, dim, N, L = 1, 16400, 16, 131072
+    x = I.make_scan_inputs(batch, dim, N, L, 1, io="bf16", recipe="scaled", seed=47, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(4700)
+    dy = torch.randn((batch, dim, L), generator=g, device="cuda").to(torch.bfloat16)
+    got = ssm.scan_bwd(x.u, x.delta, x.A, x.B, x.C, dy, z=x.z, D=x.D, dt_bias=x.dt_bias)
+    torch.cuda.synchronize()
+    assert ssm.device_status() == 0
+    B, C = f64(x.B), f64(x.C)
+    A, D, bias = f64(x.A), f64(x.D), f64(x.dt_bias)
+    for d in [0, dim // 2, dim - 17, dim - 1]:
+        sl = slice(d, d + 1)
+        ref = oracle.scan_bwd(f64(x.u[:, sl]), f64(x.delta[:, sl]), A[sl], B, C, f64(dy[:, sl]),
+                              z=f64(x.z[:, sl]), Dskip=D[sl], dt_bias=bias[sl])
+        for k in ("du", "ddelta", "dz"):
+            e = rel_l2(f64(got[k][:, sl]), ref[k])
+            assert e <= BF16_REL_L2, f"channel {d}: {k} rel_l2 {e:.3e}"
+        for k, tol in (("dA", 1e-3), ("dD", 1e-3), ("ddt_bias", 1e-3), ("dh0", 1e-3)):
+            e = rel_l2(f64(got[k][sl] if got[k].dim() < 3 else got[k][:, sl]), ref[k])
+            assert e <= tol, f"channel {d}: {k} rel_l2 {e:.3e}"
