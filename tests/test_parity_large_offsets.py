@@ -1,6 +1,6 @@
 """Tensors past 2^31 elements on the GPU: every offset into them must be
-64-bit.  The scan and the backward pass run on activations of 2^31 + 2^21
-elements (bf16, 4.3 GB each) and the decode step on a state of 2^31 + 2^20
+64-bit.  The scan, the backward pass and the SSD layer run on activations of
+more than 2^31 elements (bf16, 4.3 GB each) and the decode step on a state of 2^31 + 2^20
 fp32 elements (8.6 GB); sampled channels -- at the start, in the middle and
 at the end, whose elements lie beyond 2^31 -- are compared with the oracle
 (for the backward pass, every per-channel gradient; dB and dC sum over all
@@ -108,3 +108,24 @@ def test_backward_past_2_31_elements(ssm):
         for k, tol in (("dA", 1e-3), ("dD", 1e-3), ("ddt_bias", 1e-3), ("dh0", 1e-3)):
             e = rel_l2(f64(got[k][sl] if got[k].dim() < 3 else got[k][:, sl]), ref[k])
             assert e <= tol, f"channel {d}: {k} rel_l2 {e:.3e}"
+
+
+def test_ssd_past_2_31_elements(ssm):
+    batch, nheads, P, N, L = 2, 64, 64, 128, 270336
+    assert batch * nheads * P * L > 2 ** 31
+    x = I.make_ssd_inputs(batch, nheads, P, N, L, 1, seed=49, device="cuda", with_h0=True)
+    y, hf = ssm.ssd_fwd(x["x"], x["delta"], x["A"], x["B"], x["C"], z=x["z"], D=x["D"], dt_bias=x["dt_bias"],
+                        h0=x["h0"], headdim=P, return_final_state=True)
+    torch.cuda.synchronize()
+    assert ssm.device_status() == 0
+    A, D, bias = f64(x["A"]), f64(x["D"]), f64(x["dt_bias"])
+    for b, h in [(0, 0), (1, nheads // 2), (1, nheads - 1)]:
+        ch = slice(h * P, (h + 1) * P)
+        ry, rh = oracle.ssd(f64(x["x"][b:b + 1, ch]), f64(x["delta"][b:b + 1, h:h + 1]), A[h:h + 1],
+                            f64(x["B"][b:b + 1]), f64(x["C"][b:b + 1]), z=f64(x["z"][b:b + 1, ch]),
+                            Dskip=D[h:h + 1], dt_bias=bias[h:h + 1], h0=f64(x["h0"][b:b + 1, ch]),
+                            headdim=P, return_final_state=True)
+        e = rel_l2(f64(y[b:b + 1, ch]), ry)
+        eh = rel_l2(f64(hf[b:b + 1, ch]), rh)
+        assert e <= BF16_REL_L2, f"(b, h) = {(b, h)}: y rel_l2 {e:.3e}"
+        assert eh <= STATE_REL_L2, f"(b, h) = {(b, h)}: h_final rel_l2 {eh:.3e}"
