@@ -1,6 +1,6 @@
 """Tensors past 2^31 elements on the GPU: every offset into them must be
-64-bit.  The scan, the backward pass and the SSD layer run on activations of
-more than 2^31 elements (bf16, 4.3 GB each) and the decode step on a state of 2^31 + 2^20
+64-bit.  The scan, the packed scan, the short convolution, the backward
+pass and the SSD layer run on activations of more than 2^31 elements (bf16, 4.3 GB each) and the decode step on a state of 2^31 + 2^20
 fp32 elements (8.6 GB); sampled channels -- at the start, in the middle and
 at the end, whose elements lie beyond 2^31 -- are compared with the oracle
 (for the backward pass, every per-channel gradient; dB and dC sum over all
@@ -129,3 +129,47 @@ def test_ssd_past_2_31_elements(ssm):
         eh = rel_l2(f64(hf[b:b + 1, ch]), rh)
         assert e <= BF16_REL_L2, f"(b, h) = {(b, h)}: y rel_l2 {e:.3e}"
         assert eh <= STATE_REL_L2, f"(b, h) = {(b, h)}: h_final rel_l2 {eh:.3e}"
+
+
+def _randn_cuda(shape, seed, dtype=torch.bfloat16, scale=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.randn(shape, generator=g, device="cuda") * scale).to(dtype)
+
+
+def test_conv1d_past_2_31_elements(ssm):
+    batch, dim, L, W = 1, 16400, 131072, 4
+    x = _randn_cuda((batch, dim, L), 51)
+    w = _randn_cuda((dim, W), 52, torch.float32, W ** -0.5)
+    bias = _randn_cuda((dim,), 53, torch.float32, 0.1)
+    out = ssm.causal_conv1d(x, w, bias)
+    torch.cuda.synchronize()
+    for d in [0, dim // 2, dim - 17, dim - 1]:
+        sl = slice(d, d + 1)
+        ref = oracle.causal_conv1d(f64(x[:, sl]), f64(w[sl]), f64(bias[sl]))
+        e = rel_l2(f64(out[:, sl]), ref)
+        assert e <= BF16_REL_L2, f"channel {d}: rel_l2 {e:.3e}"
+
+
+def test_packed_scan_past_2_31_elements(ssm):
+    dim, N = 16384, 16
+    lengths = [16385] * 8                     # T = 131080 steps: dim * T > 2^31
+    T = sum(lengths)
+    assert dim * T > 2 ** 31
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32, device="cuda")
+    u, delta, z = (_randn_cuda((dim, T), s) for s in (61, 62, 63))
+    B, C = (_randn_cuda((1, N, T), s, scale=N ** -0.5) for s in (64, 65))
+    A = I.a_values(dim, N, "cuda")
+    D = 1.0 + 0.1 * _randn_cuda((dim,), 66, torch.float32)
+    bias = I.dt_bias_values(dim, 67, "cuda")
+    y, hf = ssm.scan_fwd_varlen(u, delta, A, B, C, cu, z=z, D=D, dt_bias=bias, return_final_state=True)
+    torch.cuda.synchronize()
+    assert ssm.device_status() == 0
+    cun = cu.cpu().numpy()
+    for d in [0, dim // 2, dim - 17, dim - 1]:
+        sl = slice(d, d + 1)
+        ry, rh = oracle.scan_varlen(f64(u[sl]), f64(delta[sl]), f64(A[sl]), f64(B), f64(C), cun,
+                                    z=f64(z[sl]), Dskip=f64(D[sl]), dt_bias=f64(bias[sl]), return_final_state=True)
+        e = rel_l2(f64(y[sl]), ry)
+        eh = rel_l2(f64(hf[:, sl]), rh)
+        assert e <= BF16_REL_L2, f"channel {d}: y rel_l2 {e:.3e}"
+        assert eh <= STATE_REL_L2, f"channel {d}: h_final rel_l2 {eh:.3e}"
