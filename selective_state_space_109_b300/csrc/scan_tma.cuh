@@ -554,8 +554,9 @@ scan_tma_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 // and state it turns the chunk summaries (P_c, E_c), c = 0..nchunks-2, into
 // the state entering each chunk, h_{c+1} = P_c * h_c + E_c from h_0 = h0 (or
 // zero), and stores h_{c+1} over E_c.  One thread per (channel, state pair)
-// issues every load before the short dependent chain of FMAs, so the chain
-// costs one memory latency instead of one per chunk.
+// issues the loads of sixteen summaries before their short dependent chain
+// of FMAs, so the chain costs one memory latency per sixteen chunks instead
+// of one per chunk (and no register array grows with the chunk cap).
 template <int N, int MAXC>
 __global__ void __launch_bounds__(256)
 scan_carry_kernel(float* __restrict__ agg, const float* __restrict__ h0, long long BD, int nchunks) {
@@ -566,21 +567,27 @@ scan_carry_kernel(float* __restrict__ agg, const float* __restrict__ h0, long lo
     if (i >= BD * NP) return;
     const long long bd = i / NP;
     const int k = static_cast<int>(i % NP);
-    float2 Pc[MAXC - 1], Ec[MAXC - 1];
-#pragma unroll
-    for (int c = 0; c < MAXC - 1; ++c) {
-        if (c < nchunks - 1) {
-            const float2* a = reinterpret_cast<const float2*>(agg + (c * BD + bd) * (2 * N));
-            Pc[c] = __ldcg(a + k);
-            Ec[c] = __ldcg(a + NP + k);
-        }
-    }
+    static_assert(MAXC >= 2, "at least two chunks");
+    const int nc = nchunks - 1;
     float2 h = h0 ? __ldg(reinterpret_cast<const float2*>(h0 + bd * N) + k) : make_float2(0.f, 0.f);
+    // Blocks of G summaries: all loads of a block in flight before its chain.
+    constexpr int G = MAXC - 1 < 16 ? MAXC - 1 : 16;
+    for (int c0 = 0; c0 < nc; c0 += G) {
+        float2 Pc[G], Ec[G];
 #pragma unroll
-    for (int c = 0; c < MAXC - 1; ++c) {
-        if (c < nchunks - 1) {
-            h = __ffma2_rn(Pc[c], h, Ec[c]);
-            reinterpret_cast<float2*>(agg + (c * BD + bd) * (2 * N))[NP + k] = h;
+        for (int q = 0; q < G; ++q) {
+            if (c0 + q < nc) {
+                const float2* a = reinterpret_cast<const float2*>(agg + ((c0 + q) * BD + bd) * (2 * N));
+                Pc[q] = __ldcg(a + k);
+                Ec[q] = __ldcg(a + NP + k);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < G; ++q) {
+            if (c0 + q < nc) {
+                h = __ffma2_rn(Pc[q], h, Ec[q]);
+                reinterpret_cast<float2*>(agg + ((c0 + q) * BD + bd) * (2 * N))[NP + k] = h;
+            }
         }
     }
 }

@@ -194,7 +194,7 @@ constexpr int kTmaWarps = 4;
 // The time-chunk plan aims to fill a B300 (148 SMs).  It is a function of the
 // problem's arguments only, so the workspace size query needs no device.
 constexpr int kPlanSms = 148;
-constexpr int kMaxChunks = 32;
+constexpr int kMaxChunks = 64;
 
 // Workspace header: the device-side status word written by kernels that wait.
 constexpr size_t kWorkspaceHeader = 256;

@@ -15,9 +15,9 @@ def ssm():
 
 
 @pytest.mark.parametrize("shape,lanes,chunks", [
-    ((2, 1536, 16, 2048), 2, 12),     # the headline call
+    ((2, 1536, 16, 2048), 2, 12),
     ((8, 2048, 16, 4096), 2, 1),
-    ((1, 5120, 16, 65536), 1, 29),
+    ((1, 5120, 16, 65536), 1, 59),    # the headline call: 2182 us against 2225 us at 29 chunks
     ((2, 1536, 32, 2048), 2, 12),
     ((2, 1536, 64, 2048), 4, 6),
     ((2, 1536, 128, 2048), 8, 1),
@@ -39,9 +39,9 @@ def test_plan_rules(ssm):
     assert ssm.scan_plan(2, 1536, 16, 2048, 1, torch.bfloat16, chunked=False)["chunks"] == 1
     # rows that are not whole 16-byte packets take the generic kernel
     assert not ssm.scan_plan(2, 64, 16, 2047, 1, torch.bfloat16)["staged"]
-    # the chunk count never exceeds 32 nor the tiles of the sequence
+    # the chunk count never exceeds 64 nor the tiles of the sequence
     assert ssm.scan_plan(1, 16, 16, 64, 1, torch.bfloat16)["chunks"] <= 4
-    assert ssm.scan_plan(1, 64, 16, 1 << 20, 1, torch.float32)["chunks"] <= 32
+    assert ssm.scan_plan(1, 64, 16, 1 << 20, 1, torch.float32)["chunks"] <= 64
     # N = 128 on rows that are not whole 16-byte packets: the register-staged kernel
     p128 = ssm.scan_plan(1, 64, 128, 2047, 1, torch.bfloat16)
     assert not p128["staged"] and p128["chunks"] == 1 and p128["kernels"] == 1
