@@ -610,7 +610,7 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int i = 0; i < PC; ++i) {
                 const uint32_t off = half * HALF_X + sw128_elem(cg * PC + i, tc);
                 float yv = fmaf(dsk, xv[i], fmaf(e_t, yo[i], yd[i]));
-                if (has_z) yv *= silu<false>(bf_at(Zs, off));
+                if (has_z) yv *= silu_tanh(bf_at(Zs, off));
                 bf_put(Zs, off, yv);
             }
             fence_proxy_async_smem();

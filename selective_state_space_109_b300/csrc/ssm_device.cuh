@@ -36,6 +36,12 @@ __device__ __forceinline__ float rcp_approx(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// MUFU.TANH (approximate: relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // e^x to about 1 ulp on the FMA pipe (used where the I/O type is fp32):
 // Cody & Waite's argument reduction x = k ln2 + r with |r| <= ln2/2 (ln2 split
@@ -106,9 +112,19 @@ __device__ __forceinline__ float silu(float z) {
     }
 }
 
-// Two-lane (fp32x2) forms of the fast softplus and silu above, for two steps
-// at once: the same operations element by element, issued as packed FMA-pipe
-// instructions where the operation has a packed form.
+// silu through the identity z sigmoid(z) = h + h tanh(h), h = z / 2: one
+// MUFU operation instead of an exponential and a reciprocal.  Its relative
+// error (about 2^-11) is below the bf16 rounding of the outputs it gates; the
+// scan's fused passes and the SSD output use it for bf16 I/O, whose outputs
+// are held to the bf16 rel-L2 tolerance.
+__device__ __forceinline__ float silu_tanh(float z) {
+    const float h = 0.5f * z;
+    return fmaf(h, tanh_approx(h), h);
+}
+
+// Two-lane (fp32x2) forms of the fast softplus and of silu_tanh above, for
+// two steps at once: the same operations element by element, issued as packed
+// FMA-pipe instructions where the operation has a packed form.
 __device__ __forceinline__ float2 softplus2_fast(float2 v) {
     const float w0 = ex2_approx(fabsf(v.x) * -kLog2e);
     const float w1 = ex2_approx(fabsf(v.y) * -kLog2e);
@@ -125,9 +141,8 @@ __device__ __forceinline__ float2 softplus2_fast(float2 v) {
 }
 
 __device__ __forceinline__ float2 silu2_fast(float2 z) {
-    const float2 x = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
-    const float2 d = __fadd2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), make_float2(1.f, 1.f));
-    return __fmul2_rn(z, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+    const float2 h = __fmul2_rn(z, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
 }
 
 // ---------------------------------------------------------------------------
