@@ -49,6 +49,9 @@ FALLBACK_HBM_GBS = 6400.0
 # ssm_probe_alu_rates (nominal B300 rates: 32 ex2 and 128 FMA per SM per
 # clock, i.e. 32 updates per SM per clock from either pipe).
 NOMINAL_UPDATES_PER_SM_CLK = 32.0
+# Nominal HBM3e bandwidth the scan's memory target is stated against (the
+# measured copy bandwidth of the peaks file is the roofline's denominator).
+NOMINAL_HBM_GBS = 8000.0
 
 
 # ---------------------------------------------------------------------------
@@ -804,7 +807,9 @@ def run_ours(args):
                                             "all chunks but the last"}},
         "hbm_roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "peak_source": peak_src, "traffic": traffic},
+                         "peak_source": peak_src, "traffic": traffic,
+                         "nominal_peak": NOMINAL_HBM_GBS,
+                         "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": args.steps * r["plan"]["kernels"],
@@ -815,6 +820,7 @@ def run_ours(args):
                          "us_per_step": round(dec["cold"]["us_per_step"], 3),
                          "state_GBps": round(dec["cold"]["state_gbs"], 1),
                          "frac_of_hbm": round(dec["cold"]["state_gbs"] / peaks["hbm_gbs"], 4),
+                         "frac_of_nominal_hbm": round(dec["cold"]["state_gbs"] / NOMINAL_HBM_GBS, 4),
                          "warm_l2_us_per_step": round(dec["warm"]["us_per_step"], 3),
                          "warm_l2_tokens_per_s": round(dec["warm"]["tokens_per_s"], 1)}
     if extra:
