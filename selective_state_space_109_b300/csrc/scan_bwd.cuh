@@ -204,6 +204,24 @@ struct BwdShape {
     static_assert(N % S == 0 && LN >= 1 && LN <= 32, "N in {4, 8, 16, 32, 64, 128, 256}");
 };
 
+// The main pass's widened B/C entry of a state pair, (B_n, B_n+1, C_n,
+// C_n+1): fp32 for fp32 I/O; for bf16 I/O the four bf16 values as they
+// arrive (8 bytes: half the shared-memory traffic of the reads, which is a
+// co-bound of that pass), widened where they are read.
+template <typename T>
+struct BwdBcf {
+    using type = float4;
+    static __device__ __forceinline__ float4 get(const float4& v) { return v; }
+};
+template <>
+struct BwdBcf<__nv_bfloat16> {
+    using type = uint2;
+    static __device__ __forceinline__ float4 get(const uint2& v) {
+        return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    }
+};
+
 // Channel (b, d) and chunk of this thread; inactive lanes (past the group's
 // last channel) compute on a valid channel but write nothing.
 struct BwdLane {
@@ -492,7 +510,8 @@ scan_bwd_kernel(const BwdParams p) {
     T (*bc_s)[2][N][TT] = reinterpret_cast<T (*)[2][N][TT]>(smem + Lay::BC);
     float4 (*sc)[CH] = reinterpret_cast<float4 (*)[CH]>(smem + Lay::SC);
     float2 (*sc2)[CH] = reinterpret_cast<float2 (*)[CH]>(smem + Lay::SC2);
-    float4 (*bcf)[Sh::NQP] = reinterpret_cast<float4 (*)[Sh::NQP]>(smem + Lay::BCF);
+    using Bcf = BwdBcf<T>;
+    typename Bcf::type (*bcf)[Sh::NQP] = reinterpret_cast<typename Bcf::type (*)[Sh::NQP]>(smem + Lay::BCF);
     float (*red)[TT][2 * N] = reinterpret_cast<float (*)[TT][2 * N]>(smem + Lay::RED);
     float (*outs)[CH][TT + 1] = reinterpret_cast<float (*)[CH][TT + 1]>(smem + Lay::OUTS);
 
@@ -578,7 +597,7 @@ scan_bwd_kernel(const BwdParams p) {
             const int t = item % TT, n = (item / TT) % N, isC = item / (TT * N);
             const int q = n >> 1;
             const int slot = (q % P2) * LN + q / P2;
-            reinterpret_cast<float*>(&bcf[t][slot])[isC * 2 + (n & 1)] = bwd_to_f(bc_s[buf][isC][n][t]);
+            reinterpret_cast<T*>(&bcf[t][slot])[isC * 2 + (n & 1)] = bc_s[buf][isC][n][t];
         }
     };
 
@@ -603,7 +622,7 @@ scan_bwd_kernel(const BwdParams p) {
             const float4 q = sc[t][l.r];
 #pragma unroll
             for (int k = 0; k < P2; ++k) {
-                const float4 bq = bcf[t][k * LN + l.j];
+                const float4 bq = Bcf::get(bcf[t][k * LN + l.j]);
                 h[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), h[k], __fmul2_rn(f2(q.y), f2(bq.x, bq.y)));
             }
         }
@@ -649,7 +668,7 @@ scan_bwd_kernel(const BwdParams p) {
             float2 y2 = f2(0.f);
 #pragma unroll
             for (int k = 0; k < P2; ++k) {
-                const float4 bq = bcf[t][k * LN + l.j];
+                const float4 bq = Bcf::get(bcf[t][k * LN + l.j]);
                 hist[t][k] = hh[k];
                 hh[k] = __ffma2_rn(decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k])), hh[k], __fmul2_rn(f2(q.y), f2(bq.x, bq.y)));
                 y2 = __ffma2_rn(f2(bq.z, bq.w), hh[k], y2);
@@ -666,7 +685,7 @@ scan_bwd_kernel(const BwdParams p) {
             float2 sb2 = f2(0.f), sd2 = f2(0.f);
 #pragma unroll
             for (int k = 0; k < P2; ++k) {
-                const float4 bq = bcf[t][k * LN + l.j];
+                const float4 bq = Bcf::get(bcf[t][k * LN + l.j]);
                 const float2 Bv = f2(bq.x, bq.y), Cv = f2(bq.z, bq.w);
                 const float2 hcur = (t == TT - 1) ? hh[k] : hist[t + 1 < TT ? t + 1 : t][k];
                 const float2 a = decay2<ACCURATE>(__fmul2_rn(f2(q.x), a2[k]));
