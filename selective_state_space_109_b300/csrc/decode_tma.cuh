@@ -274,6 +274,11 @@ decode_ws_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
     const bool has_z = p.has_z != 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // Programmatic dependent launch: the next kernel in the stream may start
+    // its launch now (it waits in turn before touching memory), and this one
+    // waits for the previous kernel's writes before its first global access,
+    // so that launch and prologue overlap the previous step's tail.
+    grid_dep_launch();
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
@@ -283,6 +288,7 @@ decode_ws_kernel(const __grid_constant__ CUtensorMap tm_state, const __grid_cons
         fence_mbar_init();
     }
     __syncthreads();
+    grid_dep_wait();
 
     auto tile_of = [&](int k, int& b, int& cb) {
         const long long t = t_begin + k;

@@ -777,8 +777,21 @@ cudaError_t launch_decode_tma_v(float* state, const int* slots, int nslots, cons
         if (e != cudaSuccess) return e;
         const long long grid =
             std::min<long long>(p.ntiles, static_cast<long long>(device_sm_count()) * std::max(1, per_sm));
-        kern<<<static_cast<unsigned>(grid), CH + 32, WLay::SMEM_BYTES, st>>>(ms, mso, mu, md, mz, mB, mC, p);
-        return cudaGetLastError();
+        // Programmatic dependent launch: consecutive steps overlap one
+        // kernel's launch and prologue with the previous one's tail (the
+        // kernel waits for the previous writes before reading anything):
+        // 30.8-31.1 us against 31.6-31.7 us per cold step on b256 d5120.
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(CH + 32);
+        cfg.dynamicSmemBytes = WLay::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, ms, mso, mu, md, mz, mB, mC, p);
     }
     auto kern = ssm::decode_tma_kernel<T, CH, STAGES, sizeof(T) == 4>;
     static unsigned long long done = 0;
