@@ -24,6 +24,7 @@
 #include <stdint.h>
 
 #include "ssm_device.cuh"
+#include "tma.cuh"
 
 namespace ssm {
 
@@ -64,6 +65,11 @@ __device__ __forceinline__ void conv_st(T* p, long long i, float v) {
 template <typename T, int W, typename Idx>
 __global__ void __launch_bounds__(256, 5)
 conv1d_vec_kernel(const ConvParams p) {
+    // Programmatic dependent launch (when launched with it): let the next
+    // kernel begin launching, and wait for the previous kernel's writes
+    // before the first global access.
+    grid_dep_launch();
+    grid_dep_wait();
     constexpr int VPC = 16 / static_cast<int>(sizeof(T));
     constexpr int H = W - 1;  // history length
     constexpr int U = 4;      // 32-chunk groups per warp iteration
@@ -193,6 +199,8 @@ __global__ void __launch_bounds__(256)
 conv1d_update_kernel(void* conv_state, const void* xin, const float* w, const float* bias, void* out,
                      long long rows, int dim, int silu_act) {
     constexpr int H = W - 1;
+    grid_dep_launch();  // programmatic dependent launch, as in conv1d_vec_kernel
+    grid_dep_wait();
     const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (row >= rows) return;
     const int d = static_cast<int>(row % dim);

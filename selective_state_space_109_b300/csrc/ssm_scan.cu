@@ -964,6 +964,23 @@ ssm_status_t static_scratch_address(void** out) {
 // Short causal convolution in front of the scan
 // ---------------------------------------------------------------------------
 
+// Launches a kernel with programmatic dependent launch (the kernel calls
+// grid_dep_launch / grid_dep_wait): its launch overlaps the previous kernel's
+// tail in the stream.  Errors surface through cudaGetLastError.
+template <typename... KArgs, typename... Args>
+void launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = st;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    (void)cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 template <typename T>
 cudaError_t launch_conv_t(const ssm::ConvParams& p, int width, cudaStream_t st) {
     const int es = static_cast<int>(sizeof(T));
@@ -976,9 +993,9 @@ cudaError_t launch_conv_t(const ssm::ConvParams& p, int width, cudaStream_t st) 
         constexpr int W = decltype(wc)::value;
         if (vec) {
             if (p.rows * (p.seqlen / (16 / es)) < (1LL << 31))
-                ssm::conv1d_vec_kernel<T, W, unsigned><<<grid, 256, 0, st>>>(p);
+                launch_pdl(ssm::conv1d_vec_kernel<T, W, unsigned>, grid, 256, st, p);
             else
-                ssm::conv1d_vec_kernel<T, W, unsigned long long><<<grid, 256, 0, st>>>(p);
+                launch_pdl(ssm::conv1d_vec_kernel<T, W, unsigned long long>, grid, 256, st, p);
         } else {
             ssm::conv1d_elem_kernel<T, W><<<grid, 256, 0, st>>>(p);
             if (p.x_last && W > 1)
@@ -1000,10 +1017,10 @@ cudaError_t launch_conv_update_t(void* state, const void* x, const float* w, con
                                  long long rows, int dim, int width, int silu_act, cudaStream_t st) {
     const unsigned grid = static_cast<unsigned>((rows + 255) / 256);
     switch (width) {
-        case 1: ssm::conv1d_update_kernel<T, 1><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
-        case 2: ssm::conv1d_update_kernel<T, 2><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
-        case 3: ssm::conv1d_update_kernel<T, 3><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
-        case 4: ssm::conv1d_update_kernel<T, 4><<<grid, 256, 0, st>>>(state, x, w, bias, out, rows, dim, silu_act); break;
+        case 1: launch_pdl(ssm::conv1d_update_kernel<T, 1>, grid, 256, st, state, x, w, bias, out, rows, dim, silu_act); break;
+        case 2: launch_pdl(ssm::conv1d_update_kernel<T, 2>, grid, 256, st, state, x, w, bias, out, rows, dim, silu_act); break;
+        case 3: launch_pdl(ssm::conv1d_update_kernel<T, 3>, grid, 256, st, state, x, w, bias, out, rows, dim, silu_act); break;
+        case 4: launch_pdl(ssm::conv1d_update_kernel<T, 4>, grid, 256, st, state, x, w, bias, out, rows, dim, silu_act); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
