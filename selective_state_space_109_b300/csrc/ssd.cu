@@ -123,7 +123,18 @@ extern "C" ssm_status_t ssm_ssd_fwd(const void* x, const void* delta, const void
     }
     const long long grid = static_cast<long long>(batch) * nheads;
     if (grid > 0x7fffffffLL) return SSM_ERR_INVALID_ARG;
-    ssm::ssd_fwd_kernel<<<static_cast<unsigned>(grid), ssm::ssd::THREADS, ssm::ssd::SMEM_BYTES, st>>>(mx, mb, mc, mz, my, p);
-    const cudaError_t e = cudaGetLastError();
+    // Launched with programmatic stream serialization, so that its launch
+    // overlaps the tail of the previous kernel in the stream.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(ssm::ssd::THREADS);
+    cfg.dynamicSmemBytes = ssm::ssd::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, ssm::ssd_fwd_kernel, mx, mb, mc, mz, my, p);
     return e == cudaSuccess ? SSM_OK : ssm_note_cuda_error(e);
 }

@@ -263,6 +263,10 @@ ssd_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_z,
                const __grid_constant__ CUtensorMap tm_y, const SsdParams p) {
     using namespace ssd;
+    // Programmatic dependent launch: the next kernel may begin launching now;
+    // this one waits for the previous kernel's writes before reading anything.
+    grid_dep_launch();
+    grid_dep_wait();
     extern __shared__ __align__(16) unsigned char smem_raw[];  // aligned below at run time
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     unsigned char* Cs = smem + CS_OFF;
