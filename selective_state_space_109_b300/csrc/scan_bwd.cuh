@@ -491,10 +491,19 @@ struct BwdLayout {
     static constexpr int BYTES = OUTS + 3 * Sh::CH * (TT + 1) * 4;
 };
 
-// Three CTAs per SM: at four the register cap (128) spills the tile's
-// recomputed states, which measured 40% slower on B300.
+// Three CTAs per SM at most: at four the register cap (128) spills the
+// tile's recomputed states, which measured 40% slower on B300.  Where the
+// shared-memory footprint leaves fewer resident CTAs (N = 256: one), the
+// bound follows it, so the registers that occupancy leaves free hold the
+// 8 states a lane instead of spilling them.
+template <typename T, int N>
+constexpr int bwd_min_blocks() {
+    constexpr int b = (228 * 1024) / (BwdLayout<T, N>::BYTES + 1024);
+    return b < 1 ? 1 : (b > 3 ? 3 : b);
+}
+
 template <typename T, int N, bool ACCURATE>
-__global__ void __launch_bounds__(kBwdWarps * 32, 3)
+__global__ void __launch_bounds__(kBwdWarps * 32, (bwd_min_blocks<T, N>()))
 scan_bwd_kernel(const BwdParams p) {
     using Sh = BwdShape<N>;
     using Lay = BwdLayout<T, N>;
