@@ -94,6 +94,16 @@ def test_bwd_lengths(ssm, L):
         check(got, ref, io, f"L={L} io={io}")
 
 
+@pytest.mark.parametrize("N", [128, 256])
+def test_bwd_odd_length_large_state(ssm, N):
+    """An odd length at the large state sizes: scalar dB/dC adds, a ragged
+    last tile (its padded steps must add nothing to the dB/dC staging that
+    later tiles reuse), several chunks of 64 steps."""
+    for io in ("f32", "bf16"):
+        got, ref = run_case(ssm, 1, 40, N, 203, 1, io, seed=N + 203)
+        check(got, ref, io, f"N={N} L=203 io={io}")
+
+
 def test_bwd_empty_sequence(ssm):
     x = I.make_scan_inputs(2, 16, 16, 0, 1, io="f32", seed=3, device="cuda", with_h0=True)
     dhf = torch.randn((2, 16, 16), device="cuda")
