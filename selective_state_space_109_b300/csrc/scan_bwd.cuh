@@ -486,8 +486,11 @@ struct BwdLayout {
     static constexpr int SC = BC + 2 * 2 * N * TT * static_cast<int>(sizeof(T));   // float4 [TT][CH]
     static constexpr int SC2 = SC + TT * Sh::CH * 16;                               // float2 [TT][CH]
     static constexpr int BCF = SC2 + TT * Sh::CH * 8;                               // float4 [TT][NQP]
-    static constexpr int RED = BCF + TT * Sh::NQP * 16;                             // float [WARPS][TT][2N]
-    static constexpr int OUTS = RED + kBwdWarps * TT * 2 * N * 4;                   // float [3][CH][TT + 1]
+    // dB/dC staging per warp: the whole tile, or at N = 256 (512 values a
+    // step) half of it, flushed twice a tile, so that two CTAs fit on an SM.
+    static constexpr int RED_STEPS = N >= 256 ? TT / 2 : TT;
+    static constexpr int RED = BCF + TT * Sh::NQP * 16;                             // float [WARPS][RED_STEPS][2N]
+    static constexpr int OUTS = RED + kBwdWarps * RED_STEPS * 2 * N * 4;            // float [3][CH][TT + 1]
     static constexpr int BYTES = OUTS + 3 * Sh::CH * (TT + 1) * 4;
 };
 
@@ -521,7 +524,8 @@ scan_bwd_kernel(const BwdParams p) {
     float2 (*sc2)[CH] = reinterpret_cast<float2 (*)[CH]>(smem + Lay::SC2);
     using Bcf = BwdBcf<T>;
     typename Bcf::type (*bcf)[Sh::NQP] = reinterpret_cast<typename Bcf::type (*)[Sh::NQP]>(smem + Lay::BCF);
-    float (*red)[TT][2 * N] = reinterpret_cast<float (*)[TT][2 * N]>(smem + Lay::RED);
+    constexpr int TR = Lay::RED_STEPS;
+    float (*red)[TR][2 * N] = reinterpret_cast<float (*)[TR][2 * N]>(smem + Lay::RED);
     float (*outs)[CH][TT + 1] = reinterpret_cast<float (*)[CH][TT + 1]>(smem + Lay::OUTS);
 
     const BwdLane l = bwd_lane<N>(p);
@@ -685,6 +689,43 @@ scan_bwd_kernel(const BwdParams p) {
             ys[t] = fmaf(dsk, q.w, lane_sum<LN>(y2.x + y2.y));
         }
 
+        // dB, dC of steps tb .. tb + TR - 1 of the tile: sum over warps, one
+        // atomic add per CTA -- four steps per vector add when the rows keep
+        // 16-byte alignment.
+        auto flush_red = [&](int tb) {
+            if (L % 4 == 0) {
+                for (int e = threadIdx.x; e < 2 * N * (TR / 4); e += THREADS) {
+                    const int t = (e % (TR / 4)) * 4;
+                    const int k = e / (TR / 4);  // tensor * N + n
+                    if (t0 + tb + t < L) {
+                        float v[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            v[q] = 0.f;
+#pragma unroll
+                            for (int w = 0; w < kBwdWarps; ++w) v[q] += red[w][t + q][k];
+                        }
+                        float* dst = ((k / N) ? p.dC : p.dB) + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + tb + t;
+                        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v[0]), "f"(v[1]),
+                                     "f"(v[2]), "f"(v[3])
+                                     : "memory");
+                    }
+                }
+            } else {
+                for (int e = threadIdx.x; e < 2 * N * TR; e += THREADS) {
+                    const int t = e % TR;
+                    const int k = e / TR;  // tensor * N + n
+                    if (t0 + tb + t < L) {
+                        float v = 0.f;
+#pragma unroll
+                        for (int w = 0; w < kBwdWarps; ++w) v += red[w][t][k];
+                        float* dst = (k / N) ? p.dC : p.dB;
+                        atomicAdd(dst + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + tb + t, v);
+                    }
+                }
+            }
+        };
+
         // The adjoint, backwards over the tile.
 #pragma unroll
         for (int t = TT - 1; t >= 0; --t) {
@@ -727,45 +768,20 @@ scan_bwd_kernel(const BwdParams p) {
 #pragma unroll
                 for (int qq = 0; qq < Sh::CF; ++qq) {
                     const int id = xid0 + qq;
-                    red[l.warp][t][(id / S) * N + l.j * S + id % S] = vals[qq];
+                    red[l.warp][t % TR][(id / S) * N + l.j * S + id % S] = vals[qq];
+                }
+            }
+            if constexpr (TR < TT) {
+                if (t % TR == 0 && t > 0) {  // the upper steps' staging is full: flush it
+                    __syncthreads();
+                    flush_red(t);
+                    __syncthreads();
                 }
             }
         }
         __syncthreads();
 
-        // dB, dC of the tile: sum over warps, one atomic add per CTA -- four
-        // steps per vector add when the rows keep 16-byte alignment.
-        if (L % 4 == 0) {
-            for (int e = threadIdx.x; e < 2 * N * (TT / 4); e += THREADS) {
-                const int t = (e % (TT / 4)) * 4;
-                const int k = e / (TT / 4);  // tensor * N + n
-                if (t0 + t < L) {
-                    float v[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        v[q] = 0.f;
-#pragma unroll
-                        for (int w = 0; w < kBwdWarps; ++w) v[q] += red[w][t + q][k];
-                    }
-                    float* dst = ((k / N) ? p.dC : p.dB) + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + t;
-                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v[0]), "f"(v[1]),
-                                 "f"(v[2]), "f"(v[3])
-                                 : "memory");
-                }
-            }
-        } else {
-            for (int e = threadIdx.x; e < 2 * N * TT; e += THREADS) {
-                const int t = e % TT;
-                const int k = e / TT;  // tensor * N + n
-                if (t0 + t < L) {
-                    float v = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kBwdWarps; ++w) v += red[w][t][k];
-                    float* dst = (k / N) ? p.dC : p.dB;
-                    atomicAdd(dst + (static_cast<long long>(l.bg) * N + k % N) * L + t0 + t, v);
-                }
-            }
-        }
+        flush_red(0);
         // du, ddelta, dz rows of the tile.
         {
             constexpr int VP = 16 / static_cast<int>(sizeof(T));
