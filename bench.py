@@ -585,7 +585,8 @@ def bench_ssd(ssm, I, torch, peaks, name="ssd_bf16_b2_h64_p64_n128_l2048"):
                        kernel="ssd_fwd_kernel (tcgen05.mma, TMEM accumulators, TMA)")}
 
 
-def bench_bwd(ssm, I, torch, peaks, names=("scan_bf16_b2_d1536_l2048", "scan_bf16_b8_d2048_l4096")):
+def bench_bwd(ssm, I, torch, peaks, names=("scan_bf16_b2_d1536_l2048", "scan_bf16_b8_d2048_l4096",
+                                           "scan_bf16_b2_d1536_l2048_n256")):
     """Backward pass (every gradient, no final-state gradient) on the scan
     shapes: device time per call over rotating inputs (> 3x L2)."""
     dev = torch.device("cuda")
