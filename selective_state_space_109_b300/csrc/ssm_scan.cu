@@ -338,6 +338,20 @@ ScanPlan plan_scan(int batch, int dim, int dstate, int seqlen, int ngroups, ssm_
     // against 2407 and 2618), where the cost model above preferred 2 lanes
     // for the first.
     if (best.chunks > 1 && dstate <= 16) best.agg_lanes = lmin;
+    // At 16 lanes a channel (N = 256) the model prices the summary pass like
+    // the fused pass, but it has no readout to reduce across the 16 lanes.
+    // When one pass would leave SMs short of three resident CTAs (the fused
+    // pass's 148 registers allow three), a split into three chunks measured
+    // best: b2 d1536 L2048 bf16, 872 us against 938 us in one pass (884 at
+    // two chunks, 903 at four, 878 at six).
+    if (dstate >= 256 && io != SSM_F32 && best.chunks == 1 && kmax >= 3) {
+        const int ch = kTmaWarps * 32 / best.lanes;
+        const long long blocks = static_cast<long long>((dpg + ch - 1) / ch) * ngroups * batch;
+        if (blocks < 3LL * kPlanSms) {
+            best.chunks = 3;
+            best.agg_lanes = best.lanes;
+        }
+    }
     const int fl = env_int("SSM_FORCE_LANES", 0);
     if ((fl == 1 || fl == 2 || fl == 4) && fl <= lmax && fl >= lmin) best.lanes = fl;
     const int fk = env_int("SSM_FORCE_CHUNKS", 0);

@@ -21,7 +21,7 @@ def ssm():
     ((2, 1536, 32, 2048), 2, 12),
     ((2, 1536, 64, 2048), 4, 6),
     ((2, 1536, 128, 2048), 8, 1),
-    ((2, 1536, 256, 2048), 16, 1),
+    ((2, 1536, 256, 2048), 16, 3),    # 872 us against 938 us in one pass
 ])
 def test_plans_of_the_measured_workloads(ssm, shape, lanes, chunks):
     b, d, n, L = shape
